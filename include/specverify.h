@@ -1,0 +1,219 @@
+/*
+ * specverify.h -- C ABI of libspecverify, the GB300 (sm_103a) verify-and-accept
+ * hot path of multi-token-prediction (MTP) speculative decoding.
+ *
+ * One speculative cycle, as the pages describe it ("MTPLX 2.24x faster TPS",
+ * section "Layer 2: Speculative cycle (the hot loop)"): the drafter proposes K
+ * tokens; the target model verifies all of them in one batched forward over
+ * M = K+1 rows (the last committed token plus the K drafts -- "MTP in
+ * llama.cpp", section "How speculative decoding works"); a probability-ratio
+ * test accepts a prefix; a rejection emits one replacement from the residual
+ * (p - q)+; a full acceptance emits a bonus token; the GatedDeltaNet state is
+ * committed by replaying the innovation tape over the accepted prefix.
+ *
+ * This library provides the data-parallel steps of that cycle:
+ *   qmv_smallm        the target's 4-bit small-M quantised mat-vec (M = 1..8)
+ *   spec_accept       fp32 acceptance, residual resampling and bonus token
+ *   gdn_tape_capture  GatedDeltaNet recurrence over the verify tokens, with a
+ *                     (gate, innovation, key) tape per token and head
+ *   gdn_tape_replay   rebuild the recurrent state over an accepted prefix
+ *
+ * Conventions (all entry points):
+ *  - Every tensor argument is a DEVICE pointer owned by the caller, to
+ *    contiguous row-major memory.  The library keeps no pointer after a call
+ *    returns and allocates no device memory.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream) and
+ *    never synchronise with the host.
+ *  - Arguments are validated on the host before any launch.  A nonzero status
+ *    means nothing was launched (SV_ERR_CUDA: the launch itself failed).
+ *    sv_last_error() returns a thread-local message for the last failure.
+ *  - Data-dependent problems found on the device (a draft token out of range,
+ *    a NaN logit, ...) never trap: they are reported in per-sequence flag
+ *    words and the result stays well defined (see spec_accept).
+ *  - No C++ exception crosses this boundary.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SV_ABI_VERSION 1
+
+/* A CUDA stream (cudaStream_t); NULL selects the legacy default stream. */
+typedef struct CUstream_st *sv_stream_t;
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or value is invalid     */
+    SV_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement   */
+    SV_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed        */
+    SV_ERR_DEVICE_FLAG = 4  /* sv_device_status: a kernel hit a bounded-wait limit */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Per-sequence error flag bits written by spec_accept (err_flags) and
+ * gdn_tape_replay. */
+#define SV_FLAG_DRAFT_OUT_OF_RANGE 1 /* draft token not in [0, V): rejected          */
+#define SV_FLAG_DRAFT_ZERO_Q 2       /* q(d) == 0, the draft could not have been drawn */
+#define SV_FLAG_NONFINITE_LOGIT 4    /* a NaN or +inf logit in a row that was used   */
+#define SV_FLAG_EMPTY_DIST 8         /* nothing to sample from: token -1 emitted     */
+#define SV_FLAG_REPLAY_RANGE 16      /* gdn_tape_replay: record count clamped to [0,T] */
+
+int sv_abi_version(void);
+const char *sv_status_string(int status);
+/* Message describing the most recent failure on the calling thread ("" if none). */
+const char *sv_last_error(void);
+
+/* Programmatic dependent launch (PDL) for qmv_smallm, process-wide, default 0.
+ * When enabled, a qmv_smallm kernel may start while the kernel enqueued
+ * before it on the same stream is still running, and may read w_packed,
+ * scales and biases before that kernel has finished (x is read, and y
+ * written, only after it has).  Enable it only when no kernel enqueued right
+ * before a qmv_smallm call writes that call's weights. */
+void sv_set_pdl(int enable);
+int sv_get_pdl(void);
+
+/* Reads and clears the device-side error word (synchronises the current
+ * device).  Returns SV_OK, or SV_ERR_DEVICE_FLAG if some kernel gave up on a
+ * bounded wait since the last call (it then returned without a result). */
+sv_status sv_device_status(void);
+
+/* ------------------------------------------------------------------------ */
+/* qmv_smallm: Y[M,N] = X[M,K] . W^T with 4-bit affine group-64 weights.     */
+/* ------------------------------------------------------------------------ */
+/* Source: "MTPLX 2.24x faster TPS", section "Layer 0: MLX Runtime" -- the
+ * verify forward multiplies M = 3..6 rows (one per drafted position) by the
+ * 4-bit weights, a shape stock large-M kernels handle badly; "MTPLX | Apple
+ * Silicon..." (ai-navigate-news), "what I had to solve" item 3 -- MLP
+ * projections took 51 % of verify time before the small-M kernel.
+ *
+ *   W[n,i] = scales[n, i/64] * q[n,i] + biases[n, i/64]
+ *   q[n,i] = (w_packed[n*(K/8) + i/8] >> (4*(i%8))) & 15     (LSB-first)
+ *   y[m*N + n] = sum_i x[m*K + i] * W[n,i]      (fp32 accumulation)
+ *
+ * w_packed  uint32 [N][K/8];  scales, biases: bf16 bit patterns [N][K/64];
+ * x         [M][K], fp32 (SV_F32) or bf16 (SV_BF16);   y: fp32 [M][N].
+ * Requires 1 <= M <= 8 (M == 0 or N == 0: no-op), K > 0, K % 64 == 0,
+ * group_size == 64, bits == 4; w_packed, scales, biases and x 16-byte
+ * aligned; y 4-byte aligned and not overlapping any input.  Each output is a
+ * fixed-order sum (deterministic run to run).  Accuracy: fp32 accumulation
+ * of exact products; fp32 x is split into two bf16 terms (|x - hi - lo| <=
+ * 2^-16 |x|). */
+sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales, const uint16_t *biases,
+                     const void *x, sv_dtype x_dtype, float *y, int M, int N, int K,
+                     int group_size, int bits, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* spec_accept: probability-ratio verification of K drafts per sequence.     */
+/* ------------------------------------------------------------------------ */
+/* Sources: "MTPLX 2.24x faster TPS", sections "Layer 2: Speculative cycle"
+ * (fp32 Leviathan-Chen acceptance per position, (p - q)+ residual on
+ * rejection, bonus token on full acceptance) and "QWEN 3.6 27B @ 63 TPS"
+ * (temperature 0.6, top_p 0.95, top_k 20); "MTP in llama.cpp", section
+ * "lossless" (temperature 0: accept until the first mismatch with the
+ * target's argmax, plus one extra target token).
+ *
+ * Distribution of a logits row z (target p_k, draft q_k):
+ *   z' = z / temperature -> keep the top_k largest (equal values: lower id)
+ *   -> softmax over the kept set -> keep the shortest descending prefix whose
+ *   cumulative probability >= top_p (at least one) -> renormalise.
+ * For k = 1..K: accept d_k iff u_accept[k] < p_k(d_k) / q_k(d_k).  At the
+ * first rejection emit the smallest token id x whose cumulative sum of
+ * R = max(0, p_k - q_k) (in ascending id order) exceeds u_sample * sum(R)
+ * (R = p_k if sum(R) == 0), and stop.  If all K are accepted, emit a bonus
+ * token from p_{K+1} the same way.  temperature == 0: greedy (p_k is the
+ * argmax one-hot, lowest id on ties; draft_logits is not read, may be NULL).
+ *
+ * target_logits fp32 [B][K+1][V]; draft_logits fp32 [B][K][V];
+ * draft_tokens int32 [B][K]; u_accept fp32 [B][K]; u_sample fp32 [B] (uniforms
+ * in [0,1), supplied by the caller).  Outputs: out_tokens int32 [B][K+1]
+ * (accepted drafts, then the emitted token, then -1 padding), n_accepted
+ * int32 [B] in [0,K], err_flags int32 [B] (SV_FLAG_*; may be NULL).
+ * Device-side data errors: a draft outside [0,V) or with q(d) == 0 is
+ * rejected; NaN and +inf logits are never kept (-inf is a mask); a
+ * distribution with no finite logit is empty and emits -1.
+ * Requires B >= 0 (0: no-op), B*(2K+1) <= 65535, 1 <= K <= 8,
+ * 1 <= V <= 1048576, all pointers 4-byte aligned (16-byte aligned logits with
+ * V % 4 == 0 use 16-byte loads); temperature finite and >= 0; if
+ * temperature > 0 then 1 <= top_k <= 64 and 0 < top_p <= 1.  No output may
+ * overlap an input or another output.
+ * workspace: device memory of spec_accept_workspace_bytes(B, K, V) bytes,
+ * 16-byte aligned, zero-filled before its first use; each completed call
+ * leaves it ready for the next.  Calls that run concurrently must use
+ * different workspaces. */
+typedef struct {
+    float temperature; /* 0 => greedy */
+    int top_k;         /* 1..64 (ignored when temperature == 0) */
+    float top_p;       /* (0, 1]; 1 disables */
+} sv_sampling;
+
+size_t spec_accept_workspace_bytes(int B, int K, int V);
+
+sv_status spec_accept(const float *target_logits, const float *draft_logits,
+                      const int32_t *draft_tokens, const float *u_accept, const float *u_sample,
+                      int B, int K, int V, sv_sampling sampling, int32_t *out_tokens,
+                      int32_t *n_accepted, int32_t *err_flags, void *workspace,
+                      size_t workspace_bytes, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* GatedDeltaNet innovation tape.                                            */
+/* ------------------------------------------------------------------------ */
+/* Sources: "MTPLX 2.24x faster TPS", section "Layer 0: MLX Runtime"
+ * (innovation-tape GDN capture: KB-scale (token, gate, state-delta) tuples;
+ * a rejection replays the tape instead of restoring a state snapshot, bit
+ * exact); "MTP와 DFlash" (mlxcel manual), section "Qwen3.8-Flash-Next
+ * (qwen4_exp) MTP" (rollback replays the GatedDeltaNet recurrence over the
+ * accepted tokens).  The update is the gated delta rule, per (b, h) with
+ * S in R^{dv x dk}, in this order (fp32, no fused multiply-add in the state
+ * update):
+ *     S' = alpha_t * S;   u = S' k_t;   e_t = beta_t * (v_t - u);
+ *     S_t = S' + e_t k_t^T;   o_t = S_t q_t.
+ * Tape record (b,t,h) = (alpha_t, e_t, k_t).  Tape layout, fp32, in one
+ * buffer of gdn_tape_bytes(B,T,H,dk,dv) bytes: B blocks of
+ * F = T*H*(dv+dk) + 4*ceil(T*H/4) floats, block b at float offset b*F holding
+ *     e     [T][H][dv]  at float 0
+ *     k     [T][H][dk]  at float T*H*dv
+ *     alpha [T][H]      at float T*H*(dv+dk)   (padded to a multiple of 4)
+ * so the tapes of consecutive batches, stacked, form the tape of the
+ * concatenated batch (one replay launch can commit several layers).
+ * Replaying records t = 0..L-1 applies S[i][j] <- alpha_t*S[i][j] + e_t[i]*k_t[j]
+ * (multiply, multiply, add: the same roundings as the capture), so the state
+ * after replaying L records equals, bit for bit, the capture's state after
+ * its first L tokens.
+ * Shapes: state [B][H][dv][dk]; q, k [B][T][H][dk]; v [B][T][H][dv];
+ * alpha, beta [B][T][H]; out [B][T][H][dv].
+ * Requires B >= 0 (0: no-op), 1 <= T <= 16, H >= 1, dk and dv in [4, 128]
+ * and multiples of 4, all pointers 16-byte aligned, outputs not
+ * overlapping inputs. */
+size_t gdn_tape_bytes(int B, int T, int H, int dk, int dv);
+
+/* Runs the recurrence over T tokens from the snapshot state0 (read only) and
+ * writes the tape; when not NULL, out receives the outputs o_t and state_out
+ * [B][H][dv][dk] the state after all T tokens. */
+sv_status gdn_tape_capture(const float *state0, const float *q, const float *k, const float *v,
+                           const float *alpha, const float *beta, int B, int T, int H, int dk,
+                           int dv, float *out, float *tape, float *state_out, sv_stream_t stream);
+
+/* Applies, in place, the first L_b = n_replay[b % n_replay_count] +
+ * n_replay_bias tape records of every head of state row-block b to state
+ * (L_b clamped to [0,T]; a clamp sets SV_FLAG_REPLAY_RANGE in err_flags[b]
+ * when err_flags != NULL).  n_replay_count in [1, B]: pass B for one count per
+ * sequence, or the number of sequences when state and tape stack several
+ * layers' [B_seq] blocks ([layers][B_seq][...]) that share one accepted
+ * length per sequence.  n_replay is read on the device, so spec_accept's
+ * n_accepted can feed it directly (bias 1 when the tape's first record is the
+ * last committed token).  Blocks with L_b == 0 are not touched. */
+sv_status gdn_tape_replay(float *state, const float *tape, const int32_t *n_replay,
+                          int n_replay_count, int n_replay_bias, int B, int T, int H, int dk,
+                          int dv, int32_t *err_flags, sv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,262 @@
+"""GB300 (sm_103a) verify-and-accept hot path of MTP speculative decoding.
+
+A thin binding over libspecverify's C ABI (``include/specverify.h``): each
+function here has the C entry point's name, checks and marshals torch
+tensors (device, dtype, shape, contiguity) and calls the C function on the
+current CUDA stream.  All arithmetic runs in the library's CUDA kernels; if
+the library is missing, every call raises -- there is no fallback.
+
+  qmv_smallm        4-bit affine group-64 mat-vec over M = 1..8 verify rows
+  spec_accept       fp32 probability-ratio acceptance, residual, bonus token
+  gdn_tape_capture  GatedDeltaNet recurrence + innovation tape
+  gdn_tape_replay   rebuild the recurrent state over an accepted prefix
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+__all__ = [
+    "SvError", "lib", "abi_version", "qmv_smallm", "spec_accept", "spec_accept_workspace_bytes",
+    "make_accept_workspace", "gdn_tape_bytes", "gdn_tape_capture", "gdn_tape_replay",
+    "set_pdl", "get_pdl", "device_status", "FLAGS",
+]
+
+_LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_DEVICE_FLAG = range(5)
+SV_F32, SV_BF16 = 0, 1
+FLAGS = {"draft_out_of_range": 1, "draft_zero_q": 2, "nonfinite_logit": 4, "empty_dist": 8,
+         "replay_range": 16}
+
+
+class SvError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        super().__init__(f"{where}: {message} (status {status})")
+        self.status = status
+
+
+class _Sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int),
+                ("top_p", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libspecverify; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not _LIB_PATH.exists():
+            raise RuntimeError(
+                f"{_LIB_PATH.name} is not built; run `python -m "
+                "mtp_speculative_decoding_qmv_gb300.build` (or __graft_entry__.build())")
+        L = ctypes.CDLL(str(_LIB_PATH))
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.sv_abi_version.restype = I
+        L.sv_status_string.restype = ctypes.c_char_p
+        L.sv_status_string.argtypes = [I]
+        L.sv_last_error.restype = ctypes.c_char_p
+        L.sv_set_pdl.argtypes = [I]
+        L.sv_get_pdl.restype = I
+        L.sv_device_status.restype = I
+        L.qmv_smallm.argtypes = [P, P, P, P, I, P, I, I, I, I, I, P]
+        L.qmv_smallm.restype = I
+        L.spec_accept_workspace_bytes.argtypes = [I, I, I]
+        L.spec_accept_workspace_bytes.restype = Z
+        L.spec_accept.argtypes = [P, P, P, P, P, I, I, I, _Sampling, P, P, P, P, Z, P]
+        L.spec_accept.restype = I
+        L.gdn_tape_bytes.argtypes = [I, I, I, I, I]
+        L.gdn_tape_bytes.restype = Z
+        L.gdn_tape_capture.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P]
+        L.gdn_tape_capture.restype = I
+        L.gdn_tape_replay.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P]
+        L.gdn_tape_replay.restype = I
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != SV_OK:
+        msg = lib().sv_last_error().decode() or lib().sv_status_string(status).decode()
+        raise SvError(status, where, msg)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def abi_version() -> int:
+    return lib().sv_abi_version()
+
+
+def set_pdl(enable: bool) -> None:
+    """Programmatic dependent launch for qmv_smallm (see specverify.h)."""
+    lib().sv_set_pdl(1 if enable else 0)
+
+
+def get_pdl() -> bool:
+    return bool(lib().sv_get_pdl())
+
+
+def device_status() -> None:
+    """Synchronises and raises SvError if a kernel gave up on a bounded wait."""
+    _check(lib().sv_device_status(), "sv_device_status")
+
+
+# ----------------------------------------------------------------------------
+def qmv_smallm(w_packed: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+               x: torch.Tensor, y: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M, N] (fp32) = x[M, K] . W^T.
+
+    w_packed int32/uint32 view [N, K/8]; scales, biases bf16 [N, K/64] (or
+    int16 bit patterns); x fp32 or bf16 [M, K].
+    """
+    dev = w_packed.device
+    N, K8 = w_packed.shape
+    K = K8 * 8
+    M = x.shape[0]
+    wdt = w_packed.dtype
+    if wdt not in (torch.int32, torch.uint32):
+        raise TypeError("w_packed must be int32 or uint32")
+    _need(w_packed, "w_packed", wdt, (N, K8), dev)
+    sdt = scales.dtype
+    if sdt not in (torch.bfloat16, torch.int16):
+        raise TypeError("scales must be bfloat16 (or int16 bit patterns)")
+    _need(scales, "scales", sdt, (N, K // 64), dev)
+    _need(biases, "biases", sdt, (N, K // 64), dev)
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be float32 or bfloat16")
+    _need(x, "x", x.dtype, (M, K), dev)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, (M, N), dev)
+    st = lib().qmv_smallm(_ptr(w_packed), _ptr(scales), _ptr(biases), _ptr(x),
+                          SV_BF16 if x.dtype == torch.bfloat16 else SV_F32, _ptr(y),
+                          M, N, K, 64, 4, _stream(dev))
+    _check(st, "qmv_smallm")
+    return y
+
+
+def spec_accept_workspace_bytes(B: int, K: int, V: int) -> int:
+    return int(lib().spec_accept_workspace_bytes(B, K, V))
+
+
+def make_accept_workspace(B: int, K: int, V: int, device) -> torch.Tensor:
+    """A zero-filled workspace (uint8) for spec_accept at these sizes."""
+    n = spec_accept_workspace_bytes(B, K, V)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor | None,
+                draft_tokens: torch.Tensor, u_accept: torch.Tensor, u_sample: torch.Tensor,
+                temperature: float, top_k: int, top_p: float,
+                workspace: torch.Tensor | None = None, out_tokens: torch.Tensor | None = None,
+                n_accepted: torch.Tensor | None = None, err_flags: torch.Tensor | None = None):
+    """Returns (out_tokens [B, K+1] int32, n_accepted [B] int32, err_flags [B] int32)."""
+    dev = target_logits.device
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    _need(target_logits, "target_logits", torch.float32, (B, K + 1, V), dev)
+    if draft_logits is not None:
+        _need(draft_logits, "draft_logits", torch.float32, (B, K, V), dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
+    _need(u_accept, "u_accept", torch.float32, (B, K), dev)
+    _need(u_sample, "u_sample", torch.float32, (B,), dev)
+    if workspace is None:
+        workspace = make_accept_workspace(B, K, V, dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if err_flags is None:
+        err_flags = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
+    _need(n_accepted, "n_accepted", torch.int32, (B,), dev)
+    _need(err_flags, "err_flags", torch.int32, (B,), dev)
+    samp = _Sampling(float(temperature), int(top_k), float(top_p))
+    st = lib().spec_accept(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
+                           _ptr(u_accept), _ptr(u_sample), B, K, V, samp, _ptr(out_tokens),
+                           _ptr(n_accepted), _ptr(err_flags), _ptr(workspace),
+                           workspace.numel(), _stream(dev))
+    _check(st, "spec_accept")
+    return out_tokens, n_accepted, err_flags
+
+
+def gdn_tape_bytes(B: int, T: int, H: int, dk: int, dv: int) -> int:
+    return int(lib().gdn_tape_bytes(B, T, H, dk, dv))
+
+
+def gdn_tape_capture(state0: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                     alpha: torch.Tensor, beta: torch.Tensor, tape: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None, want_out: bool = True,
+                     state_out: torch.Tensor | None = None):
+    """Returns (out [B,T,H,dv] fp32 or None, tape fp32 flat); ``state_out``
+    [B,H,dv,dk], when given, receives the state after all T tokens."""
+    dev = state0.device
+    B, H, dv, dk = state0.shape
+    T = q.shape[1]
+    _need(state0, "state0", torch.float32, (B, H, dv, dk), dev)
+    _need(q, "q", torch.float32, (B, T, H, dk), dev)
+    _need(k, "k", torch.float32, (B, T, H, dk), dev)
+    _need(v, "v", torch.float32, (B, T, H, dv), dev)
+    _need(alpha, "alpha", torch.float32, (B, T, H), dev)
+    _need(beta, "beta", torch.float32, (B, T, H), dev)
+    n = gdn_tape_bytes(B, T, H, dk, dv) // 4
+    if tape is None:
+        tape = torch.empty(n, dtype=torch.float32, device=dev)
+    _need(tape, "tape", torch.float32, (n,), dev)
+    if out is None and want_out:
+        out = torch.empty((B, T, H, dv), dtype=torch.float32, device=dev)
+    if out is not None:
+        _need(out, "out", torch.float32, (B, T, H, dv), dev)
+    if state_out is not None:
+        _need(state_out, "state_out", torch.float32, (B, H, dv, dk), dev)
+    st = lib().gdn_tape_capture(_ptr(state0), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                B, T, H, dk, dv, _ptr(out), _ptr(tape), _ptr(state_out),
+                                _stream(dev))
+    _check(st, "gdn_tape_capture")
+    return out, tape
+
+
+def gdn_tape_replay(state: torch.Tensor, tape: torch.Tensor, n_replay: torch.Tensor, T: int,
+                    n_replay_bias: int = 0, err_flags: torch.Tensor | None = None) -> torch.Tensor:
+    """Replays n_replay[b % len(n_replay)] + bias records of ``tape`` into
+    ``state`` [B, H, dv, dk] in place; returns state."""
+    dev = state.device
+    B, H, dv, dk = state.shape
+    _need(state, "state", torch.float32, (B, H, dv, dk), dev)
+    n = gdn_tape_bytes(B, T, H, dk, dv) // 4
+    _need(tape, "tape", torch.float32, (n,), dev)
+    _need(n_replay, "n_replay", torch.int32, None, dev)
+    if n_replay.dim() != 1:
+        raise ValueError("n_replay must be 1-D")
+    if err_flags is not None:
+        _need(err_flags, "err_flags", torch.int32, (B,), dev)
+    st = lib().gdn_tape_replay(_ptr(state), _ptr(tape), _ptr(n_replay), n_replay.numel(),
+                               int(n_replay_bias), B, T, H, dk, dv, _ptr(err_flags), _stream(dev))
+    _check(st, "gdn_tape_replay")
+    return state

@@ -1,0 +1,323 @@
+// gdn_tape.cu -- GatedDeltaNet innovation tape: capture over the verify tokens
+// and replay over the accepted prefix, sm_103a.
+//
+// Sources: "MTPLX 2.24x faster TPS", section "Layer 0: MLX Runtime"
+// (innovation-tape GDN capture records KB-scale (token, gate, state-delta)
+// tuples; a rejection replays the tape instead of restoring a snapshot, bit
+// exact) and "Layer 2: Speculative cycle" (the tape commits accepted deltas,
+// rolls back rejected ones); "MTP와 DFlash" (mlxcel manual), section
+// "Qwen3.8-Flash-Next (qwen4_exp) MTP" (rollback replays the GatedDeltaNet
+// recurrence over the accepted tokens).
+//
+// Gated delta rule per (sequence b, head h), S in R^{dv x dk} (fp32):
+//   S' = alpha_t S;  u = S' k_t;  e_t = beta_t (v_t - u);  S_t = S' + e_t k_t^T;
+//   o_t = S_t q_t.
+// Rows of S never interact: row i needs only v_t[i] and the shared k_t, q_t,
+// alpha_t, beta_t.  So a CTA owns 64 rows of one head, a thread owns half a
+// row (64 fp32 in registers) and the only reduction is between the two
+// halves of a row (one shuffle).  The state element update is written as
+// separate round-to-nearest multiply, multiply, add (no contraction) in both
+// kernels, so replaying the tape reproduces the capture's states bit for bit.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int kRowsPerCta = 64;
+constexpr int kThreads = 2 * kRowsPerCta;
+constexpr int kHalf = 64;          // columns per thread
+constexpr int kPadHalf = kHalf + 4;  // smem stride between the two column halves
+constexpr int kMaxT = 16;
+
+// Tape: one block per sequence b of tape_block_floats(T,H,dk,dv) floats, each
+// block holding e [T][H][dv], then k [T][H][dk], then alpha [T][H] (padded to
+// 4 floats).  Stacking the tapes of several batches gives the tape of the
+// concatenated batch.
+__host__ __device__ inline size_t tape_block_floats(int T, int H, int dk, int dv) {
+  return (size_t)T * H * (dv + dk) + (((size_t)T * H + 3) / 4) * 4;
+}
+struct TapeView {
+  float *base;
+  size_t blk;
+  int T, H, dk, dv;
+  __device__ float *e(int b, int t, int h) const {
+    return base + b * blk + ((size_t)t * H + h) * dv;
+  }
+  __device__ float *k(int b, int t, int h) const {
+    return base + b * blk + (size_t)T * H * dv + ((size_t)t * H + h) * dk;
+  }
+  __device__ float *alpha(int b, int t, int h) const {
+    return base + b * blk + (size_t)T * H * (dv + dk) + (size_t)t * H + h;
+  }
+};
+
+struct GdnArgs {
+  const float *state0;  // capture: snapshot (read only)
+  float *state;         // replay: in/out
+  const float *q, *k, *v, *alpha, *beta;
+  float *out;
+  float *state_out;  // capture: S_T (may be null)
+  TapeView tape;
+  const int32_t *n_replay;
+  int n_replay_count;
+  int n_replay_bias;
+  int32_t *err_flags;
+  int B, T, H, dk, dv;
+};
+
+__device__ __forceinline__ int pad_col(int j) { return j < kHalf ? j : j + (kPadHalf - kHalf); }
+
+
+__global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) {
+  __shared__ __align__(16) float ks[2 * kPadHalf];
+  __shared__ __align__(16) float qs[2 * kPadHalf];
+  const int tid = threadIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int i = blockIdx.x * kRowsPerCta + (tid >> 1);  // state row (value dim)
+  const int half = tid & 1;
+  const int j0 = half * kHalf;
+  const bool row_ok = i < a.dv;
+  const int ncol = max(0, min(kHalf, a.dk - j0));  // valid columns, multiple of 4
+
+  float S[kHalf];
+  const float *src = a.state0 + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk + j0;
+#pragma unroll
+  for (int c = 0; c < kHalf; c += 4) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row_ok && c < ncol) f = *reinterpret_cast<const float4 *>(src + c);
+    S[c] = f.x;
+    S[c + 1] = f.y;
+    S[c + 2] = f.z;
+    S[c + 3] = f.w;
+  }
+
+  for (int t = 0; t < a.T; ++t) {
+    const size_t bth = ((size_t)b * a.T + t) * a.H + h;
+    if (tid < a.dk) {
+      ks[pad_col(tid)] = a.k[bth * a.dk + tid];
+      qs[pad_col(tid)] = a.q[bth * a.dk + tid];
+    }
+    const float al = a.alpha[bth], be = a.beta[bth];
+    const float vi = row_ok ? a.v[bth * a.dv + i] : 0.f;
+    __syncthreads();
+    const float *kh = ks + half * kPadHalf;
+    const float *qh = qs + half * kPadHalf;
+    // S' = alpha S ; u = S' k
+    float u = 0.f;
+#pragma unroll
+    for (int c = 0; c < kHalf; c += 4) {
+      if (c < ncol) {
+        const float4 kk = *reinterpret_cast<const float4 *>(kh + c);
+        S[c] = __fmul_rn(al, S[c]);
+        S[c + 1] = __fmul_rn(al, S[c + 1]);
+        S[c + 2] = __fmul_rn(al, S[c + 2]);
+        S[c + 3] = __fmul_rn(al, S[c + 3]);
+        u = fmaf(S[c], kk.x, u);
+        u = fmaf(S[c + 1], kk.y, u);
+        u = fmaf(S[c + 2], kk.z, u);
+        u = fmaf(S[c + 3], kk.w, u);
+      }
+    }
+    u += __shfl_xor_sync(0xffffffffu, u, 1);
+    const float e = be * (vi - u);
+    // S_t = S' + e k^T ; o = S_t q
+    float o = 0.f;
+#pragma unroll
+    for (int c = 0; c < kHalf; c += 4) {
+      if (c < ncol) {
+        const float4 kk = *reinterpret_cast<const float4 *>(kh + c);
+        const float4 qq = *reinterpret_cast<const float4 *>(qh + c);
+        S[c] = __fadd_rn(S[c], __fmul_rn(e, kk.x));
+        S[c + 1] = __fadd_rn(S[c + 1], __fmul_rn(e, kk.y));
+        S[c + 2] = __fadd_rn(S[c + 2], __fmul_rn(e, kk.z));
+        S[c + 3] = __fadd_rn(S[c + 3], __fmul_rn(e, kk.w));
+        o = fmaf(S[c], qq.x, o);
+        o = fmaf(S[c + 1], qq.y, o);
+        o = fmaf(S[c + 2], qq.z, o);
+        o = fmaf(S[c + 3], qq.w, o);
+      }
+    }
+    o += __shfl_xor_sync(0xffffffffu, o, 1);
+    if (row_ok && half == 0) {
+      a.tape.e(b, t, h)[i] = e;
+      if (a.out) a.out[bth * a.dv + i] = o;
+    }
+    if (blockIdx.x == 0) {
+      if (tid < a.dk) a.tape.k(b, t, h)[tid] = ks[pad_col(tid)];
+      if (tid == 0) *a.tape.alpha(b, t, h) = al;
+    }
+    __syncthreads();
+  }
+  if (a.state_out && row_ok) {
+    float *dst = a.state_out + (((size_t)b * a.H + h) * a.dv + i) * a.dk + j0;
+#pragma unroll
+    for (int c = 0; c < kHalf; c += 4)
+      if (c < ncol)
+        *reinterpret_cast<float4 *>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) gdn_replay_kernel(const GdnArgs a) {
+  __shared__ __align__(16) float ks[kMaxT][2 * kPadHalf];
+  __shared__ float es[kMaxT][kRowsPerCta];
+  __shared__ float als[kMaxT];
+  const int tid = threadIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  int L = a.n_replay[b % a.n_replay_count] + a.n_replay_bias;
+  const bool clamped = L < 0 || L > a.T;
+  L = min(max(L, 0), a.T);
+  if (clamped && a.err_flags && blockIdx.x == 0 && h == 0 && tid == 0)
+    atomicOr(&a.err_flags[b], SV_FLAG_REPLAY_RANGE);
+  if (L == 0) return;  // nothing accepted: the state is untouched
+  const int r0 = blockIdx.x * kRowsPerCta;
+  const int i = r0 + (tid >> 1);
+  const int half = tid & 1;
+  const int j0 = half * kHalf;
+  const bool row_ok = i < a.dv;
+  const int ncol = max(0, min(kHalf, a.dk - j0));
+  for (int t = 0; t < L; ++t) {
+    if (tid < a.dk) ks[t][pad_col(tid)] = a.tape.k(b, t, h)[tid];
+    if (tid < kRowsPerCta) es[t][tid] = r0 + tid < a.dv ? a.tape.e(b, t, h)[r0 + tid] : 0.f;
+    if (tid == 0) als[t] = *a.tape.alpha(b, t, h);
+  }
+  float S[kHalf];
+  float *dst = a.state + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk + j0;
+#pragma unroll
+  for (int c = 0; c < kHalf; c += 4) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row_ok && c < ncol) f = *reinterpret_cast<const float4 *>(dst + c);
+    S[c] = f.x;
+    S[c + 1] = f.y;
+    S[c + 2] = f.z;
+    S[c + 3] = f.w;
+  }
+  __syncthreads();
+  if (!row_ok) return;
+  for (int t = 0; t < L; ++t) {
+    const float al = als[t], et = es[t][tid >> 1];
+    const float *kh = &ks[t][half * kPadHalf];
+#pragma unroll
+    for (int c = 0; c < kHalf; c += 4) {
+      const float4 kk = *reinterpret_cast<const float4 *>(kh + c);
+      S[c] = __fadd_rn(__fmul_rn(al, S[c]), __fmul_rn(et, kk.x));
+      S[c + 1] = __fadd_rn(__fmul_rn(al, S[c + 1]), __fmul_rn(et, kk.y));
+      S[c + 2] = __fadd_rn(__fmul_rn(al, S[c + 2]), __fmul_rn(et, kk.z));
+      S[c + 3] = __fadd_rn(__fmul_rn(al, S[c + 3]), __fmul_rn(et, kk.w));
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < kHalf; c += 4)
+    if (c < ncol) *reinterpret_cast<float4 *>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+}
+
+sv_status validate(const char *who, int B, int T, int H, int dk, int dv) {
+  if (B < 0 || T < 1 || H < 1 || dk < 1 || dv < 1)
+    return fail(SV_ERR_INVALID_ARG, "%s: need B >= 0, T, H, dk, dv >= 1", who);
+  if (T > kMaxT) return fail(SV_ERR_UNSUPPORTED, "%s: T=%d > %d", who, T, kMaxT);
+  if (dk > 2 * kHalf || dv > 2 * kHalf || dk % 4 || dv % 4)
+    return fail(SV_ERR_UNSUPPORTED, "%s: dk, dv must be multiples of 4 and <= 128 (dk=%d dv=%d)",
+                who, dk, dv);
+  if ((long long)H > 65535 || (long long)B > 65535)
+    return fail(SV_ERR_UNSUPPORTED, "%s: B and H must be <= 65535", who);
+  return SV_OK;
+}
+
+}  // namespace
+
+unsigned take_device_error_gdn() { return 0u; }  // no bounded waits in this unit
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t gdn_tape_bytes(int B, int T, int H, int dk, int dv) {
+  if (B < 0 || T < 1 || H < 1 || dk < 1 || dv < 1) return 0;
+  return (size_t)B * tape_block_floats(T, H, dk, dv) * sizeof(float);
+}
+
+extern "C" sv_status gdn_tape_capture(const float *state0, const float *q, const float *k,
+                                      const float *v, const float *alpha, const float *beta,
+                                      int B, int T, int H, int dk, int dv, float *out, float *tape,
+                                      float *state_out, sv_stream_t stream) {
+  clear_error();
+  sv_status st = validate("gdn_tape_capture", B, T, H, dk, dv);
+  if (st != SV_OK) return st;
+  if (B == 0) return SV_OK;
+  if (!state0 || !q || !k || !v || !alpha || !beta || !tape)
+    return fail(SV_ERR_INVALID_ARG, "gdn_tape_capture: null pointer");
+  const void *ptrs[9] = {state0, q, k, v, alpha, beta, out, tape, state_out};
+  for (const void *p : ptrs)
+    if (p && !aligned(p, 16))
+      return fail(SV_ERR_INVALID_ARG, "gdn_tape_capture: pointers must be 16-byte aligned");
+  const size_t n_bth = (size_t)B * T * H;
+  const size_t sb = (size_t)B * H * dv * dk * 4, qkb = n_bth * dk * 4, vb = n_bth * dv * 4,
+               ab = n_bth * 4, tb = gdn_tape_bytes(B, T, H, dk, dv);
+  const void *ins[6] = {state0, q, k, v, alpha, beta};
+  const size_t insb[6] = {sb, qkb, qkb, vb, ab, ab};
+  for (int j = 0; j < 6; ++j)
+    if (overlaps(tape, tb, ins[j], insb[j]) || overlaps(out, vb, ins[j], insb[j]) ||
+        overlaps(state_out, sb, ins[j], insb[j]))
+      return fail(SV_ERR_INVALID_ARG, "gdn_tape_capture: an output overlaps an input");
+  if (overlaps(out, vb, tape, tb) || overlaps(state_out, sb, tape, tb) ||
+      overlaps(state_out, sb, out, vb))
+    return fail(SV_ERR_INVALID_ARG, "gdn_tape_capture: outputs overlap");
+  GdnArgs args = {};
+  args.state0 = state0;
+  args.q = q;
+  args.k = k;
+  args.v = v;
+  args.alpha = alpha;
+  args.beta = beta;
+  args.out = out;
+  args.state_out = state_out;
+  args.tape = TapeView{tape, tape_block_floats(T, H, dk, dv), T, H, dk, dv};
+  args.B = B;
+  args.T = T;
+  args.H = H;
+  args.dk = dk;
+  args.dv = dv;
+  dim3 grid((unsigned)((dv + kRowsPerCta - 1) / kRowsPerCta), (unsigned)H, (unsigned)B);
+  gdn_capture_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+  return check_launch("gdn_tape_capture");
+}
+
+extern "C" sv_status gdn_tape_replay(float *state, const float *tape, const int32_t *n_replay,
+                                     int n_replay_count, int n_replay_bias, int B, int T, int H,
+                                     int dk, int dv, int32_t *err_flags, sv_stream_t stream) {
+  clear_error();
+  sv_status st = validate("gdn_tape_replay", B, T, H, dk, dv);
+  if (st != SV_OK) return st;
+  if (B == 0) return SV_OK;
+  if (!state || !tape || !n_replay)
+    return fail(SV_ERR_INVALID_ARG, "gdn_tape_replay: null pointer");
+  if (n_replay_count < 1 || n_replay_count > B)
+    return fail(SV_ERR_INVALID_ARG, "gdn_tape_replay: n_replay_count=%d outside [1, B=%d]",
+                n_replay_count, B);
+  if (!aligned(state, 16) || !aligned(tape, 16) || !aligned(n_replay, 4) ||
+      (err_flags && !aligned(err_flags, 4)))
+    return fail(SV_ERR_INVALID_ARG, "gdn_tape_replay: misaligned pointer");
+  const size_t sb = (size_t)B * H * dv * dk * 4, tb = gdn_tape_bytes(B, T, H, dk, dv);
+  if (overlaps(state, sb, tape, tb) || overlaps(state, sb, n_replay, (size_t)n_replay_count * 4) ||
+      overlaps(err_flags, (size_t)B * 4, state, sb) || overlaps(err_flags, (size_t)B * 4, tape, tb))
+    return fail(SV_ERR_INVALID_ARG, "gdn_tape_replay: state/flags overlap the tape or counts");
+  GdnArgs args = {};
+  args.state = state;
+  args.tape = TapeView{const_cast<float *>(tape), tape_block_floats(T, H, dk, dv), T, H, dk, dv};
+  args.n_replay = n_replay;
+  args.n_replay_count = n_replay_count;
+  args.n_replay_bias = n_replay_bias;
+  args.err_flags = err_flags;
+  args.B = B;
+  args.T = T;
+  args.H = H;
+  args.dk = dk;
+  args.dv = dv;
+  dim3 grid((unsigned)((dv + kRowsPerCta - 1) / kRowsPerCta), (unsigned)H, (unsigned)B);
+  gdn_replay_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+  return check_launch("gdn_tape_replay");
+}

@@ -1,0 +1,649 @@
+// spec_accept.cu -- fp32 probability-ratio verification of K drafted tokens
+// per sequence, residual resampling and bonus token, sm_103a.
+//
+// Sources: "MTPLX 2.24x faster TPS", sections "Layer 2: Speculative cycle"
+// (Leviathan-Chen acceptance per position in fp32, (p - q)+ residual on the
+// first rejection, bonus token when all K are accepted) and "QWEN 3.6 27B @ 63
+// TPS" (temperature 0.6, top_p 0.95, top_k 20); "MTP in llama.cpp", section
+// "lossless" (temperature 0: accept until the first mismatch with the
+// target's argmax, plus one target token).
+//
+// The distributions are filtered to at most top_k <= 64 tokens, so the only
+// vocabulary-wide work is a top-k per logits row: an HBM-bound read of
+// (2K+1) rows of V fp32 per sequence.  One kernel does everything:
+//  * chunk phase: CTA (chunk, row) reads 16384 logits (coalesced 16-byte
+//    streaming loads), bounds the k-th largest from below by the minimum of
+//    64 (or 32, 16) group maxima, keeps only elements at or above that bound
+//    (typically ~1 % of them), finds the exact top-k among those with a block
+//    radix select on 64-bit keys (ordered float bits, then lower token id),
+//    sorts them and writes them to the workspace;
+//  * the last CTA of a sequence to finish (threadfence + atomic counter, no
+//    spinning) merges the per-chunk lists of each row (one warp per row,
+//    k-way merge) and runs the acceptance for that sequence in one warp:
+//    softmax over the kept logits, top-p cut on the descending order,
+//    u < p/q test, residual (p - q)+ sampled by inverse CDF in ascending
+//    token-id order, bonus token.
+// The workspace counters are reset by the last CTA, so each completed call
+// leaves the workspace ready for the next.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 16384;                  // logits per chunk CTA
+constexpr int kPerThread = kChunk / kThreads;  // 32
+constexpr int kMaxTopK = 64;
+constexpr int kCap = 2048;                     // candidate buffer entries
+constexpr int kMaxChunks = 64;                 // V <= 64 * 16384
+constexpr int kMaxK = 8;
+constexpr int kMaxRows = 2 * kMaxK + 1;
+
+typedef unsigned long long u64;
+
+struct AcceptArgs {
+  const float *tl, *dl;
+  const int32_t *dt;
+  const float *ua, *us;
+  int B, K, V;
+  float temperature;
+  int top_k;
+  float top_p;
+  int32_t *out, *nacc, *flags;
+  u64 *cand;      // [B][rows_max][C][kMaxTopK]
+  int *counters;  // [B]
+  int *rowflags;  // [B][rows_max]
+  int rows;       // rows read per sequence (K+1 greedy, 2K+1 sampling)
+  int rows_max;   // 2K+1 (workspace stride)
+  int C;          // chunks per row
+  int ksel;       // tokens kept per row (1 greedy, top_k otherwise)
+  int vec;        // 16-byte loads allowed
+  int rows_per_wave;
+};
+
+struct WsLayout {
+  size_t rowflags, cand, total;
+};
+__host__ __device__ inline WsLayout ws_layout(int B, int K, int V) {
+  const size_t rows_max = 2 * (size_t)K + 1;
+  const size_t C = ((size_t)V + kChunk - 1) / kChunk;
+  WsLayout L;
+  L.rowflags = ((size_t)B * 4 + 15) / 16 * 16;
+  L.cand = L.rowflags + ((size_t)B * rows_max * 4 + 15) / 16 * 16;
+  L.total = L.cand + (size_t)B * rows_max * C * kMaxTopK * 8;
+  return L;
+}
+
+// ordered key of a logit: larger float -> larger key; 0 marks an excluded
+// element (-inf mask, NaN, +inf; NaN and +inf also raise `nonfinite`)
+__device__ __forceinline__ uint32_t logit_key(float v, int &nonfinite) {
+  uint32_t u = __float_as_uint(v);
+  if ((u & 0x7F800000u) == 0x7F800000u) {
+    if ((u & 0x007FFFFFu) != 0 || (u >> 31) == 0) nonfinite = 1;
+    return 0u;
+  }
+  if ((u & 0x7FFFFFFFu) == 0) u = 0;  // -0 and +0 compare equal
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// composite: key, then the lower token id wins ties
+__device__ __forceinline__ u64 composite(uint32_t key, uint32_t idx) {
+  return ((u64)key << 32) | (u64)(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ int composite_id(u64 c) { return (int)(0xFFFFFFFFu - (uint32_t)c); }
+__device__ __forceinline__ float composite_logit(u64 c) { return key_logit((uint32_t)(c >> 32)); }
+
+struct ChunkSmem {
+  u64 buf[kCap];
+  u64 top[kMaxTopK];
+  unsigned hist[256];
+  uint32_t gmax[64];
+  uint32_t tau;
+  int nc, ntop, done, rem;
+  u64 prefix;
+  int last;
+};
+
+// Exact ksel-th largest among the keys each thread enumerates (all distinct,
+// all nonzero): 8-bit radix passes from the top; stops as soon as the whole
+// bin at the boundary belongs to the top set.  Returns the threshold T such
+// that exactly min(ksel, total) keys are >= T.
+template <class Each>
+__device__ u64 block_select_threshold(ChunkSmem &S, int ksel, Each each) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  u64 prefix = 0, mask = 0;
+  int rem = ksel;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    for (int i = tid; i < 256; i += kThreads) S.hist[i] = 0;
+    __syncthreads();
+    each([&](u64 c) {
+      if ((c & mask) == prefix) atomicAdd(&S.hist[(c >> shift) & 255u], 1u);
+    });
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l ... 248-8l (descending)
+      unsigned cnt[8], s = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cnt[j] = S.hist[255 - 8 * lane - j];
+        s += cnt[j];
+      }
+      unsigned incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const unsigned total = __shfl_sync(0xffffffffu, incl, 31);
+      if (pass == 0 && total <= (unsigned)rem) {  // fewer keys than ksel: keep all
+        if (lane == 0) {
+          S.prefix = 0;
+          S.done = 1;
+          S.rem = 0;
+        }
+      } else {
+        unsigned above = incl - s;
+        int found = -1;
+        unsigned above_at = 0, bin_cnt = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (found < 0 && above < (unsigned)rem && (unsigned)rem <= above + cnt[j]) {
+            found = 255 - 8 * lane - j;
+            above_at = above;
+            bin_cnt = cnt[j];
+          }
+          above += cnt[j];
+        }
+        if (found >= 0) {
+          S.prefix = prefix | ((u64)found << shift);
+          S.rem = rem - (int)above_at;
+          S.done = (bin_cnt == (unsigned)(rem - (int)above_at)) ? 1 : 0;
+        }
+      }
+    }
+    __syncthreads();
+    prefix = S.prefix;
+    mask |= (u64)0xFF << shift;
+    rem = S.rem;
+    const int done = S.done;
+    __syncthreads();
+    if (done) break;
+  }
+  return prefix;
+}
+
+// Filtered distribution of one merged row held by a warp: entry j (sorted by
+// logit, descending) lives in lane j & 31, half j >> 5.
+struct RowDist {
+  int id[2];
+  float p[2];
+  int n;  // entries with nonzero probability (0: empty)
+};
+
+__device__ RowDist row_dist(const u64 *top, int n, float temperature, float top_p) {
+  const int lane = threadIdx.x & 31;
+  RowDist D;
+  D.n = n;
+  float e[2] = {0.f, 0.f};
+  const float zmax = n > 0 ? composite_logit(top[0]) : 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = lane + 32 * h;
+    D.id[h] = -1;
+    if (j < n) {
+      D.id[h] = composite_id(top[j]);
+      e[h] = expf((composite_logit(top[j]) - zmax) / temperature);
+    }
+  }
+  const float S = warp_sum(e[0] + e[1]);
+  D.p[0] = n > 0 ? e[0] / S : 0.f;
+  D.p[1] = n > 0 ? e[1] / S : 0.f;
+  if (n > 0 && top_p < 1.f) {
+    const float c0 = warp_inclusive_scan(D.p[0]);
+    const float t0 = __shfl_sync(0xffffffffu, c0, 31);
+    const float c1 = warp_inclusive_scan(D.p[1]) + t0;
+    const unsigned b0 = __ballot_sync(0xffffffffu, lane < n && c0 >= top_p);
+    const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < n && c1 >= top_p);
+    int cut = n;
+    if (b0) cut = __ffs(b0);
+    else if (b1) cut = 32 + __ffs(b1);
+    const int last = cut - 1;
+    const float mass = __shfl_sync(0xffffffffu, last < 32 ? c0 : c1, last & 31);
+    D.p[0] = lane < cut ? D.p[0] / mass : 0.f;
+    D.p[1] = lane + 32 < cut ? D.p[1] / mass : 0.f;
+    D.n = cut;
+  }
+  return D;
+}
+
+__device__ float dist_lookup(const RowDist &D, int token) {
+  const unsigned hit0 = __ballot_sync(0xffffffffu, D.id[0] == token && D.p[0] > 0.f);
+  const unsigned hit1 = __ballot_sync(0xffffffffu, D.id[1] == token && D.p[1] > 0.f);
+  float v = 0.f;
+  if (hit0) v = __shfl_sync(0xffffffffu, D.p[0], __ffs(hit0) - 1);
+  else if (hit1) v = __shfl_sync(0xffffffffu, D.p[1], __ffs(hit1) - 1);
+  return token >= 0 ? v : 0.f;
+}
+
+// Smallest token id whose running sum of R (ascending id) exceeds u * sum(R);
+// the last token with R > 0 if rounding never crosses; -1 if sum(R) <= 0.
+// ids[h], R[h] as in RowDist; scratch: 64 floats + 64 ints of warp smem.
+__device__ int inverse_cdf_by_id(const int (&ids)[2], const float (&R)[2], float u, float *sR,
+                                 int *sId) {
+  const int lane = threadIdx.x & 31;
+  // rank of each of the 64 slots by (token id, slot); id -1 (unused) sorts last
+  int rank[2] = {0, 0};
+  u64 mykey[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) mykey[h] = ((u64)(uint32_t)ids[h] << 8) | (u64)(lane + 32 * h);
+  for (int src = 0; src < 64; ++src) {
+    const int other = __shfl_sync(0xffffffffu, ids[src >> 5], src & 31);
+    const u64 okey = ((u64)(uint32_t)other << 8) | (u64)src;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) rank[h] += (okey < mykey[h]) ? 1 : 0;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    sR[rank[h]] = (ids[h] >= 0) ? R[h] : 0.f;
+    sId[rank[h]] = ids[h];
+  }
+  __syncwarp();
+  const float r0 = sR[lane], r1 = sR[lane + 32];
+  const float c0 = warp_inclusive_scan(r0);
+  const float t0 = __shfl_sync(0xffffffffu, c0, 31);
+  const float c1 = warp_inclusive_scan(r1) + t0;
+  const float Z = __shfl_sync(0xffffffffu, c1, 31);
+  int result = -1;
+  if (Z > 0.f) {
+    const float thr = u * Z;
+    const unsigned x0 = __ballot_sync(0xffffffffu, r0 > 0.f && c0 > thr);
+    const unsigned x1 = __ballot_sync(0xffffffffu, r1 > 0.f && c1 > thr);
+    int pos = -1;
+    if (x0) pos = __ffs(x0) - 1;
+    else if (x1) pos = 32 + __ffs(x1) - 1;
+    else {  // rounding: take the last entry with mass
+      const unsigned l0 = __ballot_sync(0xffffffffu, r0 > 0.f);
+      const unsigned l1 = __ballot_sync(0xffffffffu, r1 > 0.f);
+      pos = l1 ? 32 + 31 - __clz(l1) : 31 - __clz(l0);
+    }
+    result = sId[pos];
+  }
+  __syncwarp();
+  return result;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  ChunkSmem &S = *reinterpret_cast<ChunkSmem *>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row_g = blockIdx.y;
+  const int b = row_g / a.rows, rloc = row_g % a.rows;
+  const int cx = blockIdx.x;
+  const int K = a.K, V = a.V;
+  const float *row = rloc <= K ? a.tl + ((size_t)b * (K + 1) + rloc) * V
+                               : a.dl + ((size_t)b * K + (rloc - K - 1)) * V;
+  const int base = cx * kChunk;
+  const int ksel = a.ksel;
+
+  // ---- load the chunk and map it to ordered keys ---------------------------
+  uint32_t key[kPerThread];
+  int nonfinite = 0;
+  if (a.vec) {
+#pragma unroll
+    for (int i = 0; i < kPerThread / 4; ++i) {
+      const int e = base + 4 * (tid + kThreads * i);
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool in = e < V;  // V % 4 == 0 on this path
+      if (in) f = __ldcs(reinterpret_cast<const float4 *>(row + e));
+      key[4 * i + 0] = in ? logit_key(f.x, nonfinite) : 0u;
+      key[4 * i + 1] = in ? logit_key(f.y, nonfinite) : 0u;
+      key[4 * i + 2] = in ? logit_key(f.z, nonfinite) : 0u;
+      key[4 * i + 3] = in ? logit_key(f.w, nonfinite) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      const int e = base + tid + kThreads * i;
+      key[i] = e < V ? logit_key(__ldcs(row + e), nonfinite) : 0u;
+    }
+  }
+  auto index_of = [&](int i) -> uint32_t {
+    return a.vec ? (uint32_t)(base + 4 * (tid + kThreads * (i >> 2)) + (i & 3))
+                 : (uint32_t)(base + tid + kThreads * i);
+  };
+
+  // ---- lower bound on the ksel-th largest: min over >= ksel group maxima --
+  uint32_t tmax = 0;
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) tmax = max(tmax, key[i]);
+  const int n_groups = ksel <= 16 ? 16 : (ksel <= 32 ? 32 : 64);
+  const int tpg = kThreads / n_groups;  // 32, 16 or 8 threads per group
+  for (int o = 1; o < tpg; o <<= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+  if ((tid % tpg) == 0) S.gmax[tid / tpg] = tmax;
+  if (tid == 0) S.nc = 0;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t g0 = lane < n_groups ? S.gmax[lane] : 0u;
+    const uint32_t g1 = lane + 32 < n_groups ? S.gmax[lane + 32] : 0u;
+    const int nz = __popc(__ballot_sync(0xffffffffu, g0 != 0)) +
+                   __popc(__ballot_sync(0xffffffffu, g1 != 0));
+    uint32_t mn = 0xFFFFFFFFu;
+    if (g0) mn = min(mn, g0);
+    if (g1) mn = min(mn, g1);
+    for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    if (lane == 0) S.tau = nz >= ksel ? mn : 1u;
+  }
+  __syncthreads();
+  const uint32_t tau = S.tau;
+
+  // ---- keep the candidates at or above the bound ---------------------------
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) cnt += key[i] >= tau ? 1 : 0;
+  int incl = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int wbase = 0;
+  if (lane == 31) wbase = atomicAdd(&S.nc, incl);
+  wbase = __shfl_sync(0xffffffffu, wbase, 31);
+  int pos = wbase + incl - cnt;
+#pragma unroll
+  for (int i = 0; i < kPerThread; ++i) {
+    if (key[i] >= tau) {
+      if (pos < kCap) S.buf[pos] = composite(key[i], index_of(i));
+      ++pos;
+    }
+  }
+  const int any_nonfinite = __syncthreads_or(nonfinite);
+  const int nc = S.nc;
+
+  // ---- exact top-ksel of the chunk -----------------------------------------
+  u64 thr;
+  if (nc <= kCap) {
+    thr = block_select_threshold(S, ksel, [&](auto f) {
+      for (int i = tid; i < nc; i += kThreads) f(S.buf[i]);
+    });
+    if (tid == 0) S.ntop = 0;
+    __syncthreads();
+    for (int i = tid; i < nc; i += kThreads) {
+      const u64 c = S.buf[i];
+      if (c >= thr) S.top[atomicAdd(&S.ntop, 1)] = c;
+    }
+  } else {  // many ties / a flat row: select over the whole chunk
+    thr = block_select_threshold(S, ksel, [&](auto f) {
+#pragma unroll
+      for (int i = 0; i < kPerThread; ++i)
+        if (key[i]) f(composite(key[i], index_of(i)));
+    });
+    if (tid == 0) S.ntop = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      if (key[i]) {
+        const u64 c = composite(key[i], index_of(i));
+        if (c >= thr) S.top[atomicAdd(&S.ntop, 1)] = c;
+      }
+    }
+  }
+  __syncthreads();
+  const int ntop = S.ntop;
+  // sort descending by rank (keys are distinct) and publish
+  u64 mine = 0;
+  int rank = 0;
+  if (tid < ntop) {
+    mine = S.top[tid];
+    for (int j = 0; j < ntop; ++j) rank += S.top[j] > mine ? 1 : 0;
+  }
+  u64 *dst = a.cand + ((size_t)b * a.rows_max + rloc) * (size_t)a.C * kMaxTopK +
+             (size_t)cx * kMaxTopK;
+  if (tid < ntop) dst[rank] = mine;
+  else if (tid < ksel) dst[tid] = 0;  // empty slots
+  if (tid == 0 && any_nonfinite) atomicOr(&a.rowflags[b * a.rows_max + rloc], SV_FLAG_NONFINITE_LOGIT);
+
+  // ---- the last CTA of this sequence finishes it ---------------------------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) S.last = atomicAdd(&a.counters[b], 1) == a.rows * a.C - 1;
+  __syncthreads();
+  if (!S.last) return;
+  __threadfence();
+
+  // merge: one warp per row, rows in waves.  The chunk-phase buffers are dead
+  // from here on; this region aliases them.
+  u64 *merged = reinterpret_cast<u64 *>(smem_raw);              // [kMaxRows][kMaxTopK]
+  int *mcount = reinterpret_cast<int *>(merged + kMaxRows * kMaxTopK);
+  u64 *stage = reinterpret_cast<u64 *>(mcount + kMaxRows + 1);  // [wave][C*ksel] (8-aligned)
+  const int per_row = a.C * ksel;
+  for (int r0 = 0; r0 < a.rows; r0 += a.rows_per_wave) {
+    const int r = r0 + warp;
+    const bool active = warp < a.rows_per_wave && r < a.rows;
+    if (active) {
+      u64 *st = stage + (size_t)warp * per_row;
+      const u64 *src = a.cand + ((size_t)b * a.rows_max + r) * (size_t)a.C * kMaxTopK;
+      for (int i = lane; i < per_row; i += 32) st[i] = __ldcg(src + (i / ksel) * kMaxTopK + i % ksel);
+      __syncwarp();
+      int h0 = 0, h1 = 0;  // heads of lists lane and lane+32
+      int j = 0;
+      for (; j < ksel; ++j) {
+        const u64 v0 = (lane < a.C && h0 < ksel) ? st[lane * ksel + h0] : 0ull;
+        const u64 v1 = (lane + 32 < a.C && h1 < ksel) ? st[(lane + 32) * ksel + h1] : 0ull;
+        const u64 best = v0 > v1 ? v0 : v1;
+        const u64 g = warp_max_u64(best);
+        if (g == 0ull) break;
+        if (v0 == g) ++h0;
+        else if (v1 == g) ++h1;
+        if (lane == 0) merged[r * kMaxTopK + j] = g;
+      }
+      if (lane == 0) mcount[r] = j;
+    }
+    __syncthreads();
+  }
+  if (warp != 0) return;
+
+  // ---- acceptance for sequence b (one warp) ---------------------------------
+  float *sR = reinterpret_cast<float *>(stage);  // 64 floats
+  int *sId = reinterpret_cast<int *>(sR + 64);   // 64 ints
+  int flags = 0, nacc = 0;
+  int emitted = -2;  // -2: none yet
+  const bool greedy = a.temperature == 0.f;
+  int32_t *out = a.out + (size_t)b * (K + 1);
+  for (int j = lane; j <= K; j += 32) out[j] = -1;
+  __syncwarp();
+  int k = 0;
+  for (; k < K; ++k) {
+    const int d = a.dt[(size_t)b * K + k];
+    const bool d_ok = d >= 0 && d < V;
+    flags |= __ldcg(&a.rowflags[b * a.rows_max + k]);
+    if (greedy) {
+      const int am = mcount[k] > 0 ? composite_id(merged[k * kMaxTopK]) : -1;
+      if (!d_ok) flags |= SV_FLAG_DRAFT_OUT_OF_RANGE;
+      if (d_ok && am >= 0 && d == am) {
+        if (lane == 0) out[k] = d;
+        ++nacc;
+        continue;
+      }
+      emitted = am;
+      break;
+    }
+    flags |= __ldcg(&a.rowflags[b * a.rows_max + K + 1 + k]);
+    const RowDist P = row_dist(merged + k * kMaxTopK, mcount[k], a.temperature, a.top_p);
+    const RowDist Q =
+        row_dist(merged + (K + 1 + k) * kMaxTopK, mcount[K + 1 + k], a.temperature, a.top_p);
+    bool accept = false;
+    if (!d_ok) {
+      flags |= SV_FLAG_DRAFT_OUT_OF_RANGE;
+    } else {
+      const float qd = dist_lookup(Q, d);
+      if (qd == 0.f) {
+        flags |= SV_FLAG_DRAFT_ZERO_Q;
+      } else {
+        const float pd = dist_lookup(P, d);
+        accept = a.ua[(size_t)b * K + k] < pd / qd;
+      }
+    }
+    if (accept) {
+      if (lane == 0) out[k] = d;
+      ++nacc;
+      continue;
+    }
+    // residual max(0, p - q) over p's support
+    float R[2] = {P.p[0], P.p[1]};
+    for (int src = 0; src < 64; ++src) {
+      const int qid = __shfl_sync(0xffffffffu, Q.id[src >> 5], src & 31);
+      const float qp = __shfl_sync(0xffffffffu, Q.p[src >> 5], src & 31);
+      if (qid >= 0 && qp > 0.f) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (P.id[h] == qid) R[h] = P.p[h] - qp;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) R[h] = R[h] > 0.f ? R[h] : 0.f;
+    const float Z = warp_sum(R[0] + R[1]);
+    if (!(Z > 0.f)) {
+      R[0] = P.p[0];
+      R[1] = P.p[1];
+    }
+    emitted = inverse_cdf_by_id(P.id, R, a.us[b], sR, sId);
+    break;
+  }
+  if (emitted == -2) {  // all K accepted: bonus from position K+1
+    flags |= __ldcg(&a.rowflags[b * a.rows_max + K]);
+    if (greedy) {
+      emitted = mcount[K] > 0 ? composite_id(merged[K * kMaxTopK]) : -1;
+    } else {
+      const RowDist P = row_dist(merged + K * kMaxTopK, mcount[K], a.temperature, a.top_p);
+      float R[2] = {P.p[0], P.p[1]};
+      emitted = inverse_cdf_by_id(P.id, R, a.us[b], sR, sId);
+    }
+  }
+  if (emitted < 0) flags |= SV_FLAG_EMPTY_DIST;
+  if (lane == 0) {
+    out[nacc] = emitted;
+    a.nacc[b] = nacc;
+    if (a.flags) a.flags[b] = flags;
+    a.counters[b] = 0;  // ready for the next call
+  }
+  for (int r = lane; r < a.rows_max; r += 32) a.rowflags[b * a.rows_max + r] = 0;
+}
+
+}  // namespace
+
+unsigned take_device_error_accept() { return 0u; }  // no bounded waits in this unit
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t spec_accept_workspace_bytes(int B, int K, int V) {
+  if (B < 0 || K < 1 || V < 1) return 0;
+  return ws_layout(B, K, V).total;
+}
+
+extern "C" sv_status spec_accept(const float *target_logits, const float *draft_logits,
+                                 const int32_t *draft_tokens, const float *u_accept,
+                                 const float *u_sample, int B, int K, int V, sv_sampling sampling,
+                                 int32_t *out_tokens, int32_t *n_accepted, int32_t *err_flags,
+                                 void *workspace, size_t workspace_bytes, sv_stream_t stream) {
+  clear_error();
+  if (B < 0 || K < 1 || V < 1)
+    return fail(SV_ERR_INVALID_ARG, "spec_accept: need B >= 0, K >= 1, V >= 1 (B=%d K=%d V=%d)", B,
+                K, V);
+  if (K > kMaxK) return fail(SV_ERR_UNSUPPORTED, "spec_accept: K=%d > %d", K, kMaxK);
+  if ((long long)V > (long long)kMaxChunks * kChunk)
+    return fail(SV_ERR_UNSUPPORTED, "spec_accept: V=%d > %d", V, kMaxChunks * kChunk);
+  const bool greedy = sampling.temperature == 0.f;
+  if (!(sampling.temperature >= 0.f) || !(sampling.temperature < 3.0e38f))
+    return fail(SV_ERR_INVALID_ARG, "spec_accept: temperature must be finite and >= 0");
+  if (!greedy) {
+    if (sampling.top_k < 1 || sampling.top_k > kMaxTopK)
+      return fail(SV_ERR_UNSUPPORTED, "spec_accept: top_k=%d outside [1, %d]", sampling.top_k,
+                  kMaxTopK);
+    if (!(sampling.top_p > 0.f) || !(sampling.top_p <= 1.f))
+      return fail(SV_ERR_INVALID_ARG, "spec_accept: top_p must be in (0, 1]");
+  }
+  if (B == 0) return SV_OK;
+  if ((long long)B * (2 * K + 1) > 65535)
+    return fail(SV_ERR_UNSUPPORTED, "spec_accept: B*(2K+1) = %lld > 65535", (long long)B * (2 * K + 1));
+  if (!target_logits || !draft_tokens || !u_accept || !u_sample || !out_tokens || !n_accepted ||
+      !workspace || (!greedy && !draft_logits))
+    return fail(SV_ERR_INVALID_ARG, "spec_accept: null pointer");
+  const WsLayout W = ws_layout(B, K, V);
+  if (workspace_bytes < W.total)
+    return fail(SV_ERR_INVALID_ARG, "spec_accept: workspace of %zu bytes, need %zu",
+                workspace_bytes, W.total);
+  if (!aligned(workspace, 16)) return fail(SV_ERR_INVALID_ARG, "spec_accept: workspace must be 16-byte aligned");
+  if (!aligned(target_logits, 4) || (draft_logits && !aligned(draft_logits, 4)) ||
+      !aligned(draft_tokens, 4) || !aligned(u_accept, 4) || !aligned(u_sample, 4) ||
+      !aligned(out_tokens, 4) || !aligned(n_accepted, 4) || (err_flags && !aligned(err_flags, 4)))
+    return fail(SV_ERR_INVALID_ARG, "spec_accept: misaligned pointer");
+  const size_t tlb = (size_t)B * (K + 1) * V * 4, dlb = (size_t)B * K * V * 4;
+  const size_t ob = (size_t)B * (K + 1) * 4, nb = (size_t)B * 4;
+  const void *ins[5] = {target_logits, draft_logits, draft_tokens, u_accept, u_sample};
+  const size_t insb[5] = {tlb, greedy ? 0 : dlb, (size_t)B * K * 4, (size_t)B * K * 4, nb};
+  const void *outs[4] = {out_tokens, n_accepted, err_flags, workspace};
+  const size_t outsb[4] = {ob, nb, err_flags ? nb : 0, W.total};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 5; ++j)
+      if (overlaps(outs[i], outsb[i], ins[j], insb[j]))
+        return fail(SV_ERR_INVALID_ARG, "spec_accept: an output overlaps an input");
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i], outsb[i], outs[j], outsb[j]))
+        return fail(SV_ERR_INVALID_ARG, "spec_accept: outputs overlap");
+  }
+
+  AcceptArgs args;
+  args.tl = target_logits;
+  args.dl = draft_logits;
+  args.dt = draft_tokens;
+  args.ua = u_accept;
+  args.us = u_sample;
+  args.B = B;
+  args.K = K;
+  args.V = V;
+  args.temperature = sampling.temperature;
+  args.top_k = sampling.top_k;
+  args.top_p = sampling.top_p;
+  args.out = out_tokens;
+  args.nacc = n_accepted;
+  args.flags = err_flags;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  args.counters = reinterpret_cast<int *>(ws);
+  args.rowflags = reinterpret_cast<int *>(ws + W.rowflags);
+  args.cand = reinterpret_cast<u64 *>(ws + W.cand);
+  args.rows = greedy ? K + 1 : 2 * K + 1;
+  args.rows_max = 2 * K + 1;
+  args.C = (V + kChunk - 1) / kChunk;
+  args.ksel = greedy ? 1 : std::min(sampling.top_k, V);
+  args.vec = (V % 4 == 0) && aligned(target_logits, 16) && (greedy || aligned(draft_logits, 16));
+  // final-phase staging: one warp per row, C*ksel keys each, at most 48 KB
+  const size_t per_row = (size_t)args.C * args.ksel * 8;
+  args.rows_per_wave = (int)std::max<size_t>(
+      1, std::min<size_t>({(size_t)args.rows, (size_t)kWarps, (size_t)(48 * 1024) / per_row}));
+  const size_t final_bytes = (size_t)kMaxRows * kMaxTopK * 8 + (kMaxRows + 1) * 4 +
+                             std::max<size_t>((size_t)args.rows_per_wave * per_row, 64 * 8);
+  const size_t smem = std::max(sizeof(ChunkSmem), final_bytes);
+  static bool configured[64] = {};
+  const int dev = current_device();
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    if (cudaFuncSetAttribute(spec_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             160 * 1024) != cudaSuccess)
+      return fail(SV_ERR_CUDA, "spec_accept: cudaFuncSetAttribute failed");
+    configured[dev] = true;
+  }
+  dim3 grid((unsigned)args.C, (unsigned)(B * args.rows));
+  spec_accept_kernel<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+  return check_launch("spec_accept");
+}

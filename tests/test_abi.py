@@ -1,0 +1,152 @@
+"""The C ABI boundary, on the host (no GPU): the library loads, exports every
+entry point include/specverify.h declares, and rejects invalid arguments
+before any launch (every call below returns during host-side validation)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "specverify.h"
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mtp_speculative_decoding_qmv_gb300 import build as b
+
+    b.build()
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    return sv.lib()
+
+
+def _declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    text = re.sub(r"#.*", "", text)
+    names = []
+    for stmt in text.split(";"):
+        stmt = " ".join(stmt.split())
+        if stmt.startswith("typedef") or "(" not in stmt or "{" in stmt:
+            continue
+        m = re.search(r"([A-Za-z_]\w*)\s*\(", stmt)
+        if m:
+            names.append(m.group(1))
+    return names
+
+
+def test_header_declares_the_path():
+    names = set(_declared_functions())
+    assert {"qmv_smallm", "spec_accept", "gdn_tape_capture", "gdn_tape_replay"} <= names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.sv_abi_version() == 1
+    assert L.sv_status_string(0) == b"ok"
+    assert L.sv_status_string(1) == b"invalid argument"
+    assert L.sv_status_string(99) == b"unknown status"
+
+
+def test_pdl_switch(L):
+    L.sv_set_pdl(1)
+    assert L.sv_get_pdl() == 1
+    L.sv_set_pdl(0)
+    assert L.sv_get_pdl() == 0
+
+
+A = 0x10000  # a 16-byte aligned fake device address; never dereferenced here
+
+
+def _qmv(L, w=A, s=A + 0x1000000, b=A + 0x2000000, x=A + 0x3000000, dt=1, y=A + 0x4000000,
+         M=4, N=64, K=256, gs=64, bits=4):
+    return L.qmv_smallm(w, s, b, x, dt, y, M, N, K, gs, bits, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"K": 100}, 1), ({"K": 0}, 1), ({"M": -1}, 1), ({"gs": 32}, 2), ({"bits": 8}, 2),
+    ({"M": 9}, 2), ({"dt": 7}, 1), ({"w": 0}, 1), ({"y": 0}, 1), ({"w": A + 4}, 1),
+    ({"x": A + 0x3000008}, 1), ({"y": A + 2}, 1), ({"y": A + 0x3000000}, 1),
+])
+def test_qmv_rejects(L, kw, status):
+    assert _qmv(L, **kw) == status
+    assert L.sv_last_error() != b""
+
+
+def test_qmv_empty_is_a_noop(L):
+    assert _qmv(L, M=0) == 0
+    assert _qmv(L, N=0) == 0
+
+
+def _accept(L, tl=A, dl=A + 0x1000000, dt=A + 0x2000000, ua=A + 0x2100000, us=A + 0x2200000,
+            B=2, K=3, V=1000, T=0.6, top_k=20, top_p=0.95, out=A + 0x3000000,
+            nacc=A + 0x3100000, flags=A + 0x3200000, ws=A + 0x4000000, ws_bytes=None):
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    if ws_bytes is None:
+        ws_bytes = max(L.spec_accept_workspace_bytes(max(B, 0), max(K, 1), max(V, 1)), 16)
+    return L.spec_accept(tl, dl, dt, ua, us, B, K, V, sv._Sampling(T, top_k, top_p), out, nacc,
+                         flags, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"K": 0}, 1), ({"K": 9}, 2), ({"V": 0}, 1), ({"V": 2_000_000}, 2), ({"B": -1}, 1),
+    ({"top_k": 0}, 2), ({"top_k": 65}, 2), ({"top_p": 0.0}, 1), ({"top_p": 1.5}, 1),
+    ({"T": -1.0}, 1), ({"T": float("nan")}, 1), ({"ws_bytes": 8}, 1), ({"ws": A + 8}, 1),
+    ({"tl": 0}, 1), ({"dl": 0}, 1), ({"out": A}, 1), ({"nacc": A + 0x3000000}, 1),
+    ({"B": 10000}, 2),
+])
+def test_accept_rejects(L, kw, status):
+    assert _accept(L, **kw) == status
+
+
+def test_accept_greedy_allows_null_draft_logits_and_empty_batch(L):
+    assert _accept(L, B=0) == 0
+    # greedy validation passes with draft_logits == NULL (launch not reached: B=0)
+    assert _accept(L, B=0, dl=0, T=0.0, top_k=0, top_p=1.0) == 0
+
+
+def test_workspace_size_is_monotone(L):
+    a = L.spec_accept_workspace_bytes(32, 3, 151936)
+    assert a > 0 and L.spec_accept_workspace_bytes(64, 3, 151936) > a
+    assert L.spec_accept_workspace_bytes(32, 0, 100) == 0
+
+
+def test_tape_bytes_matches_record_size(L):
+    # one record per (b, t, h): alpha + e[dv] + k[dk] fp32 = 1028 bytes at 128/128
+    # (T*H = 240 gates per sequence block: already a multiple of 4)
+    assert L.gdn_tape_bytes(16, 5, 48, 128, 128) == 16 * 5 * 48 * 1028
+    assert L.gdn_tape_bytes(1, 1, 1, 4, 4) == 4 * (8 + 4)
+    assert L.gdn_tape_bytes(0, 5, 48, 128, 128) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"T": 0}, 1), ({"T": 17}, 2), ({"dk": 130}, 2), ({"dv": 6}, 2), ({"H": 0}, 1),
+    ({"state0": 0}, 1), ({"q": A + 4}, 1), ({"tape": A}, 1),
+])
+def test_capture_rejects(L, kw, status):
+    args = dict(state0=A, q=A + 0x1000000, k=A + 0x2000000, v=A + 0x3000000, alpha=A + 0x4000000,
+                beta=A + 0x5000000, B=2, T=5, H=4, dk=128, dv=128, out=A + 0x6000000,
+                tape=A + 0x7000000, state_out=None)
+    args.update(kw)
+    st = L.gdn_tape_capture(args["state0"], args["q"], args["k"], args["v"], args["alpha"],
+                            args["beta"], args["B"], args["T"], args["H"], args["dk"],
+                            args["dv"], args["out"], args["tape"], args["state_out"], None)
+    assert st == status
+
+
+def test_replay_rejects(L):
+    assert L.gdn_tape_replay(A, A + 0x1000000, None, 2, 1, 2, 5, 4, 128, 128, None, None) == 1
+    assert L.gdn_tape_replay(A, A, A + 0x2000000, 2, 1, 2, 5, 4, 128, 128, None, None) == 1
+    assert L.gdn_tape_replay(A + 4, A + 0x1000000, A + 0x2000000, 2, 1, 2, 5, 4, 128, 128, None,
+                             None) == 1
+    assert L.gdn_tape_replay(A, A + 0x1000000, A + 0x2000000, 3, 1, 2, 5, 4, 128, 128, None,
+                             None) == 1  # count > B
+    assert L.gdn_tape_replay(A, A + 0x1000000, A + 0x2000000, 0, 1, 2, 5, 4, 128, 128, None,
+                             None) == 1  # count < 1
+    assert L.gdn_tape_replay(A, A + 0x1000000, A + 0x2000000, 1, 0, 0, 5, 4, 128, 128, None,
+                             None) == 0

@@ -1,0 +1,181 @@
+"""spec_accept on the GPU against the oracle, sequence by sequence.
+
+Token decisions and accepted lengths must be bit-exact, except for sequences
+in which the oracle (float64) met a near tie that fp32 may resolve the other
+way: |u_k - p/q| < 1e-5 (accept test), a top-p cumulative sum within 1e-5 of
+top_p, or an inverse-CDF boundary within 1e-5 * Z.  Those are counted,
+reported and checked only for validity (accepted prefix == drafts, emitted
+token in range, -1 padding).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import dev, f32, sv_module, wl
+
+pytestmark = pytest.mark.gpu
+
+NEAR = 1e-5
+
+
+@pytest.fixture(scope="module")
+def sv():
+    return sv_module()
+
+
+def _drafts_from_q(oracle, dl, T, top_k, top_p, stream):
+    """Draft tokens drawn from the draft distributions q_k (inverse CDF)."""
+    B, K, V = dl.shape
+    u = wl.uniforms(stream, (B, K))
+    dr = np.zeros((B, K), np.int32)
+    for b in range(B):
+        for k in range(K):
+            if T == 0.0:
+                dr[b, k] = int(np.argmax(dl[b, k]))
+                continue
+            q = oracle.filter_row(dl[b, k], T, top_k, top_p)[0]
+            c = np.cumsum(q)
+            dr[b, k] = min(int(np.searchsorted(c, u[b, k] * c[-1], side="right")), V - 1)
+    return dr
+
+
+def _gpu(sv, tl, dl, dr, ua, us, T, top_k, top_p, ws=None):
+    d = dev()
+    out = sv.spec_accept(torch.from_numpy(tl).to(d),
+                         None if dl is None else torch.from_numpy(dl).to(d),
+                         torch.from_numpy(dr).to(d), torch.from_numpy(ua).to(d),
+                         torch.from_numpy(us).to(d), T, top_k, top_p, workspace=ws)
+    torch.cuda.synchronize()
+    return [t.cpu().numpy() for t in out]
+
+
+def _compare(r, gpu, dr, V):
+    tok, nacc, flags = gpu
+    diag = r["diag"]
+    near = (diag[:, 0] < NEAR) | (diag[:, 1] < NEAR) | (diag[:, 2] < NEAR)
+    ok = ~near
+    np.testing.assert_array_equal(nacc[ok], r["n_accepted"][ok])
+    np.testing.assert_array_equal(tok[ok], r["out_tokens"][ok])
+    np.testing.assert_array_equal(flags[ok], r["err_flags"][ok])
+    K = dr.shape[1]
+    for b in np.flatnonzero(near):  # validity only
+        n = nacc[b]
+        assert 0 <= n <= K
+        assert (tok[b, :n] == dr[b, :n]).all()
+        assert -1 <= tok[b, n] < V and (tok[b, n + 1:] == -1).all()
+    return int(near.sum())
+
+
+def _case(sv, oracle, B, K, V, T, top_k, top_p, stream, sigma=2.0, noise=None):
+    T, top_p = f32(T), f32(top_p)
+    tl, dl = wl.accept_logits(stream, B, K, V, sigma=sigma, draft_noise=noise)
+    dr = _drafts_from_q(oracle, dl, T, top_k, top_p, stream)
+    ua, us = wl.accept_uniforms(stream, B, K)
+    r = oracle.spec_accept(tl, dl, dr, ua, us, T, top_k, top_p)
+    gpu = _gpu(sv, tl, None if T == 0.0 else dl, dr, ua, us, T, top_k, top_p)
+    return r, gpu, _compare(r, gpu, dr, V)
+
+
+def test_tiny_config(sv, oracle):
+    """vocab 1000, K=3, target and draft logits ~ N(0, 2) drawn independently,
+    temp 0.6 / top_k 20 / top_p 0.95 and temp 0; batches of 8 pooled into
+    launches of 512 sequences.  Independent logits leave little overlap
+    between p and q, so a second run with draft = target + N(0, 0.5) covers
+    the acceptance branch as well."""
+    _, _, near = _case(sv, oracle, 512, 3, 1000, 0.6, 20, 0.95, 1)
+    assert near <= 5
+    r, _, near = _case(sv, oracle, 512, 3, 1000, 0.6, 20, 0.95, 3, noise=0.5)
+    assert near <= 5
+    assert 1.0 < r["n_accepted"].mean() < 3.0
+    _, _, near0 = _case(sv, oracle, 512, 3, 1000, 0.0, 0, 1.0, 2)
+    assert near0 == 0
+
+
+@pytest.mark.parametrize("K,T,top_k,top_p", [
+    (1, 0.6, 20, 0.95), (2, 1.0, 1, 1.0), (5, 0.3, 64, 0.9), (8, 2.0, 5, 0.5),
+    (3, 1.0, 64, 1.0), (4, 0.8, 7, 0.99),
+])
+@pytest.mark.parametrize("V", [1000, 1001, 16384, 16387, 40000])
+def test_shapes_and_settings(sv, oracle, K, T, top_k, top_p, V):
+    _, _, near = _case(sv, oracle, 48, K, V, T, top_k, top_p, 10 + K + V % 97)
+    assert near <= 3
+
+
+@pytest.mark.parametrize("T,top_k,top_p", [(0.6, 20, 0.95), (0.0, 0, 1.0)])
+def test_lm_head_config(sv, oracle, T, top_k, top_p):
+    """vocab 151936, K=3, batch 32; draft = target + N(0, 0.5); logit scale
+    3.0 puts the per-position acceptance near 70 %."""
+    r, gpu, near = _case(sv, oracle, 32, 3, 151936, T, top_k, top_p, 20, sigma=3.0, noise=0.5)
+    assert near <= 2
+    print(f"mean accepted {r['n_accepted'].mean():.2f} of 3, near ties {near}")
+
+
+def test_workspace_reuse_and_repeat(sv, oracle):
+    B, K, V = 16, 3, 20000
+    tl, dl = wl.accept_logits(30, B, K, V)
+    dr = _drafts_from_q(oracle, dl, f32(0.7), 10, f32(0.9), 30)
+    ua, us = wl.accept_uniforms(30, B, K)
+    ws = sv.make_accept_workspace(B, K, V, dev())
+    outs = [_gpu(sv, tl, dl, dr, ua, us, 0.7, 10, 0.9, ws=ws) for _ in range(3)]
+    for o in outs[1:]:
+        for a, b in zip(o, outs[0]):
+            np.testing.assert_array_equal(a, b)
+    assert int(ws[: 4 * B].view(torch.int32).abs().sum()) == 0  # counters reset
+
+
+def test_error_flags_and_masks(sv, oracle):
+    B, K, V = 8, 3, 5000
+    T, top_k, top_p = f32(0.9), 12, f32(0.97)
+    tl, dl = wl.accept_logits(40, B, K, V)
+    dr = _drafts_from_q(oracle, dl, T, top_k, top_p, 40)
+    dr[0, 0] = -3                       # out of range
+    dr[1, 1] = V + 5                    # out of range at position 2
+    dl[2, 0, :] = -np.inf               # q one-hot on token 9; draft 11 has q = 0
+    dl[2, 0, 9] = 1.0
+    dr[2, 0] = 11
+    tl[3, 0, 100] = np.nan              # NaN in a used target row
+    tl[4, :, :] = -np.inf               # empty target rows
+    dl[5, 1, 200] = np.inf              # +inf in a draft row
+    tl[6, 0, :V // 2] = -np.inf         # half-masked target row
+    ua, us = wl.accept_uniforms(40, B, K)
+    r = oracle.spec_accept(tl, dl, dr, ua, us, T, top_k, top_p)
+    gpu = _gpu(sv, tl, dl, dr, ua, us, T, top_k, top_p)
+    _compare(r, gpu, dr, V)
+    assert gpu[2][0] & 1 and gpu[2][2] & 2 and gpu[2][3] & 4 and gpu[2][4] & 8
+
+
+def test_greedy_with_ties_and_masks(sv, oracle):
+    B, K, V = 64, 4, 3000
+    g = np.random.default_rng(7)
+    tl = g.integers(-4, 5, size=(B, K + 1, V)).astype(np.float32)  # many exact ties
+    am = np.argmax(tl[:, :K], axis=2)
+    dr = np.where(g.random((B, K)) < 0.8, am, g.integers(0, V, (B, K))).astype(np.int32)
+    tl[0, 1, :] = -np.inf
+    ua, us = wl.accept_uniforms(41, B, K)
+    r = oracle.spec_accept(tl, None, dr, ua, us, 0.0, 0, 1.0)
+    gpu = _gpu(sv, tl, None, dr, ua, us, 0.0, 0, 1.0)
+    assert _compare(r, gpu, dr, V) == 0
+
+
+def test_flat_rows_take_the_exact_path(sv, oracle):
+    """All-equal logits defeat the group-maximum filter; the exact path must
+    keep the lowest ids."""
+    B, K, V = 4, 2, 70000
+    tl = np.zeros((B, K + 1, V), np.float32)
+    dl = np.zeros((B, K, V), np.float32)
+    dl[:, :, 5] = 0.5
+    dr = np.full((B, K), 5, np.int32)
+    ua, us = wl.accept_uniforms(42, B, K)
+    r = oracle.spec_accept(tl, dl, dr, ua, us, 1.0, 16, 1.0)
+    gpu = _gpu(sv, tl, dl, dr, ua, us, 1.0, 16, 1.0)
+    _compare(r, gpu, dr, V)
+
+
+def test_empty_batch(sv):
+    d = dev()
+    z = torch.zeros((0, 4, 100), dtype=torch.float32, device=d)
+    out = sv.spec_accept(z, torch.zeros((0, 3, 100), dtype=torch.float32, device=d),
+                         torch.zeros((0, 3), dtype=torch.int32, device=d),
+                         torch.zeros((0, 3), dtype=torch.float32, device=d),
+                         torch.zeros((0,), dtype=torch.float32, device=d), 0.6, 20, 0.95)
+    assert out[0].shape == (0, 4)
