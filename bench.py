@@ -1,0 +1,694 @@
+#!/usr/bin/env python
+"""Benchmark of the verify-and-accept hot path on GB300.
+
+Default workload (one step = one verify+accept cycle at draft depth K=3,
+M=K+1=4 verify rows, batch 1, 27B-class stack):
+  per layer (64): q, k, v, o (5120x5120), gate, up (5120->17408), down
+      (17408->5120) -- all 4-bit affine g64 qmv_smallm -- and
+      gdn_tape_capture over the 4 verify tokens (48 heads, 128 x 128 fp32)
+  then the LM head (5120->151936) qmv_smallm whose output is the target
+  logits, spec_accept (temperature 0.6, top_k 20, top_p 0.95), and one
+  gdn_tape_replay launch committing n_accepted + 1 tape records in all 64
+  layers (n_accepted read on the device).
+The cycle is captured once as a CUDA graph (programmatic dependent launch
+between the qmv kernels) and replayed; its 13.84 GB weight stream is far
+larger than L2, so every step streams from HBM.
+
+Prints one JSON line.  --impl reference times the CPU oracle instead
+(bounded sample of the same cycle, extrapolated).  --workload mlp | lmhead |
+gdn measure the MLP projections, the LM head + accept batch and the GDN tape
+on their own.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import workloads as wl  # noqa: E402
+
+METRIC = "qmv_smallm HBM GB/s (% of peak) at M=4; verify+accept cycles/s at K=3"
+GROUP = 64
+WEIGHT_BYTES = 0.5625  # 4-bit nibble + bf16 scale and bias per 64 weights
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def qmv_bytes(M: int, N: int, K: int) -> int:
+    """Algorithmic bytes of one qmv_smallm call: packed nibbles, bf16 scales
+    and biases, bf16 rows in, fp32 rows out."""
+    return N * K // 2 + 2 * 2 * N * (K // GROUP) + 2 * M * K + 4 * M * N
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in Path(self.path).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------
+# the cycle on the GPU
+# ----------------------------------------------------------------------------
+class Cycle:
+    """Device buffers and the launch sequence of one verify+accept cycle."""
+
+    def __init__(self, sv, torch, device, depth: int = 3, layers: int = wl.N_LAYERS,
+                 heads: int = wl.GDN_HEADS, dim: int = wl.GDN_DIM, seed: int = 0):
+        self.sv, self.torch, self.dev = sv, torch, device
+        self.K = depth
+        self.M = depth + 1
+        self.layers = layers
+        self.V = wl.VOCAB
+        self.heads, self.dim = heads, dim
+        g = torch.Generator(device=device)
+        g.manual_seed(wl.MASTER_SEED + 17 + seed)
+        self.g = g
+        self.proj = []  # (w, s, b, x, y)
+        for _ in range(layers):
+            for _, N, Kin in wl.LAYER_PROJECTIONS:
+                self.proj.append(self._qmv_buffers(N, Kin))
+        self.lm = self._qmv_buffers(self.V, wl.HIDDEN)
+        self.qmv_calls = self.proj + [self.lm]
+        self.qmv_bytes = sum(qmv_bytes(self.M, w.shape[0], w.shape[1] * 8)
+                             for (w, _, _, _, _) in self.qmv_calls)
+        self.weight_bytes = sum(int(w.numel() * 4 + s.numel() * 2 * 2)
+                                for (w, s, _, _, _) in self.qmv_calls)
+        # GDN: committed state of every layer, per-layer verify inputs, one tape
+        T, H, d = self.M, heads, dim
+        f32 = torch.float32
+        self.state = torch.randn((layers, H, d, d), generator=g, device=device, dtype=f32) * 0.05
+
+        def unit(shape):
+            a = torch.randn(shape, generator=g, device=device, dtype=f32)
+            return (a / a.norm(dim=-1, keepdim=True)).contiguous()
+
+        self.gq = [unit((1, T, H, d)) for _ in range(layers)]
+        self.gk = [unit((1, T, H, d)) for _ in range(layers)]
+        self.gv = [torch.randn((1, T, H, d), generator=g, device=device, dtype=f32)
+                   for _ in range(layers)]
+        self.galpha = [torch.exp(-torch.nn.functional.softplus(
+            torch.randn((1, T, H), generator=g, device=device, dtype=f32))) for _ in range(layers)]
+        self.gbeta = [torch.sigmoid(torch.randn((1, T, H), generator=g, device=device, dtype=f32))
+                      for _ in range(layers)]
+        self.gout = [torch.empty((1, T, H, d), device=device, dtype=f32) for _ in range(layers)]
+        blk = sv.gdn_tape_bytes(1, T, H, d, d) // 4
+        self.tape = torch.empty(layers * blk, device=device, dtype=f32)
+        self.tapes = [self.tape[i * blk:(i + 1) * blk] for i in range(layers)]
+        self.gdn_bytes = layers * (H * d * d * 4            # capture reads the snapshot
+                                   + T * H * (3 * d + 2) * 4  # q, k, v, alpha, beta
+                                   + T * H * d * 4            # outputs
+                                   + blk * 4)                 # tape
+        # accept: target logits = LM-head output [K+1, V] = [1][K+1][V]
+        self.target = self.lm[4].view(1, self.M, self.V)
+        self.draft = torch.zeros((1, self.K, self.V), device=device, dtype=f32)
+        self.draft_tokens = torch.zeros((1, self.K), device=device, dtype=torch.int32)
+        ua, us = wl.accept_uniforms(99 + seed, 1, self.K)
+        self.ua = torch.from_numpy(ua).to(device)
+        self.us = torch.from_numpy(us).to(device)
+        self.ws = sv.make_accept_workspace(1, self.K, self.V, device)
+        self.out_tokens = torch.empty((1, self.M), device=device, dtype=torch.int32)
+        self.n_acc = torch.empty((1,), device=device, dtype=torch.int32)
+        self.flags = torch.empty((1,), device=device, dtype=torch.int32)
+        self.launches_per_step = len(self.qmv_calls) + layers + 2
+
+    def _qmv_buffers(self, N, Kin):
+        t, g, d = self.torch, self.g, self.dev
+        w = t.randint(-(2 ** 31), 2 ** 31 - 1, (N, Kin // 8), generator=g, device=d,
+                      dtype=t.int32)
+        s = (t.randn((N, Kin // GROUP), generator=g, device=d) * 0.02).to(t.bfloat16)
+        b = (t.randn((N, Kin // GROUP), generator=g, device=d) * 0.02).to(t.bfloat16)
+        x = t.randn((self.M, Kin), generator=g, device=d).to(t.bfloat16)
+        y = t.empty((self.M, N), device=d, dtype=t.float32)
+        return (w, s, b, x, y)
+
+    def prepare_drafts(self, noise: float = 0.5):
+        """Draft logits = target logits + N(0, noise) (once, outside timing);
+        drafts = the top token of each draft row."""
+        t = self.torch
+        self.run_qmv(self.lm)
+        t.cuda.synchronize()
+        z = self.target[:, : self.K].clone()
+        z += t.randn(z.shape, generator=self.g, device=self.dev) * noise
+        self.draft.copy_(z)
+        self.draft_tokens.copy_(z.argmax(dim=-1).to(t.int32))
+
+    def run_qmv(self, c):
+        w, s, b, x, y = c
+        self.sv.qmv_smallm(w, s, b, x, y)
+
+    def run(self):
+        sv = self.sv
+        i = 0
+        for layer in range(self.layers):
+            for _ in range(4):  # q, k, v, o
+                self.run_qmv(self.proj[i])
+                i += 1
+            sv.gdn_tape_capture(self.state[layer:layer + 1], self.gq[layer], self.gk[layer],
+                                self.gv[layer], self.galpha[layer], self.gbeta[layer],
+                                tape=self.tapes[layer], out=self.gout[layer])
+            for _ in range(3):  # gate, up, down
+                self.run_qmv(self.proj[i])
+                i += 1
+        self.run_qmv(self.lm)
+        sv.spec_accept(self.target, self.draft, self.draft_tokens, self.ua, self.us,
+                       0.6, 20, 0.95, workspace=self.ws, out_tokens=self.out_tokens,
+                       n_accepted=self.n_acc, err_flags=self.flags)
+        sv.gdn_tape_replay(self.state, self.tape, self.n_acc, self.M, n_replay_bias=1)
+
+    def run_qmv_only(self):
+        for c in self.qmv_calls:
+            self.run_qmv(c)
+
+
+def capture(torch, fn, stream):
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()
+        fn()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return graph
+
+
+def time_graph(torch, graph, stream, steps: int, warmup: int, barrier=None):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end)
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the cycle
+# ----------------------------------------------------------------------------
+def oracle_cycle_sample(depth: int = 3, layer_fraction: float = 1.0, repeats: int = 8,
+                        lm_fraction: float = 1.0 / 8, head_fraction: float = 1.0):
+    """Times the oracle on a sample of one cycle and extrapolates to a full
+    cycle: `layer_fraction` of the rows of one layer's seven projections, run
+    `repeats` times (x64/repeats layers), `lm_fraction` of the LM-head rows,
+    spec_accept at batch 1 on the full vocabulary, and GDN capture + replay on
+    `head_fraction` of one layer's heads (x64 layers).  Returns (seconds per
+    cycle, sample text, threads)."""
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    threads = oracle.set_threads(len(os.sched_getaffinity(0)))
+    M = depth + 1
+    t_qmv = 0.0
+    for j, (_, N, Kin) in enumerate(wl.LAYER_PROJECTIONS):
+        n = max(16, int(N * layer_fraction))
+        w, s, b = wl.qmv_weights(700 + j, n, Kin)
+        x = wl.qmv_activations(700 + j, M, Kin, "bf16")
+        t0 = time.perf_counter()
+        for _ in range(repeats):
+            oracle.qmv(w, s, b, x)
+        t_qmv += (time.perf_counter() - t0) / repeats * (N / n) * wl.N_LAYERS
+    n = max(16, int(wl.VOCAB * lm_fraction))
+    w, s, b = wl.qmv_weights(720, n, wl.HIDDEN)
+    x = wl.qmv_activations(720, M, wl.HIDDEN, "bf16")
+    t0 = time.perf_counter()
+    logits = oracle.qmv(w, s, b, x)
+    t_lm = (time.perf_counter() - t0) * (wl.VOCAB / n)
+    tl, dl = wl.accept_logits(721, 1, depth, wl.VOCAB, sigma=3.0, draft_noise=0.5)
+    tl[0, :, :n] = logits  # the sampled rows stand in for part of the vocabulary
+    dr = np.argmax(dl, axis=2).astype(np.int32)
+    ua, us = wl.accept_uniforms(721, 1, depth)
+    t0 = time.perf_counter()
+    r = oracle.spec_accept(tl, dl, dr, ua, us, float(np.float32(0.6)), 20,
+                           float(np.float32(0.95)))
+    t_acc = time.perf_counter() - t0
+    H = max(1, int(wl.GDN_HEADS * head_fraction))
+    g = wl.gdn_inputs(722, 1, M, H, wl.GDN_DIM, wl.GDN_DIM)
+    t0 = time.perf_counter()
+    _, tape = oracle.gdn_capture(g["state0"], g["q"], g["k"], g["v"], g["alpha"], g["beta"])
+    oracle.gdn_replay(g["state0"], tape, np.array([int(r["n_accepted"][0]) + 1], np.int32))
+    t_gdn = (time.perf_counter() - t0) * (wl.GDN_HEADS / H) * wl.N_LAYERS
+    total = t_qmv + t_lm + t_acc + t_gdn
+    sample = (f"oracle on {layer_fraction:g} of the rows of one layer's 7 projections run "
+              f"{repeats}x (scaled to 64 layers), {lm_fraction:g} of the LM-head rows, "
+              f"spec_accept at batch 1 over the full vocabulary, GDN capture+replay on {H} of "
+              f"48 heads of one layer (x64); extrapolated to one full cycle")
+    return total, sample, threads
+
+
+# ----------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_cycle_sample(args.depth, 1.0, 1, 1.0 / 64, 0.25)
+    secs = []
+    sample = ""
+    threads = 1
+    for _ in range(args.steps):
+        s, sample, threads = oracle_cycle_sample(args.depth, 1.0, 1, 1.0 / 64, 0.25)
+        secs.append(s)
+    per_cycle = statistics.mean(secs)
+    value = 1.0 / per_cycle
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "cycles/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_cycle * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(args.depth), "depth_K": args.depth,
+                   "M": args.depth + 1, "batch": 1},
+        "cpu_baseline": {"value": value, "unit": "cycles/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "cycles/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_name(depth):
+    return (f"27B-class verify+accept cycle: draft depth K={depth} (M={depth + 1} verify rows), "
+            f"batch 1; 64 layers x {{q,k,v,o 5120x5120; gate,up 5120->17408; down "
+            f"17408->5120}} 4-bit affine g64 + GDN tape capture (48 heads, 128x128 fp32) per "
+            f"layer; LM head 5120->151936; spec_accept (T=0.6, top_k=20, top_p=0.95); "
+            f"one GDN tape replay over all 64 layers")
+
+
+def run_cycle(args):
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        t, sample, threads = oracle_cycle_sample(args.depth)
+        cpu = {"value": 1.0 / t, "unit": "cycles/s", "cores": threads, "kind": "oracle",
+               "sample": sample}
+        log(f"cpu oracle: {t:.2f} s per cycle (extrapolated) on {threads} threads")
+
+    sv.set_pdl(True)
+    cyc = Cycle(sv, torch, device, depth=args.depth, seed=rank)
+    cyc.prepare_drafts()
+    stream = torch.cuda.Stream(device)
+    graph = capture(torch, cyc.run, stream)
+    qgraph = capture(torch, cyc.run_qmv_only, stream)
+    sv.device_status()
+
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        ms = time_graph(torch, graph, stream, args.steps, args.warmup, barrier)
+    clocks = clk.summary()
+    per_step_ms = ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        tt = torch.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    total_cycles = args.steps * world
+    value = total_cycles / (ms / 1e3)
+
+    # the dominant kernel: the cycle's 449 qmv_smallm launches as their own graph
+    qms = time_graph(torch, qgraph, stream, args.steps, 1)
+    n_q = len(cyc.qmv_calls)
+    per_launch_s = qms / 1e3 / (args.steps * n_q)
+    bytes_per_launch = cyc.qmv_bytes / n_q
+    achieved = bytes_per_launch / per_launch_s / 1e9
+    peaks = measured_peaks()
+
+    # end to end through the API: drafts/uniforms in from pinned host memory,
+    # tokens and accepted length back, every step
+    h_draft = cyc.draft.cpu().pin_memory()
+    h_tokens = cyc.draft_tokens.cpu().pin_memory()
+    h_ua, h_us = cyc.ua.cpu().pin_memory(), cyc.us.cpu().pin_memory()
+    h_out = torch.empty_like(cyc.out_tokens, device="cpu").pin_memory()
+    h_n = torch.empty_like(cyc.n_acc, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_draft, h_tokens, h_ua, h_us))
+    d2h = h_out.numel() * 4 + h_n.numel() * 4
+    accepted = []
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            cyc.draft.copy_(h_draft, non_blocking=True)
+            cyc.draft_tokens.copy_(h_tokens, non_blocking=True)
+            cyc.ua.copy_(h_ua, non_blocking=True)
+            cyc.us.copy_(h_us, non_blocking=True)
+            graph.replay()
+            h_out.copy_(cyc.out_tokens, non_blocking=True)
+            h_n.copy_(cyc.n_acc, non_blocking=True)
+        stream.synchronize()
+        accepted.append(int(h_n[0]))
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    t_e2e = time.perf_counter() - t0
+    barrier()
+    if world > 1:
+        import torch.distributed as dist
+
+        tt = torch.tensor([t_e2e], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    sv.device_status()
+
+    if rank != 0:
+        return 0
+    cycle_bytes = cyc.qmv_bytes + cyc.gdn_bytes
+    line = {
+        "metric": METRIC, "value": value, "unit": "cycles/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(args.depth), "depth_K": args.depth,
+                   "M": args.depth + 1, "batch": 1, "layers": wl.N_LAYERS,
+                   "weight_bytes_per_cycle": cyc.weight_bytes,
+                   "algorithmic_bytes_per_cycle": cycle_bytes,
+                   "cycle_gb_per_s": cycle_bytes / (per_step_ms / 1e3) / 1e9,
+                   "l2": "inputs larger than L2 (13.8 GB weight stream per step)",
+                   "graph": "one CUDA graph per cycle, PDL between qmv launches",
+                   "arithmetic": "4-bit weights x bf16 rows on bf16 MMA, fp32 accumulate; "
+                                 "accept and GDN in fp32",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "qmv_smallm", "bound": "hbm", "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks["source"],
+                     "bytes_per_launch": bytes_per_launch,
+                     "launch_us": per_launch_s * 1e6,
+                     "how": f"the cycle's {n_q} qmv_smallm launches (M={args.depth + 1}) "
+                            f"captured as their own graph, CUDA events over {args.steps} "
+                            f"replays on the launching stream"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": total_cycles / t_e2e, "unit": "cycles/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": cyc.launches_per_step * args.steps,
+        "clocks": clocks,
+        "acceptance": {"mean_accepted": statistics.mean(accepted) if accepted else None,
+                       "depth": args.depth},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# single-config measurements (not the default step)
+# ----------------------------------------------------------------------------
+def run_mlp(args):
+    """27B-class MLP verify projections: gate/up 5120->17408, down 17408->5120,
+    64 sequences back to back, each on its own weight copies (9.6 GB > L2),
+    for M in 1..8 except 7; qmv_smallm GB/s per M."""
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    sv.set_pdl(True)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.MASTER_SEED + 23)
+    seqs = 64
+    shapes = [(wl.INTERMEDIATE, wl.HIDDEN), (wl.INTERMEDIATE, wl.HIDDEN),
+              (wl.HIDDEN, wl.INTERMEDIATE)]
+    weights = []
+    for _ in range(seqs):
+        for N, K in shapes:
+            w = torch.randint(-(2 ** 31), 2 ** 31 - 1, (N, K // 8), generator=g, device=dev,
+                              dtype=torch.int32)
+            s_ = (torch.randn((N, K // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            b_ = (torch.randn((N, K // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            weights.append((w, s_, b_))
+    stream = torch.cuda.Stream(dev)
+    per_m = {}
+    for M in (1, 2, 3, 4, 5, 6, 8):
+        xs = {K: torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+              for K in (wl.HIDDEN, wl.INTERMEDIATE)}
+        ys = [torch.empty((M, w.shape[0]), device=dev) for (w, _, _) in weights]
+
+        def fn():
+            for (w, s_, b_), y in zip(weights, ys):
+                sv.qmv_smallm(w, s_, b_, xs[w.shape[1] * 8], y)
+
+        graph = capture(torch, fn, stream)
+        ms = time_graph(torch, graph, stream, args.steps, args.warmup)
+        nbytes = sum(qmv_bytes(M, w.shape[0], w.shape[1] * 8) for (w, _, _) in weights)
+        per_m[M] = nbytes / (ms / 1e3 / args.steps) / 1e9
+        log(f"M={M}: {per_m[M]:.0f} GB/s ({ms / args.steps / len(weights) * 1e3:.2f} us/call)")
+    peaks = measured_peaks()
+    line = {"metric": METRIC, "value": per_m[4], "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "27B-class MLP verify projections: 64 sequences x "
+                                   "{gate, up 5120->17408; down 17408->5120}, distinct weight "
+                                   "copies (9.6 GB), one CUDA graph per M",
+                       "l2": "inputs larger than L2"},
+            "per_M_gbs": per_m,
+            "per_M_frac": {m: v / peaks["hbm_gbs"] for m, v in per_m.items()},
+            "peak": peaks}
+    print(json.dumps(line), flush=True)
+    sv.device_status()
+    return 0
+
+
+def run_lmhead(args):
+    """LM-head verify + accept: 32 sequences x (M=4 LM-head qmv 5120->151936)
+    then one spec_accept over the batch (draft = target + N(0, 0.5))."""
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    sv.set_pdl(True)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.MASTER_SEED + 29)
+    B, K, V, H = 32, args.depth, wl.VOCAB, wl.HIDDEN
+    M = K + 1
+    w = torch.randint(-(2 ** 31), 2 ** 31 - 1, (V, H // 8), generator=g, device=dev,
+                      dtype=torch.int32)
+    s_ = (torch.randn((V, H // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    b_ = (torch.randn((V, H // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    xs = [torch.randn((M, H), generator=g, device=dev).to(torch.bfloat16) for _ in range(B)]
+    logits = torch.empty((B, M, V), device=dev)
+    for i in range(B):
+        sv.qmv_smallm(w, s_, b_, xs[i], logits[i])
+    draft = (logits[:, :K] + torch.randn((B, K, V), generator=g, device=dev) * 0.5).contiguous()
+    tokens = draft.argmax(dim=-1).to(torch.int32)
+    ua, us = wl.accept_uniforms(31, B, K)
+    ua, us = torch.from_numpy(ua).to(dev), torch.from_numpy(us).to(dev)
+    ws = sv.make_accept_workspace(B, K, V, dev)
+    out = torch.empty((B, M), dtype=torch.int32, device=dev)
+    nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    flags = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def accept():
+        sv.spec_accept(logits, draft, tokens, ua, us, 0.6, 20, 0.95, workspace=ws,
+                       out_tokens=out, n_accepted=nacc, err_flags=flags)
+
+    def fn():
+        for i in range(B):
+            sv.qmv_smallm(w, s_, b_, xs[i], logits[i])
+        accept()
+
+    stream = torch.cuda.Stream(dev)
+    graph = capture(torch, fn, stream)
+    agraph = capture(torch, accept, stream)
+    ms = time_graph(torch, graph, stream, args.steps, args.warmup)
+    ams = time_graph(torch, agraph, stream, args.steps, args.warmup)
+    acc_bytes = B * (2 * K + 1) * V * 4
+    line = {"metric": METRIC, "value": B / (ms / 1e3 / args.steps), "unit": "sequence-cycles/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"LM-head verify + accept: batch {B}, K={K} (M={M}) rows "
+                                   f"per sequence, 5120->151936 4-bit g64, T=0.6 top_k=20 "
+                                   f"top_p=0.95, draft = target + N(0, 0.5)"},
+            "ms_per_step": ms / args.steps,
+            "qmv_gbs": B * qmv_bytes(M, V, H) / ((ms - ams) / 1e3 / args.steps) / 1e9,
+            "spec_accept_us": ams / args.steps * 1e3,
+            "spec_accept_gbs": acc_bytes / (ams / 1e3 / args.steps) / 1e9,
+            "mean_accepted": float(nacc.float().mean().item())}
+    print(json.dumps(line), flush=True)
+    sv.device_status()
+    return 0
+
+
+def run_gdn(args):
+    """GatedDeltaNet tape: 16 sequences x 48 heads x 128x128 fp32, 5 tokens;
+    capture, then replay of an accepted prefix drawn from U{0..5}."""
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    B, T, H, d = 16, 5, wl.GDN_HEADS, wl.GDN_DIM
+    x = wl.gdn_inputs(50, B, T, H, d, d)
+    # 24 independent copies of the state (1.2 GB) so timing streams from HBM
+    copies = 24
+    states = [torch.from_numpy(x["state0"]).to(dev) for _ in range(copies)]
+    t = {n: torch.from_numpy(x[n]).to(dev) for n in ("q", "k", "v", "alpha", "beta", "n_replay")}
+    tapes = [torch.empty(sv.gdn_tape_bytes(B, T, H, d, d) // 4, device=dev) for _ in range(copies)]
+    outs = [torch.empty((B, T, H, d), device=dev) for _ in range(copies)]
+
+    def cap():
+        for i in range(copies):
+            sv.gdn_tape_capture(states[i], t["q"], t["k"], t["v"], t["alpha"], t["beta"],
+                                tape=tapes[i], out=outs[i])
+
+    def rep():
+        for i in range(copies):
+            sv.gdn_tape_replay(states[i], tapes[i], t["n_replay"], T)
+
+    stream = torch.cuda.Stream(dev)
+    gc, gr = capture(torch, cap, stream), capture(torch, rep, stream)
+    mc = time_graph(torch, gc, stream, args.steps, args.warmup) / args.steps / copies
+    mr = time_graph(torch, gr, stream, args.steps, args.warmup) / args.steps / copies
+    nb = B * H * d * d * 4
+    tape_b = sv.gdn_tape_bytes(B, T, H, d, d)
+    cap_bytes = nb + B * T * H * (3 * d + 2) * 4 + B * T * H * d * 4 + tape_b
+    n_live = int((x["n_replay"] > 0).sum())
+    rep_bytes = n_live * H * d * d * 4 * 2 + tape_b * n_live // B
+    line = {"metric": "GDN tape capture/replay GB/s", "value": cap_bytes / (mc / 1e3) / 1e9,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "GDN tape: B=16, H=48, dk=dv=128, T=5, prefix ~ U{0..5}"},
+            "capture_us": mc * 1e3, "replay_us": mr * 1e3,
+            "replay_gbs": rep_bytes / (mr / 1e3) / 1e9}
+    print(json.dumps(line), flush=True)
+    sv.device_status()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--depth", type=int, default=3, help="draft depth K (M = K+1)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn"], default="cycle")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return {"cycle": run_cycle, "mlp": run_mlp, "lmhead": run_lmhead, "gdn": run_gdn}[
+        args.workload](args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -11,32 +11,50 @@
 //
 // The op streams 0.5625 bytes of weight per weight (4-bit nibble + bf16
 // scale and bias per 64) and is HBM-bound.  Design:
-//  * one CTA per tile of 16*RT output rows over the whole of K; the grid is
-//    sized so the tiles of a typical projection are resident together, and
-//    every CTA keeps several KB of weights in flight;
-//  * a producer warp streams the tile's rows through a ring of shared-memory
-//    stages with bulk async copies (cp.async.bulk, complete_tx on an
-//    mbarrier, L2 evict-first), and loads the tile's scales/biases once;
-//  * four consumer warps split each 512-input stage (two 64-groups each:
-//    split-K over warps) and reduce through shared memory at the end in a
-//    fixed order, so results are deterministic;
-//  * each weight is read from shared memory once and used for all M rows: the
-//    nibbles are widened in registers to bf16 (128 + q, exact) and fed to the
-//    tensor cores as the 16-row A operand of mma.m16n8k16 with the (<= 8)
-//    activation rows as B; per group the fp32 result is scaled,
+//  * a CTA owns a tile of 64 output rows and a contiguous run of the K axis
+//    in 512-input stages; when there are too few row tiles to fill the GPU,
+//    the stages of a tile are split over a thread-block cluster of S CTAs
+//    whose partial results meet in the first CTA's shared memory (DSMEM) and
+//    are summed there in rank order -- deterministic run to run;
+//  * a producer warp streams the CTA's stages through a ring of shared-memory
+//    buffers as 2-D tensor-map boxes (cp.async.bulk.tensor, L2 evict-first,
+//    completing on the stage's mbarrier): packed weights as 64 rows x 128
+//    bytes per 256 inputs (128-byte swizzle), the stage's 8 scales and 8
+//    biases per row as 64 x 16 bytes.  Bytes in flight decide the bandwidth
+//    (HBM latency under load is microseconds), so the ring holds only those
+//    streamed bytes and is sized to fill shared memory at the achieved
+//    occupancy; large boxes keep the copy engine far from its per-request
+//    limit;
+//  * eight consumer warps take one 64-group of each stage (split-K over
+//    warps) for all four 16-row MMA tiles, so the per-stage costs of a warp
+//    (barrier, activation fragments, sum of x) are spread over 4096 weights;
+//    the activation fragments are read from L2 with plain loads issued one
+//    stage ahead; warps reduce through shared memory at the end in a fixed
+//    order;
+//  * each weight is read from shared memory once (ldmatrix on the swizzled
+//    box: conflict-free) and used for all M rows: nibbles are widened in
+//    registers to bf16 (128 + q, exact) and fed to the tensor cores as the
+//    16-row A operand of mma.m16n8k16 with the (<= 8) activation rows as B;
+//    per group the fp32 result is scaled,
 //        acc += s * D + (b - 128 s) * sum(x),
-//    with sum(x) itself taken from an all-ones MMA.  Products are exact, the
-//    accumulation is fp32.  CUDA-core FMAs alone cannot keep up with the
-//    HBM stream at M >= 2 on this part (4 FMAs + unpack per weight per row
-//    against ~3.3 issue slots per streamed weight), the MMA path costs the
+//    with sum(x) taken from an all-ones MMA.  Products are exact, the
+//    accumulation is fp32.  CUDA-core FMAs alone cannot keep up with the HBM
+//    stream at M >= 2 on this part (4 FMAs + unpack per weight per row
+//    against ~3.3 issue slots per streamed weight); the MMA path costs the
 //    same at every M.
-//  * programmatic dependent launch: the weight stream may start before the
-//    preceding kernel on the stream ends; x is read after griddepcontrol.wait.
+//  * when K is not a multiple of 512 the scale rows are not 16-byte aligned
+//    for the copy engine; the tile's whole scale block is then loaded once
+//    (and the K axis is not split);
+//  * programmatic dependent launch: the weight stream starts before the
+//    preceding kernel on the stream ends; activations are read, and y
+//    written, only after griddepcontrol.wait.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
@@ -44,99 +62,165 @@
 namespace sv {
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kGroupsPerWarp = 2;                                  // per stage
-constexpr int kStageInputs = kConsumerWarps * kGroupsPerWarp * 64;  // 512
-// Shared-memory bytes of one row of a stage: 256 data + 32 pad, so the
-// 64-bit fragment loads of 16 lanes (4 rows x 4 lanes) hit distinct banks.
-constexpr int kStageRowBytes = kStageInputs / 2 + 32;
+constexpr int kRows = 64;                          // output rows per CTA (4 MMA tiles)
+constexpr int kTiles = kRows / 16;
+constexpr int kConsumerWarps = 8;                  // one 64-group each per stage
+constexpr int kStageInputs = kConsumerWarps * 64;  // 512 inputs per stage
+constexpr int kBoxWords = 32;                      // 128-byte box rows = 256 inputs
+constexpr int kBoxesPerStage = kStageInputs / (kBoxWords * 8);  // 2
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr uint32_t kBf16One2 = 0x3F803F80u;   // bf16x2 (1, 1)
+constexpr int kMaxSplits = 8;                      // portable cluster size
+constexpr uint32_t kBf16One2 = 0x3F803F80u;        // bf16x2 (1, 1)
 constexpr uint32_t kNibbleMask = 0x000F000Fu;
-constexpr uint32_t kBf16Base = 0x43004300u;   // bf16x2 (128, 128)
+constexpr uint32_t kBf16Base = 0x43004300u;        // bf16x2 (128, 128)
+
+// stage: [2 boxes][64 rows x 128 B] (swizzled) then, when streamed, scales
+// [64][8] and biases [64][8] (bf16); 1024-byte multiple
+constexpr uint32_t kSbOff = kBoxesPerStage * kRows * 128;
+constexpr uint32_t kStageBytesStream = (kSbOff + 2 * kRows * 16 + 1023) / 1024 * 1024;
+constexpr uint32_t kStageBytesBlock = (kSbOff + 1023) / 1024 * 1024;
+constexpr uint32_t kRedBytes = kConsumerWarps * kRows * 8 * 4;  // cross-warp partials
 
 __device__ unsigned int g_qmv_device_error;
 
 struct QmvArgs {
-  const uint32_t *w;   // [N][K/8]
-  const uint16_t *s;   // [N][K/64] bf16
-  const uint16_t *b;   // [N][K/64] bf16
-  const void *x;       // [M][K] fp32 or bf16
-  float *y;            // [M][N]
+  const uint16_t *s;  // [N][K/64] bf16
+  const uint16_t *b;  // [N][K/64] bf16
+  const void *x;      // [M][K] fp32 or bf16
+  float *y;           // [M][N]
   int M, N, K;
   int stages;
+  int splits;     // CTAs per row tile (cluster size along K)
+  int sb_stream;  // 1: scales/biases stream with the stages; 0: whole tile block once
 };
 
 struct Layout {
-  size_t sb, red, bar, total;
+  uint32_t stage, sb, bar, total;
 };
 
-__host__ __device__ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline uint32_t round_up_u32(uint32_t v, uint32_t a) {
+  return (v + a - 1) / a * a;
+}
 
-__host__ __device__ inline Layout qmv_layout(int rows_cta, int groups, int stages) {
+// [stages] then, if not streamed, the tile's scale/bias block, then the
+// mbarriers.  The end-of-kernel reductions reuse the drained ring (at least
+// kRedBytes long).  `total` includes 1 KB of alignment slack.
+__host__ __device__ inline Layout qmv_layout(int groups, int stages, bool sb_stream) {
   Layout L;
-  L.sb = (size_t)stages * rows_cta * kStageRowBytes;
-  L.red = L.sb + round_up((size_t)2 * rows_cta * groups * 2, 16);
-  L.bar = L.red + (size_t)kConsumerWarps * rows_cta * 8 * sizeof(float);
-  L.total = L.bar + (size_t)(2 * stages + 1) * sizeof(uint64_t);
+  L.stage = sb_stream ? kStageBytesStream : kStageBytesBlock;
+  const uint32_t ring = (uint32_t)stages * L.stage;
+  L.sb = (ring > kRedBytes ? ring : kRedBytes);
+  const uint32_t after = L.sb + (sb_stream ? 0u : round_up_u32(2u * kRows * groups * 2u, 16));
+  L.bar = round_up_u32(after, 16);
+  L.total = L.bar + (uint32_t)(2 * stages + 1) * 8u + 1024u;
   return L;
 }
 
-// B fragments of one 64-group for the activation row this lane feeds.
-// Lane (row m = lane/4, t = lane%4) covers inputs 64g + 16t + [0,16) as two
-// 8-input slots; each slot feeds two k16 MMA steps whose k order pairs input
-// j with input j+4 -- the order the nibble widening below produces.
+// ---- device helpers --------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Raw activation data of one 64-group for the lane's activation row m: the A
+// operand (ldmatrix) gives lane (g = lane/4, t = lane%4) packed words t and
+// 4+t of the group, i.e. inputs 8t + [0,8) and 32 + 8t + [0,8), so the lane
+// loads those 16 inputs.
 template <bool kXF32>
-__device__ __forceinline__ void load_b_fragments(const QmvArgs &a, int m, bool valid, int g, int t,
-                                                 uint32_t (&hi)[8], uint32_t (&lo)[8]) {
-  if constexpr (!kXF32) {
-    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-    if (valid) {
-      const uint16_t *p = static_cast<const uint16_t *>(a.x) + (size_t)m * a.K + g * 64 + t * 16;
-      v0 = *reinterpret_cast<const uint4 *>(p);
-      v1 = *reinterpret_cast<const uint4 *>(p + 8);
+struct XRaw {
+  uint4 v[kXF32 ? 4 : 2];
+};
+
+template <bool kXF32>
+__device__ __forceinline__ XRaw<kXF32> load_x(const void *xrow, bool valid, int g, int t) {
+  XRaw<kXF32> r;
+#pragma unroll
+  for (int i = 0; i < (kXF32 ? 4 : 2); ++i) r.v[i] = make_uint4(0, 0, 0, 0);
+  if (valid) {
+    if constexpr (!kXF32) {
+      const uint16_t *p = static_cast<const uint16_t *>(xrow) + g * 64 + 8 * t;
+      r.v[0] = *reinterpret_cast<const uint4 *>(p);
+      r.v[1] = *reinterpret_cast<const uint4 *>(p + 32);
+    } else {
+      const float *p = static_cast<const float *>(xrow) + g * 64 + 8 * t;
+      r.v[0] = *reinterpret_cast<const uint4 *>(p);
+      r.v[1] = *reinterpret_cast<const uint4 *>(p + 4);
+      r.v[2] = *reinterpret_cast<const uint4 *>(p + 32);
+      r.v[3] = *reinterpret_cast<const uint4 *>(p + 36);
     }
-    hi[0] = prmt(v0.x, v0.z, 0x5410);  // (x0, x4)
-    hi[1] = prmt(v0.x, v0.z, 0x7632);  // (x1, x5)
-    hi[2] = prmt(v0.y, v0.w, 0x5410);  // (x2, x6)
-    hi[3] = prmt(v0.y, v0.w, 0x7632);  // (x3, x7)
-    hi[4] = prmt(v1.x, v1.z, 0x5410);
-    hi[5] = prmt(v1.x, v1.z, 0x7632);
-    hi[6] = prmt(v1.y, v1.w, 0x5410);
-    hi[7] = prmt(v1.y, v1.w, 0x7632);
+  }
+  return r;
+}
+
+// B fragments from the raw activations.  Each packed word feeds two k16 MMA
+// steps whose k order pairs input j with input j+4 (the order the nibble
+// widening produces), so B takes the same pairs.  fp32 rows become
+// x = hi + lo with both parts bf16.
+template <bool kXF32>
+__device__ __forceinline__ void b_fragments(const XRaw<kXF32> &r, uint32_t (&hi)[8],
+                                            uint32_t (&lo)[8]) {
+  if constexpr (!kXF32) {
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot) {
+      const uint4 v = r.v[slot];
+      hi[4 * slot + 0] = prmt(v.x, v.z, 0x5410);  // (x0, x4)
+      hi[4 * slot + 1] = prmt(v.x, v.z, 0x7632);  // (x1, x5)
+      hi[4 * slot + 2] = prmt(v.y, v.w, 0x5410);  // (x2, x6)
+      hi[4 * slot + 3] = prmt(v.y, v.w, 0x7632);  // (x3, x7)
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) lo[i] = 0;
   } else {
-    float v[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0.f;
-    if (valid) {
-      const float *p = static_cast<const float *>(a.x) + (size_t)m * a.K + g * 64 + t * 16;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 f = reinterpret_cast<const float4 *>(p)[i];
-        v[4 * i + 0] = f.x;
-        v[4 * i + 1] = f.y;
-        v[4 * i + 2] = f.z;
-        v[4 * i + 3] = f.w;
-      }
-    }
-    // pair (j, j+4) of each 8-input slot; x = hi + lo with both bf16
-#pragma unroll
-    for (int slot = 0; slot < 2; ++slot)
+    for (int slot = 0; slot < 2; ++slot) {
+      const uint4 u0 = r.v[2 * slot], u1 = r.v[2 * slot + 1];
+      const float v[8] = {__uint_as_float(u0.x), __uint_as_float(u0.y), __uint_as_float(u0.z),
+                          __uint_as_float(u0.w), __uint_as_float(u1.x), __uint_as_float(u1.y),
+                          __uint_as_float(u1.z), __uint_as_float(u1.w)};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float xa = v[8 * slot + j], xb = v[8 * slot + j + 4];
-        const __nv_bfloat162 h = __floats2bfloat162_rn(xa, xb);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[j], v[j + 4]);
         const __nv_bfloat162 l =
-            __floats2bfloat162_rn(xa - __low2float(h), xb - __high2float(h));
+            __floats2bfloat162_rn(v[j] - __low2float(h), v[j + 4] - __high2float(h));
         hi[4 * slot + j] = *reinterpret_cast<const uint32_t *>(&h);
         lo[4 * slot + j] = *reinterpret_cast<const uint32_t *>(&l);
       }
+    }
   }
 }
 
-// Two k16 MMA steps for one packed word (8 inputs) of rows r and r+8.
+// Two k16 MMA steps for one packed word (8 inputs) of rows g and g+8.
 // Widening: (w >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair
 // (128 + q_j, 128 + q_{j+4}).
 template <bool kXF32>
@@ -158,113 +242,151 @@ __device__ __forceinline__ void mma_word(float (&d)[4], uint32_t wr, uint32_t wr
   }
 }
 
-template <int RT, bool kXF32>
-__global__ void __launch_bounds__(kThreads) qmv_smallm_kernel(const QmvArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int kRows = 16 * RT;
+// Producer: expect chunk c's bytes on stage st's barrier and issue its boxes.
+// Rows past N, inputs past K and groups past K/64 are zero-filled by the copy
+// engine and still counted in the transaction bytes.
+__device__ __forceinline__ void issue_stage(const QmvArgs &a, const CUtensorMap *wmap,
+                                            const CUtensorMap *smap, const CUtensorMap *bmap,
+                                            uint32_t stage_addr, uint32_t bar, int c, int n0,
+                                            uint64_t policy) {
+  const int k0 = c * kStageInputs;
+  const int kn = min(kStageInputs, a.K - k0);
+  const int boxes = (kn + kBoxWords * 8 - 1) / (kBoxWords * 8);
+  const uint32_t bytes = (uint32_t)(boxes * kRows * 128 + (a.sb_stream ? 2 * kRows * 16 : 0));
+  mbar_arrive_expect_tx_u32(bar, bytes);
+  for (int bx = 0; bx < boxes; ++bx)
+    tma_load_2d(stage_addr + bx * kRows * 128, wmap, k0 / 8 + bx * kBoxWords, n0, bar, policy);
+  if (a.sb_stream) {
+    tma_load_2d(stage_addr + kSbOff, smap, k0 / 64, n0, bar, policy);
+    tma_load_2d(stage_addr + kSbOff + kRows * 16, bmap, k0 / 64, n0, bar, policy);
+  }
+}
+
+// three CTAs per SM (<= 75 registers per thread) keep 24 consumer warps resident
+template <bool kXF32>
+__global__ void __launch_bounds__(kThreads, 3)
+    qmv_smallm_kernel(const __grid_constant__ CUtensorMap wmap,
+                      const __grid_constant__ CUtensorMap smap,
+                      const __grid_constant__ CUtensorMap bmap, const QmvArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzled boxes need 1024-byte aligned destinations
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t *smem = smem_raw + (base - raw);
   const int groups = a.K >> 6;
-  const int n0 = blockIdx.x * kRows;
+  const int splits = a.splits;
+  const int tile = blockIdx.x / splits;
+  const int split = blockIdx.x - tile * splits;
+  const int n0 = tile * kRows;
   const int rows = min(kRows, a.N - n0);
   const int n_chunks = (a.K + kStageInputs - 1) / kStageInputs;
+  const int c_begin = (int)((long long)split * n_chunks / splits);
+  const int c_end = (int)((long long)(split + 1) * n_chunks / splits);
   const int stages = a.stages;
-  const Layout L = qmv_layout(kRows, groups, stages);
-  uint8_t *wst = smem;
-  uint16_t *s_sm = reinterpret_cast<uint16_t *>(smem + L.sb);
-  uint16_t *b_sm = s_sm + kRows * groups;
-  float *red = reinterpret_cast<float *>(smem + L.red);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar);
-  uint64_t *empty = full + stages;
-  uint64_t *sb_bar = empty + stages;
+  const Layout L = qmv_layout(groups, stages, a.sb_stream != 0);
+  const uint32_t full0 = base + L.bar;          // full[i]  = full0 + 8 i
+  const uint32_t empty0 = full0 + 8u * stages;  // empty[i] = empty0 + 8 i
+  const uint32_t sb_bar = empty0 + 8u * stages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
+      mbar_init_u32(full0 + 8u * i, 1);
+      mbar_init_u32(empty0 + 8u * i, kConsumerWarps);
     }
-    mbar_init(sb_bar, 32);
+    mbar_init_u32(sb_bar, 32);
     fence_mbar_init();
   }
   __syncthreads();
   pdl_launch_dependents();
 
+  float part[2] = {0.f, 0.f};  // this thread's two sums of the tile (consumers)
+  bool ok = true;
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
+    // Weights, scales and biases do not depend on earlier kernels: no
+    // griddepcontrol.wait on this side.
+    uint16_t *s_sm = reinterpret_cast<uint16_t *>(smem + L.sb);
+    uint16_t *b_sm = s_sm + kRows * groups;
+    uint64_t *sb_bar_p = reinterpret_cast<uint64_t *>(smem + (sb_bar - base));
     const uint32_t sb_bytes = (uint32_t)rows * groups * 2;
-    if (sb_bytes % 16u == 0) {
+    if (a.sb_stream) {
+      mbar_arrive_u32(sb_bar);
+    } else if (sb_bytes % 16u == 0) {
       if (lane == 0) {
-        mbar_arrive_expect_tx(sb_bar, 2 * sb_bytes);
-        bulk_copy_g2s(s_sm, a.s + (size_t)n0 * groups, sb_bytes, sb_bar);
-        bulk_copy_g2s(b_sm, a.b + (size_t)n0 * groups, sb_bytes, sb_bar);
+        mbar_arrive_expect_tx_u32(sb_bar, 2 * sb_bytes);
+        bulk_copy_g2s(s_sm, a.s + (size_t)n0 * groups, sb_bytes, sb_bar_p);
+        bulk_copy_g2s(b_sm, a.b + (size_t)n0 * groups, sb_bytes, sb_bar_p);
       } else {
-        mbar_arrive(sb_bar);
+        mbar_arrive_u32(sb_bar);
       }
     } else {  // ragged tile whose scale block is not a 16-byte multiple
       for (int i = lane; i < rows * groups; i += 32) {
         s_sm[i] = a.s[(size_t)n0 * groups + i];
         b_sm[i] = a.b[(size_t)n0 * groups + i];
       }
-      mbar_arrive(sb_bar);
+      mbar_arrive_u32(sb_bar);
     }
-    const uint64_t policy = l2_policy_evict_first();
-    const size_t row_stride = (size_t)a.K / 2;
-    const uint8_t *wbase = reinterpret_cast<const uint8_t *>(a.w) + (size_t)n0 * row_stride;
-    int issued = 0;
-    bool ok = true;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int st = c % stages;
-      if (c >= stages) {
-        int got = 0;
-        if (lane == 0) got = mbar_wait(&empty[st], ((c / stages) & 1) ^ 1) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      int st = 0, ph = 0;  // stage of chunk c and the parity of its previous release
+      for (int c = c_begin; c < c_end; ++c) {
+        if (c - c_begin >= stages && !mbar_wait_u32(empty0 + 8u * st, ph ^ 1)) {
+          atomicOr(&g_qmv_device_error, 1u);
+          // let the copies already issued land before the CTA may exit
+          for (int i = max(c_begin, c - stages); i < c; ++i)
+            (void)mbar_wait_u32(full0 + 8u * ((i - c_begin) % stages),
+                                ((i - c_begin) / stages) & 1);
           break;
         }
+        issue_stage(a, &wmap, &smap, &bmap, base + st * L.stage, full0 + 8u * st, c, n0,
+                    policy);
+        if (++st == stages) {
+          st = 0;
+          ph ^= 1;
+        }
       }
-      const int k0 = c * kStageInputs;
-      const uint32_t rb = (uint32_t)(min(kStageInputs, a.K - k0) / 2);
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], rb * (uint32_t)rows);
-      __syncwarp();
-      uint8_t *dst = wst + (size_t)st * kRows * kStageRowBytes;
-      for (int r = lane; r < rows; r += 32)
-        bulk_copy_g2s_hint(dst + r * kStageRowBytes, wbase + r * row_stride + k0 / 2, rb,
-                           &full[st], policy);
-      issued = c + 1;
     }
-    if (!ok && lane == 0) {
-      atomicOr(&g_qmv_device_error, 1u);
-      // let the copies already issued land before the CTA may exit
-      for (int c = max(0, issued - stages); c < issued; ++c)
-        (void)mbar_wait(&full[c % stages], (c / stages) & 1);
-    }
-    return;
-  }
-
-  // ------------------------------ consumers -------------------------------
-  const int r = lane >> 2, t = lane & 3;
-  const int m = lane >> 2;  // activation row this lane feeds into B
-  const bool m_valid = m < a.M;
-  float acc[RT][4];
+    __syncwarp();
+    if (splits == 1) return;
+  } else {
+    // ------------------------------ consumers -----------------------------
+    const int g8 = lane >> 2, t = lane & 3;  // fragment row (= activation row m) and column
+    const bool m_valid = g8 < a.M;
+    const int gl = warp;  // the stage's group this warp reduces
+    // ldmatrix.x4 addresses: lane L reads row ((L >> 3) & 1) * 8 + (L & 7) of
+    // an MMA tile, 16-byte chunk 2 * (gl % 4) + (L >> 4) of the 128-byte box
+    // row, at its swizzled position (chunk ^ row % 8)
+    const int lrow = ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int lchunk = ((gl & 3) << 1) + (lane >> 4);
+    const uint32_t ldm_off =
+        (uint32_t)((gl >> 2) * kRows * 128 + lrow * 128 + ((lchunk ^ (lrow & 7)) << 4));
+    // scale / bias of rows g8 and g8+8 of tile 0, group gl (streamed layout)
+    const uint32_t sb_off = kSbOff + (uint32_t)(g8 * 16 + gl * 2);
+    const uint32_t blk = base + L.sb;  // whole-tile block (not streamed)
+    const void *xrow = static_cast<const uint8_t *>(a.x) +
+                       (size_t)(m_valid ? g8 : 0) * a.K * (kXF32 ? 4 : 2);
+    float acc[kTiles][4];
 #pragma unroll
-  for (int i = 0; i < RT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  // every lane waits (each needs the acquire); the outcome is made warp-uniform
-  bool ok = __all_sync(0xffffffffu, mbar_wait(sb_bar, 0));
-  pdl_wait();  // x (and y) belong to the preceding kernel until here
-  for (int c = 0; ok && c < n_chunks; ++c) {
-    const int st = c % stages;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / stages) & 1))) {
-      ok = false;
-      break;
-    }
-    const uint8_t *stage = wst + (size_t)st * kRows * kStageRowBytes;
-#pragma unroll
-    for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
-      const int gl = warp * kGroupsPerWarp + gi;
-      const int g = c * (kConsumerWarps * kGroupsPerWarp) + gl;
+    for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    // every lane waits (each needs the acquire); the outcome is made warp-uniform
+    ok = __all_sync(0xffffffffu, mbar_wait_u32(sb_bar, 0));
+    pdl_wait();  // x and y belong to the preceding kernel until here
+    int g = c_begin * kConsumerWarps + gl;
+    XRaw<kXF32> xnext = load_x<kXF32>(xrow, m_valid && g < groups, g, t);
+    int st = 0, ph = 0;  // stage of chunk c and the parity of its fill
+    for (int c = c_begin; ok && c < c_end; ++c, g += kConsumerWarps) {
+      const XRaw<kXF32> xcur = xnext;
+      const int gn = g + kConsumerWarps;  // next stage's group: its loads fly during the wait
+      if (c + 1 < c_end) xnext = load_x<kXF32>(xrow, m_valid && gn < groups, gn, t);
+      if (!__all_sync(0xffffffffu, mbar_wait_u32(full0 + 8u * st, ph))) {
+        ok = false;
+        break;
+      }
+      const uint32_t stage = base + st * L.stage;
       if (g < groups) {
         uint32_t hi[8], lo[8];
-        load_b_fragments<kXF32>(a, m, m_valid, g, t, hi, lo);
+        b_fragments<kXF32>(xcur, hi, lo);
         float xs[4] = {0.f, 0.f, 0.f, 0.f};  // sum of x over the group, cols 2t, 2t+1
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
@@ -275,78 +397,238 @@ __global__ void __launch_bounds__(kThreads) qmv_smallm_kernel(const QmvArgs a) {
                               lo[2 * s + 1]);
         }
 #pragma unroll
-        for (int rt = 0; rt < RT; ++rt) {
-          const int row = rt * 16 + r;
-          const uint8_t *rp = stage + row * kStageRowBytes + gl * 32 + t * 8;
-          const uint2 w0 = *reinterpret_cast<const uint2 *>(rp);
-          const uint2 w8 = *reinterpret_cast<const uint2 *>(rp + 8 * kStageRowBytes);
+        for (int rt = 0; rt < kTiles; ++rt) {
+          // words t, 4+t of the group for rows g8 and g8+8 of MMA tile rt
+          uint32_t w[4];
+          ldmatrix_x4(w, stage + ldm_off + rt * 16 * 128);
           float d[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_word<kXF32>(d, w0.x, w8.x, hi, lo);
-          mma_word<kXF32>(d, w0.y, w8.y, hi + 4, lo + 4);
-          const float s0 = bf16_bits_to_float(s_sm[row * groups + g]);
-          const float s8 = bf16_bits_to_float(s_sm[(row + 8) * groups + g]);
-          const float c0 = fmaf(-128.f, s0, bf16_bits_to_float(b_sm[row * groups + g]));
-          const float c8 = fmaf(-128.f, s8, bf16_bits_to_float(b_sm[(row + 8) * groups + g]));
+          mma_word<kXF32>(d, w[0], w[1], hi, lo);
+          mma_word<kXF32>(d, w[2], w[3], hi + 4, lo + 4);
+          uint32_t sr, s8, br, b8;
+          if (a.sb_stream) {  // [64][8] scales then [64][8] biases of this stage
+            const uint32_t p = stage + sb_off + rt * 16 * 16;
+            sr = lds_u16(p);
+            s8 = lds_u16(p + 8 * 16);
+            br = lds_u16(p + kRows * 16);
+            b8 = lds_u16(p + kRows * 16 + 8 * 16);
+          } else {
+            const uint32_t p = blk + (uint32_t)(((rt * 16 + g8) * groups + g) * 2);
+            const uint32_t q = p + (uint32_t)(kRows * groups * 2);
+            sr = lds_u16(p);
+            s8 = lds_u16(p + 8 * groups * 2);
+            br = lds_u16(q);
+            b8 = lds_u16(q + 8 * groups * 2);
+          }
+          const float s0 = bf16_bits_to_float(sr), s1 = bf16_bits_to_float(s8);
+          const float c0 = fmaf(-128.f, s0, bf16_bits_to_float(br));
+          const float c1 = fmaf(-128.f, s1, bf16_bits_to_float(b8));
           acc[rt][0] = fmaf(s0, d[0], fmaf(c0, xs[0], acc[rt][0]));
           acc[rt][1] = fmaf(s0, d[1], fmaf(c0, xs[1], acc[rt][1]));
-          acc[rt][2] = fmaf(s8, d[2], fmaf(c8, xs[0], acc[rt][2]));
-          acc[rt][3] = fmaf(s8, d[3], fmaf(c8, xs[1], acc[rt][3]));
+          acc[rt][2] = fmaf(s1, d[2], fmaf(c1, xs[0], acc[rt][2]));
+          acc[rt][3] = fmaf(s1, d[3], fmaf(c1, xs[1], acc[rt][3]));
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
+      if (++st == stages) {
+        st = 0;
+        ph ^= 1;
+      }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-  }
-  if (!ok && lane == 0) atomicOr(&g_qmv_device_error, 2u);
+    if (!ok && lane == 0) atomicOr(&g_qmv_device_error, 2u);
 
-  // cross-warp reduction in a fixed order: red[warp][row][col]
+    // cross-warp reduction in a fixed order, red[warp][row][col] in the drained ring
+    float *red = reinterpret_cast<float *>(smem);
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
 #pragma unroll
-  for (int rt = 0; rt < RT; ++rt) {
-    float *p = red + ((size_t)warp * kRows + rt * 16) * 8;
-    p[r * 8 + 2 * t] = acc[rt][0];
-    p[r * 8 + 2 * t + 1] = acc[rt][1];
-    p[(r + 8) * 8 + 2 * t] = acc[rt][2];
-    p[(r + 8) * 8 + 2 * t + 1] = acc[rt][3];
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-  if (!ok) return;
-  for (int idx = threadIdx.x; idx < kRows * 8; idx += kConsumerWarps * 32) {
-    const int col = idx / kRows, row = idx % kRows;  // row fastest: coalesced stores
-    if (col < a.M && row < rows) {
+    for (int rt = 0; rt < kTiles; ++rt) {
+      float *p = red + ((size_t)warp * kRows + rt * 16) * 8;
+      p[g8 * 8 + 2 * t] = acc[rt][0];
+      p[g8 * 8 + 2 * t + 1] = acc[rt][1];
+      p[(g8 + 8) * 8 + 2 * t] = acc[rt][2];
+      p[(g8 + 8) * 8 + 2 * t + 1] = acc[rt][3];
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+    // element e = col * 64 + row; thread handles e = tid and tid + 256
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = threadIdx.x + h * kConsumerWarps * 32;
+      const int col = e / kRows, row = e % kRows;
       float v = 0.f;
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) v += red[((size_t)w * kRows + row) * 8 + col];
-      a.y[(size_t)col * a.N + n0 + row] = v;
+      part[h] = v;
     }
+    if (splits == 1) {
+      if (!ok) return;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = threadIdx.x + h * kConsumerWarps * 32;
+        const int col = e / kRows, row = e % kRows;  // row fastest: coalesced stores
+        if (col < a.M && row < rows) a.y[(size_t)col * a.N + n0 + row] = part[h];
+      }
+      return;
+    }
+  }
+
+  // ---- split K: partial tiles meet in the first CTA of the cluster --------
+  // (every thread of every CTA of the cluster takes part in both barriers)
+  cluster_sync_all();  // all rings drained: the first CTA's ring may be overwritten
+  const uint32_t rank = cluster_rank();
+  if (warp < kConsumerWarps) {
+    const uint32_t slot = map_shared_to_rank(base, 0) + rank * (kRows * 8 * 4);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      st_cluster_f32(slot + 4u * (threadIdx.x + h * kConsumerWarps * 32), part[h]);
+  }
+  cluster_sync_all();  // every partial has landed
+  if (rank != 0 || warp >= kConsumerWarps) return;
+  if (__any_sync(0xffffffffu, !ok)) return;
+  const float *slots = reinterpret_cast<const float *>(smem);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = threadIdx.x + h * kConsumerWarps * 32;
+    const int col = e / kRows, row = e % kRows;
+    float v = 0.f;
+    for (int r = 0; r < splits; ++r) v += slots[r * kRows * 8 + e];
+    if (col < a.M && row < rows) a.y[(size_t)col * a.N + n0 + row] = v;
   }
 }
 
-template <int RT, bool kXF32>
-sv_status launch(const QmvArgs &args, int ctas, size_t smem, cudaStream_t stream) {
+// cuTensorMapEncodeTiled from the driver, found through the runtime (no link
+// dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+sv_status encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr,
+                    uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
+                    uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return fail(SV_ERR_CUDA, "qmv_smallm: cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(SV_ERR_CUDA, "qmv_smallm: tensor map encode failed (%d)", (int)r);
+  return SV_OK;
+}
+
+// Co-resident CTAs per SM allowed by registers and threads (cached per device).
+template <bool kXF32>
+int occupancy_without_smem(int dev) {
+  static int cached[64] = {};
+  if (dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmv_smallm_kernel<kXF32>, kThreads,
+                                                      0) != cudaSuccess || n < 1)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <bool kXF32>
+sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   static bool configured[64] = {};
   const int dev = current_device();
-  auto kern = qmv_smallm_kernel<RT, kXF32>;
+  auto kern = qmv_smallm_kernel<kXF32>;
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    int optin = 0;
-    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
         cudaSuccess)
       return fail(SV_ERR_CUDA, "qmv_smallm: cudaFuncSetAttribute failed");
     configured[dev] = true;
   }
+  const int groups = args.K / 64;
+  const int tiles = (args.N + kRows - 1) / kRows;
+  const int n_chunks = (args.K + kStageInputs - 1) / kStageInputs;
+  const int sms = device_sm_count();
+  const int occ = occupancy_without_smem<kXF32>(dev);
+  // split K over a cluster when the row tiles alone would leave CTA slots
+  // idle, as far as the grid still fits in one wave of resident CTAs
+  int splits = 1;
+  if (args.sb_stream) {
+    const int fit = (occ * sms) / tiles;
+    splits = std::max(1, std::min({fit, kMaxSplits, n_chunks}));
+  }
+  args.splits = splits;
+  const int ctas = tiles * splits;
+  // fill shared memory with stages at the occupancy the grid will reach
+  const int per_sm = std::max(1, std::min({(ctas + sms - 1) / sms, occ, 8}));
+  const uint32_t budget = (uint32_t)(224 * 1024) / per_sm - 1024u;
+  const bool sbs = args.sb_stream != 0;
+  const uint32_t fixed = qmv_layout(groups, 0, sbs).total;
+  const uint32_t stage_bytes = qmv_layout(groups, 1, sbs).stage + 16u;
+  const int per_cta_chunks = (n_chunks + splits - 1) / splits;
+  int stages = budget > fixed ? (int)((budget - fixed) / stage_bytes) : 2;
+  stages = std::max(2, std::min(stages, std::min(32, std::max(2, per_cta_chunks))));
+  Layout L = qmv_layout(groups, stages, sbs);
+  while (L.total > (uint32_t)optin && stages > 2) L = qmv_layout(groups, --stages, sbs);
+  if (L.total > (uint32_t)optin)
+    return fail(SV_ERR_UNSUPPORTED, "qmv_smallm: K=%d needs %u bytes of shared memory",
+                args.K, L.total);
+  args.stages = stages;
+
+  CUtensorMap wmap, smap, bmap;
+  sv_status st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, w, (uint64_t)args.K / 8,
+                           (uint64_t)args.N, (uint64_t)args.K / 2, kBoxWords, kRows,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != SV_OK) return st;
+  if (sbs) {
+    st = encode_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, args.s, (uint64_t)groups,
+                   (uint64_t)args.N, (uint64_t)groups * 2, 8, kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != SV_OK) return st;
+    st = encode_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, args.b, (uint64_t)groups,
+                   (uint64_t)args.N, (uint64_t)groups * 2, 8, kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != SV_OK) return st;
+  } else {
+    smap = wmap;  // unused
+    bmap = wmap;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = L.total;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  if (pdl_enabled()) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (splits > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)splits;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
-  if (cudaLaunchKernelEx(&cfg, kern, args) != cudaSuccess) {
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, kern, wmap, smap, bmap, args) != cudaSuccess) {
     return fail(SV_ERR_CUDA, "qmv_smallm: launch failed: %s",
                 cudaGetErrorString(cudaGetLastError()));
   }
@@ -385,9 +667,10 @@ extern "C" sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales
   if (!w_packed || !scales || !biases || !x || !y)
     return fail(SV_ERR_INVALID_ARG, "qmv_smallm: null pointer");
   if (!aligned(w_packed, 16) || !aligned(scales, 16) || !aligned(biases, 16) || !aligned(x, 16))
-    return fail(SV_ERR_INVALID_ARG, "qmv_smallm: w_packed, scales, biases and x must be 16-byte aligned");
+    return fail(SV_ERR_INVALID_ARG,
+                "qmv_smallm: w_packed, scales, biases and x must be 16-byte aligned");
   if (!aligned(y, 4)) return fail(SV_ERR_INVALID_ARG, "qmv_smallm: y must be 4-byte aligned");
-  if ((long long)N * (K / 8) > (1ll << 40))
+  if ((long long)K > (1ll << 30) || (long long)N * (K / 8) > (1ll << 40) || N > (1 << 30))
     return fail(SV_ERR_INVALID_ARG, "qmv_smallm: N*K too large");
   const size_t wb = (size_t)N * K / 2, sbb = (size_t)N * (K / 64) * 2;
   const size_t xb = (size_t)M * K * (x_dtype == SV_F32 ? 4 : 2), yb = (size_t)M * N * 4;
@@ -395,32 +678,8 @@ extern "C" sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales
       overlaps(y, yb, biases, sbb) || overlaps(y, yb, x, xb))
     return fail(SV_ERR_INVALID_ARG, "qmv_smallm: y overlaps an input");
 
-  const int RT = N > 16 ? 2 : 1;
-  const int rows_cta = 16 * RT;
-  const int groups = K / 64;
-  const int ctas = (N + rows_cta - 1) / rows_cta;
-  const int n_chunks = (K + kStageInputs - 1) / kStageInputs;
-  const int sms = device_sm_count();
-  // co-resident CTAs wanted per SM so that one wave covers the grid
-  const int per_sm = std::min(8, std::max(1, (ctas + sms - 1) / std::max(1, sms)));
-  const size_t budget = (size_t)(220 * 1024) / per_sm;
-  const Layout base = qmv_layout(rows_cta, groups, 0);
-  const size_t stage_bytes = (size_t)rows_cta * kStageRowBytes + 16;
-  int stages = budget > base.total ? (int)((budget - base.total) / stage_bytes) : 2;
-  stages = std::max(2, std::min(stages, std::min(16, std::max(2, n_chunks))));
-  Layout L = qmv_layout(rows_cta, groups, stages);
-  int optin = 0;
-  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, current_device());
-  while (L.total > (size_t)optin && stages > 2) L = qmv_layout(rows_cta, groups, --stages);
-  if (L.total > (size_t)optin)
-    return fail(SV_ERR_UNSUPPORTED, "qmv_smallm: K=%d needs %zu bytes of shared memory", K,
-                L.total);
-
-  QmvArgs args{w_packed, scales, biases, x, y, M, N, K, stages};
+  // scale/bias rows are 16-byte aligned for the copy engine when K % 512 == 0
+  QmvArgs args{scales, biases, x, y, M, N, K, 0, 1, K % 512 == 0 ? 1 : 0};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (RT == 2)
-    return x_dtype == SV_BF16 ? launch<2, false>(args, ctas, L.total, s)
-                              : launch<2, true>(args, ctas, L.total, s);
-  return x_dtype == SV_BF16 ? launch<1, false>(args, ctas, L.total, s)
-                            : launch<1, true>(args, ctas, L.total, s);
+  return x_dtype == SV_BF16 ? launch<false>(w_packed, args, s) : launch<true>(w_packed, args, s);
 }
