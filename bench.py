@@ -565,6 +565,53 @@ def run_mlp(args):
     return 0
 
 
+def run_qmv(args):
+    """One projection shape (--shape N K) at M = depth + 1, on enough distinct
+    weight copies that they stream from HBM (> 300 MB in all), in one CUDA
+    graph without PDL; qmv_smallm GB/s.  Also the small case the ncu captures
+    of a single qmv_smallm launch run."""
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    N, K = args.shape
+    M = args.depth + 1
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.MASTER_SEED + 37)
+    per = qmv_bytes(M, N, K)
+    copies = max(4, -(-300_000_000 // per))
+    weights = []
+    for _ in range(copies):
+        w = torch.randint(-(2 ** 31), 2 ** 31 - 1, (N, K // 8), generator=g, device=dev,
+                          dtype=torch.int32)
+        s_ = (torch.randn((N, K // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        b_ = (torch.randn((N, K // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        weights.append((w, s_, b_))
+    x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty((M, N), device=dev)
+
+    def fn():
+        for w, s_, b_ in weights:
+            sv.qmv_smallm(w, s_, b_, x, y)
+
+    stream = torch.cuda.Stream(dev)
+    graph = capture(torch, fn, stream)
+    ms = time_graph(torch, graph, stream, args.steps, args.warmup)
+    us = ms / args.steps / copies * 1e3
+    gbs = per / (us / 1e6) / 1e9
+    peaks = measured_peaks()
+    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"qmv_smallm {K}->{N}, M={M}, {copies} distinct weight "
+                                   "copies in one CUDA graph", "l2": "inputs larger than L2"},
+            "us_per_call": us, "frac": gbs / peaks["hbm_gbs"], "peak": peaks}
+    print(json.dumps(line), flush=True)
+    sv.device_status()
+    return 0
+
+
 def run_lmhead(args):
     """LM-head verify + accept: 32 sequences x (M=4 LM-head qmv 5120->151936)
     then one spec_accept over the batch (draft = target + N(0, 0.5))."""
@@ -680,13 +727,18 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--depth", type=int, default=3, help="draft depth K (M = K+1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn"], default="cycle")
+    ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn", "qmv"],
+                    default="cycle")
+    ap.add_argument("--shape", type=int, nargs=2, metavar=("N", "K"),
+                    default=[wl.INTERMEDIATE, wl.HIDDEN],
+                    help="output and input size of the --workload qmv projection")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
-    return {"cycle": run_cycle, "mlp": run_mlp, "lmhead": run_lmhead, "gdn": run_gdn}[
+    return {"cycle": run_cycle, "mlp": run_mlp, "lmhead": run_lmhead, "gdn": run_gdn,
+            "qmv": run_qmv}[
         args.workload](args)
 
 

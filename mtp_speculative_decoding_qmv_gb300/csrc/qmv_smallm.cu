@@ -577,13 +577,15 @@ sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   const int ctas = tiles * splits;
   // fill shared memory with stages at the occupancy the grid will reach
   const int per_sm = std::max(1, std::min({(ctas + sms - 1) / sms, occ, 8}));
-  const uint32_t budget = (uint32_t)(224 * 1024) / per_sm - 1024u;
+  int smem_sm = 0;
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (smem_sm <= 0) smem_sm = 228 * 1024;
+  const uint32_t budget = (uint32_t)smem_sm / per_sm - 1024u;  // 1 KB reserved per CTA
   const bool sbs = args.sb_stream != 0;
-  const uint32_t fixed = qmv_layout(groups, 0, sbs).total;
-  const uint32_t stage_bytes = qmv_layout(groups, 1, sbs).stage + 16u;
   const int per_cta_chunks = (n_chunks + splits - 1) / splits;
-  int stages = budget > fixed ? (int)((budget - fixed) / stage_bytes) : 2;
-  stages = std::max(2, std::min(stages, std::min(32, std::max(2, per_cta_chunks))));
+  const int max_stages = std::min(32, std::max(2, per_cta_chunks));
+  int stages = 2;
+  while (stages < max_stages && qmv_layout(groups, stages + 1, sbs).total <= budget) ++stages;
   Layout L = qmv_layout(groups, stages, sbs);
   while (L.total > (uint32_t)optin && stages > 2) L = qmv_layout(groups, --stages, sbs);
   if (L.total > (uint32_t)optin)
