@@ -161,6 +161,32 @@ sv_status spec_accept(const float *target_logits, const float *draft_logits,
                       int32_t *n_accepted, int32_t *err_flags, void *workspace,
                       size_t workspace_bytes, sv_stream_t stream);
 
+/* spec_accept_noalloc: spec_accept on a scratch area that the library holds
+ * as a fixed-size device global (spec_accept_noalloc_scratch_bytes() bytes,
+ * 2 MiB: e.g. B <= 32 at K = 3, V = 151936).  The pages have no counterpart;
+ * this exists for callers that cannot allocate device memory: a plain C
+ * host loop that links only this library and has no device allocator of its
+ * own, or a decode loop that must not call cudaMalloc / cudaFree per step
+ * (cudaFree synchronises the device).
+ * Arguments, outputs, flags and results are those of spec_accept without the
+ * workspace pair; every call clears the scratch's counters and row flags on
+ * `stream` before the kernel.
+ * Errors: SV_ERR_UNSUPPORTED when spec_accept_workspace_bytes(B, K, V)
+ * exceeds the scratch size (nothing is launched; use spec_accept with a
+ * caller workspace); SV_ERR_CUDA when the scratch address cannot be looked
+ * up; otherwise spec_accept's.
+ * There is one scratch per device, so calls that overlap in time (different
+ * streams or host threads on one device) race on it and must be serialised
+ * by the caller.  The first call on each device looks the scratch address up
+ * (with that device current); make it before any stream capture begins. */
+size_t spec_accept_noalloc_scratch_bytes(void);
+
+sv_status spec_accept_noalloc(const float *target_logits, const float *draft_logits,
+                              const int32_t *draft_tokens, const float *u_accept,
+                              const float *u_sample, int B, int K, int V, sv_sampling sampling,
+                              int32_t *out_tokens, int32_t *n_accepted, int32_t *err_flags,
+                              sv_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* GatedDeltaNet innovation tape.                                            */
 /* ------------------------------------------------------------------------ */

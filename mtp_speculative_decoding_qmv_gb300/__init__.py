@@ -69,6 +69,10 @@ def lib() -> ctypes.CDLL:
         L.spec_accept_workspace_bytes.restype = Z
         L.spec_accept.argtypes = [P, P, P, P, P, I, I, I, _Sampling, P, P, P, P, Z, P]
         L.spec_accept.restype = I
+        L.spec_accept_noalloc_scratch_bytes.argtypes = []
+        L.spec_accept_noalloc_scratch_bytes.restype = Z
+        L.spec_accept_noalloc.argtypes = [P, P, P, P, P, I, I, I, _Sampling, P, P, P, P]
+        L.spec_accept_noalloc.restype = I
         L.gdn_tape_bytes.argtypes = [I, I, I, I, I]
         L.gdn_tape_bytes.restype = Z
         L.gdn_tape_capture.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P]
@@ -204,6 +208,39 @@ def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor | None,
                            workspace.numel(), _stream(dev))
     _check(st, "spec_accept")
     return out_tokens, n_accepted, err_flags
+
+
+def spec_accept_noalloc_scratch_bytes() -> int:
+    return int(lib().spec_accept_noalloc_scratch_bytes())
+
+
+def spec_accept_noalloc(target_logits: torch.Tensor, draft_logits: torch.Tensor | None,
+                        draft_tokens: torch.Tensor, u_accept: torch.Tensor,
+                        u_sample: torch.Tensor, temperature: float, top_k: int, top_p: float,
+                        out_tokens: torch.Tensor, n_accepted: torch.Tensor,
+                        err_flags: torch.Tensor | None = None) -> None:
+    """spec_accept on the library's fixed device scratch: the caller passes
+    every output, so nothing is allocated.  Calls on one device must not
+    overlap in time."""
+    dev = target_logits.device
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    _need(target_logits, "target_logits", torch.float32, (B, K + 1, V), dev)
+    if draft_logits is not None:
+        _need(draft_logits, "draft_logits", torch.float32, (B, K, V), dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
+    _need(u_accept, "u_accept", torch.float32, (B, K), dev)
+    _need(u_sample, "u_sample", torch.float32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
+    _need(n_accepted, "n_accepted", torch.int32, (B,), dev)
+    if err_flags is not None:
+        _need(err_flags, "err_flags", torch.int32, (B,), dev)
+    samp = _Sampling(float(temperature), int(top_k), float(top_p))
+    st = lib().spec_accept_noalloc(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
+                                   _ptr(u_accept), _ptr(u_sample), B, K, V, samp,
+                                   _ptr(out_tokens), _ptr(n_accepted), _ptr(err_flags),
+                                   _stream(dev))
+    _check(st, "spec_accept_noalloc")
 
 
 def gdn_tape_bytes(B: int, T: int, H: int, dk: int, dv: int) -> int:

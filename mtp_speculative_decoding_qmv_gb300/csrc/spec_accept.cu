@@ -29,6 +29,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
@@ -646,4 +647,75 @@ extern "C" sv_status spec_accept(const float *target_logits, const float *draft_
   dim3 grid((unsigned)args.C, (unsigned)(B * args.rows));
   spec_accept_kernel<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
   return check_launch("spec_accept");
+}
+
+// ---- spec_accept_noalloc: the same call on a fixed, statically sized scratch --
+//
+// For callers that cannot allocate device memory: a plain C host loop that
+// links only this library and owns no device allocator, or a decode loop that
+// must not call cudaMalloc / cudaFree per step (cudaFree synchronises the
+// whole device).  The scratch is one file-scope __device__ array, so there is
+// exactly one per device: calls that overlap in time (two streams, two host
+// threads) race on it.  The first call on a device looks up the array's
+// address; make that first call before any stream capture begins.
+namespace sv {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(2) << 20;  // 2 MiB
+__device__ __align__(256) unsigned char g_accept_scratch[kStaticScratchBytes];
+
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[kScratchDevices] = {};
+
+// Address of g_accept_scratch on the current device (looked up once per device).
+sv_status static_scratch(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchDevices)
+    return fail(SV_ERR_CUDA, "spec_accept_noalloc: no usable current device");
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_accept_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(SV_ERR_CUDA, "spec_accept_noalloc: cudaGetSymbolAddress failed on device %d: %s",
+                  dev, cudaGetErrorString(e));
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return SV_OK;
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" size_t spec_accept_noalloc_scratch_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" sv_status spec_accept_noalloc(const float *target_logits, const float *draft_logits,
+                                         const int32_t *draft_tokens, const float *u_accept,
+                                         const float *u_sample, int B, int K, int V,
+                                         sv_sampling sampling, int32_t *out_tokens,
+                                         int32_t *n_accepted, int32_t *err_flags,
+                                         sv_stream_t stream) {
+  clear_error();
+  // Sizes spec_accept rejects anyway (and B == 0, a no-op) go straight to it.
+  if (B <= 0 || K < 1 || K > kMaxK || V < 1 || (long long)V > (long long)kMaxChunks * kChunk)
+    return spec_accept(target_logits, draft_logits, draft_tokens, u_accept, u_sample, B, K, V,
+                       sampling, out_tokens, n_accepted, err_flags, nullptr, 0, stream);
+  const WsLayout W = ws_layout(B, K, V);
+  if (W.total > kStaticScratchBytes)
+    return fail(SV_ERR_UNSUPPORTED,
+                "spec_accept_noalloc: B=%d K=%d V=%d needs %zu bytes of scratch, the static "
+                "scratch holds %zu; use spec_accept with a caller workspace",
+                B, K, V, W.total, kStaticScratchBytes);
+  void *scratch = nullptr;
+  const sv_status st = static_scratch(&scratch);
+  if (st != SV_OK) return st;
+  // counters and row flags must start at zero (a completed call leaves them
+  // so; clearing them here also covers a call that never completed)
+  if (cudaMemsetAsync(scratch, 0, W.cand, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return fail(SV_ERR_CUDA, "spec_accept_noalloc: clearing the scratch counters failed");
+  return spec_accept(target_logits, draft_logits, draft_tokens, u_accept, u_sample, B, K, V,
+                     sampling, out_tokens, n_accepted, err_flags, scratch, kStaticScratchBytes,
+                     stream);
 }
