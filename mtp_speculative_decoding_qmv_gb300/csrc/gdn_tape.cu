@@ -13,11 +13,15 @@
 //   S' = alpha_t S;  u = S' k_t;  e_t = beta_t (v_t - u);  S_t = S' + e_t k_t^T;
 //   o_t = S_t q_t.
 // Rows of S never interact: row i needs only v_t[i] and the shared k_t, q_t,
-// alpha_t, beta_t.  So a CTA owns 64 rows of one head, a thread owns half a
-// row (64 fp32 in registers) and the only reduction is between the two
-// halves of a row (one shuffle).  The state element update is written as
-// separate round-to-nearest multiply, multiply, add (no contraction) in both
-// kernels, so replaying the tape reproduces the capture's states bit for bit.
+// alpha_t, beta_t.  A CTA owns 16 rows of one head; eight lanes share a row,
+// each holding 16 of its fp32 elements in registers as four float4 chunks at
+// columns 32c + 4j (lane j of the row), so every load and store of the state
+// is a run of 128 contiguous bytes per row and a warp covers four rows; the
+// row's dot products are finished with three shuffles.  Small batches still
+// give (dv / 16) x H CTAs (384 at H = 48, dv = 128).  The state element
+// update is written as separate round-to-nearest multiply, multiply, add (no
+// contraction) in both kernels, so replaying the tape reproduces the
+// capture's states bit for bit.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -28,10 +32,11 @@
 namespace sv {
 namespace {
 
-constexpr int kRowsPerCta = 64;
-constexpr int kThreads = 2 * kRowsPerCta;
-constexpr int kHalf = 64;          // columns per thread
-constexpr int kPadHalf = kHalf + 4;  // smem stride between the two column halves
+constexpr int kLanesPerRow = 8;
+constexpr int kChunks = 4;                   // float4 chunks per lane
+constexpr int kMaxDim = kLanesPerRow * kChunks * 4;  // 128
+constexpr int kRowsPerCta = 16;
+constexpr int kThreads = kRowsPerCta * kLanesPerRow;  // 128
 constexpr int kMaxT = 16;
 
 // Tape: one block per sequence b of tape_block_floats(T,H,dk,dv) floats, each
@@ -70,100 +75,115 @@ struct GdnArgs {
   int B, T, H, dk, dv;
 };
 
-__device__ __forceinline__ int pad_col(int j) { return j < kHalf ? j : j + (kPadHalf - kHalf); }
+// Column of element 4 * c of lane j's chunks.
+__device__ __forceinline__ int chunk_col(int j, int c) { return 32 * c + 4 * j; }
 
+// Row-local dot product finished across the row's eight lanes.
+__device__ __forceinline__ float row_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  return v;
+}
 
 __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) {
-  __shared__ __align__(16) float ks[2 * kPadHalf];
-  __shared__ __align__(16) float qs[2 * kPadHalf];
+  __shared__ __align__(16) float ks[kMaxT][kMaxDim];
+  __shared__ __align__(16) float qs[kMaxT][kMaxDim];
+  __shared__ float vs[kMaxT][kRowsPerCta];
+  __shared__ float als[kMaxT], bes[kMaxT];
   const int tid = threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
-  const int i = blockIdx.x * kRowsPerCta + (tid >> 1);  // state row (value dim)
-  const int half = tid & 1;
-  const int j0 = half * kHalf;
+  const int r0 = blockIdx.x * kRowsPerCta;
+  const int i = r0 + tid / kLanesPerRow;  // state row (value dim)
+  const int j = tid % kLanesPerRow;
   const bool row_ok = i < a.dv;
-  const int ncol = max(0, min(kHalf, a.dk - j0));  // valid columns, multiple of 4
-
-  float S[kHalf];
-  const float *src = a.state0 + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk + j0;
-#pragma unroll
-  for (int c = 0; c < kHalf; c += 4) {
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row_ok && c < ncol) f = *reinterpret_cast<const float4 *>(src + c);
-    S[c] = f.x;
-    S[c + 1] = f.y;
-    S[c + 2] = f.z;
-    S[c + 3] = f.w;
-  }
-
+  // the tokens' keys, queries, gates and this CTA's values, once
   for (int t = 0; t < a.T; ++t) {
     const size_t bth = ((size_t)b * a.T + t) * a.H + h;
-    if (tid < a.dk) {
-      ks[pad_col(tid)] = a.k[bth * a.dk + tid];
-      qs[pad_col(tid)] = a.q[bth * a.dk + tid];
+    for (int c = tid; c < a.dk; c += kThreads) {
+      ks[t][c] = a.k[bth * a.dk + c];
+      qs[t][c] = a.q[bth * a.dk + c];
     }
-    const float al = a.alpha[bth], be = a.beta[bth];
-    const float vi = row_ok ? a.v[bth * a.dv + i] : 0.f;
-    __syncthreads();
-    const float *kh = ks + half * kPadHalf;
-    const float *qh = qs + half * kPadHalf;
-    // S' = alpha S ; u = S' k
+    if (tid < kRowsPerCta) vs[t][tid] = r0 + tid < a.dv ? a.v[bth * a.dv + r0 + tid] : 0.f;
+    if (tid == 0) {
+      als[t] = a.alpha[bth];
+      bes[t] = a.beta[bth];
+    }
+  }
+
+  float S[kChunks * 4];
+  const float *src = a.state0 + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk;
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row_ok && chunk_col(j, c) < a.dk) f = *reinterpret_cast<const float4 *>(src + chunk_col(j, c));
+    S[4 * c] = f.x;
+    S[4 * c + 1] = f.y;
+    S[4 * c + 2] = f.z;
+    S[4 * c + 3] = f.w;
+  }
+  __syncthreads();
+
+  for (int t = 0; t < a.T; ++t) {
+    const float al = als[t], be = bes[t];
+    // S' = alpha S ; u = S' k   (chunks past dk hold zeros and contribute 0)
     float u = 0.f;
 #pragma unroll
-    for (int c = 0; c < kHalf; c += 4) {
-      if (c < ncol) {
-        const float4 kk = *reinterpret_cast<const float4 *>(kh + c);
-        S[c] = __fmul_rn(al, S[c]);
-        S[c + 1] = __fmul_rn(al, S[c + 1]);
-        S[c + 2] = __fmul_rn(al, S[c + 2]);
-        S[c + 3] = __fmul_rn(al, S[c + 3]);
-        u = fmaf(S[c], kk.x, u);
-        u = fmaf(S[c + 1], kk.y, u);
-        u = fmaf(S[c + 2], kk.z, u);
-        u = fmaf(S[c + 3], kk.w, u);
+    for (int c = 0; c < kChunks; ++c) {
+      S[4 * c] = __fmul_rn(al, S[4 * c]);
+      S[4 * c + 1] = __fmul_rn(al, S[4 * c + 1]);
+      S[4 * c + 2] = __fmul_rn(al, S[4 * c + 2]);
+      S[4 * c + 3] = __fmul_rn(al, S[4 * c + 3]);
+      if (chunk_col(j, c) < a.dk) {
+        const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
+        u = fmaf(S[4 * c], kk.x, u);
+        u = fmaf(S[4 * c + 1], kk.y, u);
+        u = fmaf(S[4 * c + 2], kk.z, u);
+        u = fmaf(S[4 * c + 3], kk.w, u);
       }
     }
-    u += __shfl_xor_sync(0xffffffffu, u, 1);
-    const float e = be * (vi - u);
+    u = row_sum(u);
+    const float e = be * (vs[t][tid / kLanesPerRow] - u);
     // S_t = S' + e k^T ; o = S_t q
     float o = 0.f;
 #pragma unroll
-    for (int c = 0; c < kHalf; c += 4) {
-      if (c < ncol) {
-        const float4 kk = *reinterpret_cast<const float4 *>(kh + c);
-        const float4 qq = *reinterpret_cast<const float4 *>(qh + c);
-        S[c] = __fadd_rn(S[c], __fmul_rn(e, kk.x));
-        S[c + 1] = __fadd_rn(S[c + 1], __fmul_rn(e, kk.y));
-        S[c + 2] = __fadd_rn(S[c + 2], __fmul_rn(e, kk.z));
-        S[c + 3] = __fadd_rn(S[c + 3], __fmul_rn(e, kk.w));
-        o = fmaf(S[c], qq.x, o);
-        o = fmaf(S[c + 1], qq.y, o);
-        o = fmaf(S[c + 2], qq.z, o);
-        o = fmaf(S[c + 3], qq.w, o);
+    for (int c = 0; c < kChunks; ++c) {
+      if (chunk_col(j, c) < a.dk) {
+        const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
+        const float4 qq = *reinterpret_cast<const float4 *>(&qs[t][chunk_col(j, c)]);
+        S[4 * c] = __fadd_rn(S[4 * c], __fmul_rn(e, kk.x));
+        S[4 * c + 1] = __fadd_rn(S[4 * c + 1], __fmul_rn(e, kk.y));
+        S[4 * c + 2] = __fadd_rn(S[4 * c + 2], __fmul_rn(e, kk.z));
+        S[4 * c + 3] = __fadd_rn(S[4 * c + 3], __fmul_rn(e, kk.w));
+        o = fmaf(S[4 * c], qq.x, o);
+        o = fmaf(S[4 * c + 1], qq.y, o);
+        o = fmaf(S[4 * c + 2], qq.z, o);
+        o = fmaf(S[4 * c + 3], qq.w, o);
       }
     }
-    o += __shfl_xor_sync(0xffffffffu, o, 1);
-    if (row_ok && half == 0) {
+    o = row_sum(o);
+    const size_t bth = ((size_t)b * a.T + t) * a.H + h;
+    if (row_ok && j == 0) {
       a.tape.e(b, t, h)[i] = e;
       if (a.out) a.out[bth * a.dv + i] = o;
     }
     if (blockIdx.x == 0) {
-      if (tid < a.dk) a.tape.k(b, t, h)[tid] = ks[pad_col(tid)];
+      for (int c = tid; c < a.dk; c += kThreads) a.tape.k(b, t, h)[c] = ks[t][c];
       if (tid == 0) *a.tape.alpha(b, t, h) = al;
     }
-    __syncthreads();
   }
   if (a.state_out && row_ok) {
-    float *dst = a.state_out + (((size_t)b * a.H + h) * a.dv + i) * a.dk + j0;
+    float *dst = a.state_out + (((size_t)b * a.H + h) * a.dv + i) * a.dk;
 #pragma unroll
-    for (int c = 0; c < kHalf; c += 4)
-      if (c < ncol)
-        *reinterpret_cast<float4 *>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+    for (int c = 0; c < kChunks; ++c)
+      if (chunk_col(j, c) < a.dk)
+        *reinterpret_cast<float4 *>(dst + chunk_col(j, c)) =
+            make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
   }
 }
 
 __global__ void __launch_bounds__(kThreads) gdn_replay_kernel(const GdnArgs a) {
-  __shared__ __align__(16) float ks[kMaxT][2 * kPadHalf];
+  __shared__ __align__(16) float ks[kMaxT][kMaxDim];
   __shared__ float es[kMaxT][kRowsPerCta];
   __shared__ float als[kMaxT];
   const int tid = threadIdx.x;
@@ -175,51 +195,52 @@ __global__ void __launch_bounds__(kThreads) gdn_replay_kernel(const GdnArgs a) {
     atomicOr(&a.err_flags[b], SV_FLAG_REPLAY_RANGE);
   if (L == 0) return;  // nothing accepted: the state is untouched
   const int r0 = blockIdx.x * kRowsPerCta;
-  const int i = r0 + (tid >> 1);
-  const int half = tid & 1;
-  const int j0 = half * kHalf;
+  const int i = r0 + tid / kLanesPerRow;
+  const int j = tid % kLanesPerRow;
   const bool row_ok = i < a.dv;
-  const int ncol = max(0, min(kHalf, a.dk - j0));
   for (int t = 0; t < L; ++t) {
-    if (tid < a.dk) ks[t][pad_col(tid)] = a.tape.k(b, t, h)[tid];
+    for (int c = tid; c < a.dk; c += kThreads) ks[t][c] = a.tape.k(b, t, h)[c];
     if (tid < kRowsPerCta) es[t][tid] = r0 + tid < a.dv ? a.tape.e(b, t, h)[r0 + tid] : 0.f;
     if (tid == 0) als[t] = *a.tape.alpha(b, t, h);
   }
-  float S[kHalf];
-  float *dst = a.state + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk + j0;
+  float S[kChunks * 4];
+  float *dst = a.state + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk;
 #pragma unroll
-  for (int c = 0; c < kHalf; c += 4) {
+  for (int c = 0; c < kChunks; ++c) {
     float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row_ok && c < ncol) f = *reinterpret_cast<const float4 *>(dst + c);
-    S[c] = f.x;
-    S[c + 1] = f.y;
-    S[c + 2] = f.z;
-    S[c + 3] = f.w;
+    if (row_ok && chunk_col(j, c) < a.dk) f = *reinterpret_cast<const float4 *>(dst + chunk_col(j, c));
+    S[4 * c] = f.x;
+    S[4 * c + 1] = f.y;
+    S[4 * c + 2] = f.z;
+    S[4 * c + 3] = f.w;
   }
   __syncthreads();
   if (!row_ok) return;
   for (int t = 0; t < L; ++t) {
-    const float al = als[t], et = es[t][tid >> 1];
-    const float *kh = &ks[t][half * kPadHalf];
+    const float al = als[t], et = es[t][tid / kLanesPerRow];
 #pragma unroll
-    for (int c = 0; c < kHalf; c += 4) {
-      const float4 kk = *reinterpret_cast<const float4 *>(kh + c);
-      S[c] = __fadd_rn(__fmul_rn(al, S[c]), __fmul_rn(et, kk.x));
-      S[c + 1] = __fadd_rn(__fmul_rn(al, S[c + 1]), __fmul_rn(et, kk.y));
-      S[c + 2] = __fadd_rn(__fmul_rn(al, S[c + 2]), __fmul_rn(et, kk.z));
-      S[c + 3] = __fadd_rn(__fmul_rn(al, S[c + 3]), __fmul_rn(et, kk.w));
+    for (int c = 0; c < kChunks; ++c) {
+      if (chunk_col(j, c) < a.dk) {
+        const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
+        S[4 * c] = __fadd_rn(__fmul_rn(al, S[4 * c]), __fmul_rn(et, kk.x));
+        S[4 * c + 1] = __fadd_rn(__fmul_rn(al, S[4 * c + 1]), __fmul_rn(et, kk.y));
+        S[4 * c + 2] = __fadd_rn(__fmul_rn(al, S[4 * c + 2]), __fmul_rn(et, kk.z));
+        S[4 * c + 3] = __fadd_rn(__fmul_rn(al, S[4 * c + 3]), __fmul_rn(et, kk.w));
+      }
     }
   }
 #pragma unroll
-  for (int c = 0; c < kHalf; c += 4)
-    if (c < ncol) *reinterpret_cast<float4 *>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+  for (int c = 0; c < kChunks; ++c)
+    if (chunk_col(j, c) < a.dk)
+      *reinterpret_cast<float4 *>(dst + chunk_col(j, c)) =
+          make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
 }
 
 sv_status validate(const char *who, int B, int T, int H, int dk, int dv) {
   if (B < 0 || T < 1 || H < 1 || dk < 1 || dv < 1)
     return fail(SV_ERR_INVALID_ARG, "%s: need B >= 0, T, H, dk, dv >= 1", who);
   if (T > kMaxT) return fail(SV_ERR_UNSUPPORTED, "%s: T=%d > %d", who, T, kMaxT);
-  if (dk > 2 * kHalf || dv > 2 * kHalf || dk % 4 || dv % 4)
+  if (dk > kMaxDim || dv > kMaxDim || dk % 4 || dv % 4)
     return fail(SV_ERR_UNSUPPORTED, "%s: dk, dv must be multiples of 4 and <= 128 (dk=%d dv=%d)",
                 who, dk, dv);
   if ((long long)H > 65535 || (long long)B > 65535)
