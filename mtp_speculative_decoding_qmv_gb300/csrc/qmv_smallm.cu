@@ -48,39 +48,16 @@
 //  * programmatic dependent launch: the weight stream starts before the
 //    preceding kernel on the stream ends; activations are read, and y
 //    written, only after griddepcontrol.wait.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-
 #include <algorithm>
-#include <cstdint>
-#include <mutex>
 
-#include "sv_device.cuh"
-#include "sv_internal.h"
+#include "qmv_common.cuh"
 
 namespace sv {
 namespace {
+using namespace qmv;
 
-constexpr int kRows = 64;                          // output rows per CTA (4 MMA tiles)
-constexpr int kTiles = kRows / 16;
-constexpr int kConsumerWarps = 8;                  // one 64-group each per stage
-constexpr int kStageInputs = kConsumerWarps * 64;  // 512 inputs per stage
-constexpr int kBoxWords = 32;                      // 128-byte box rows = 256 inputs
-constexpr int kBoxesPerStage = kStageInputs / (kBoxWords * 8);  // 2
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSplits = 8;                      // portable cluster size
-constexpr uint32_t kBf16One2 = 0x3F803F80u;        // bf16x2 (1, 1)
-constexpr uint32_t kNibbleMask = 0x000F000Fu;
-constexpr uint32_t kBf16Base = 0x43004300u;        // bf16x2 (128, 128)
-
-// stage: [2 boxes][64 rows x 128 B] (swizzled) then, when streamed, scales
-// [64][8] and biases [64][8] (bf16); 1024-byte multiple
-constexpr uint32_t kSbOff = kBoxesPerStage * kRows * 128;
-constexpr uint32_t kStageBytesStream = (kSbOff + 2 * kRows * 16 + 1023) / 1024 * 1024;
-constexpr uint32_t kStageBytesBlock = (kSbOff + 1023) / 1024 * 1024;
-constexpr uint32_t kRedBytes = kConsumerWarps * kRows * 8 * 4;  // cross-warp partials
-
+constexpr int kMinCtasPerSm = 2;                   // register budget: 113 per thread
 __device__ unsigned int g_qmv_device_error;
 
 struct QmvArgs {
@@ -116,25 +93,6 @@ __host__ __device__ inline Layout qmv_layout(int groups, int stages, bool sb_str
   return L;
 }
 
-// ---- device helpers --------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -153,98 +111,10 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// Raw activation data of one 64-group for the lane's activation row m: the A
-// operand (ldmatrix) gives lane (g = lane/4, t = lane%4) packed words t and
-// 4+t of the group, i.e. inputs 8t + [0,8) and 32 + 8t + [0,8), so the lane
-// loads those 16 inputs.
-template <bool kXF32>
-struct XRaw {
-  uint4 v[kXF32 ? 4 : 2];
-};
-
-template <bool kXF32>
-__device__ __forceinline__ XRaw<kXF32> load_x(const void *xrow, bool valid, int g, int t) {
-  XRaw<kXF32> r;
-#pragma unroll
-  for (int i = 0; i < (kXF32 ? 4 : 2); ++i) r.v[i] = make_uint4(0, 0, 0, 0);
-  if (valid) {
-    if constexpr (!kXF32) {
-      const uint16_t *p = static_cast<const uint16_t *>(xrow) + g * 64 + 8 * t;
-      r.v[0] = *reinterpret_cast<const uint4 *>(p);
-      r.v[1] = *reinterpret_cast<const uint4 *>(p + 32);
-    } else {
-      const float *p = static_cast<const float *>(xrow) + g * 64 + 8 * t;
-      r.v[0] = *reinterpret_cast<const uint4 *>(p);
-      r.v[1] = *reinterpret_cast<const uint4 *>(p + 4);
-      r.v[2] = *reinterpret_cast<const uint4 *>(p + 32);
-      r.v[3] = *reinterpret_cast<const uint4 *>(p + 36);
-    }
-  }
-  return r;
-}
-
-// B fragments from the raw activations.  Each packed word feeds two k16 MMA
-// steps whose k order pairs input j with input j+4 (the order the nibble
-// widening produces), so B takes the same pairs.  fp32 rows become
-// x = hi + lo with both parts bf16.
-template <bool kXF32>
-__device__ __forceinline__ void b_fragments(const XRaw<kXF32> &r, uint32_t (&hi)[8],
-                                            uint32_t (&lo)[8]) {
-  if constexpr (!kXF32) {
-#pragma unroll
-    for (int slot = 0; slot < 2; ++slot) {
-      const uint4 v = r.v[slot];
-      hi[4 * slot + 0] = prmt(v.x, v.z, 0x5410);  // (x0, x4)
-      hi[4 * slot + 1] = prmt(v.x, v.z, 0x7632);  // (x1, x5)
-      hi[4 * slot + 2] = prmt(v.y, v.w, 0x5410);  // (x2, x6)
-      hi[4 * slot + 3] = prmt(v.y, v.w, 0x7632);  // (x3, x7)
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) lo[i] = 0;
-  } else {
-#pragma unroll
-    for (int slot = 0; slot < 2; ++slot) {
-      const uint4 u0 = r.v[2 * slot], u1 = r.v[2 * slot + 1];
-      const float v[8] = {__uint_as_float(u0.x), __uint_as_float(u0.y), __uint_as_float(u0.z),
-                          __uint_as_float(u0.w), __uint_as_float(u1.x), __uint_as_float(u1.y),
-                          __uint_as_float(u1.z), __uint_as_float(u1.w)};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(v[j], v[j + 4]);
-        const __nv_bfloat162 l =
-            __floats2bfloat162_rn(v[j] - __low2float(h), v[j + 4] - __high2float(h));
-        hi[4 * slot + j] = *reinterpret_cast<const uint32_t *>(&h);
-        lo[4 * slot + j] = *reinterpret_cast<const uint32_t *>(&l);
-      }
-    }
-  }
-}
-
-// Two k16 MMA steps for one packed word (8 inputs) of rows g and g+8.
-// Widening: (w >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair
-// (128 + q_j, 128 + q_{j+4}).
-template <bool kXF32>
-__device__ __forceinline__ void mma_word(float (&d)[4], uint32_t wr, uint32_t wr8,
-                                         const uint32_t *hi, const uint32_t *lo) {
-  const uint32_t a0 = and_or(wr, kNibbleMask, kBf16Base);
-  const uint32_t a0r8 = and_or(wr8, kNibbleMask, kBf16Base);
-  const uint32_t a1 = and_or(wr >> 4, kNibbleMask, kBf16Base);
-  const uint32_t a1r8 = and_or(wr8 >> 4, kNibbleMask, kBf16Base);
-  const uint32_t a2 = and_or(wr >> 8, kNibbleMask, kBf16Base);
-  const uint32_t a2r8 = and_or(wr8 >> 8, kNibbleMask, kBf16Base);
-  const uint32_t a3 = and_or(wr >> 12, kNibbleMask, kBf16Base);
-  const uint32_t a3r8 = and_or(wr8 >> 12, kNibbleMask, kBf16Base);
-  mma_bf16_m16n8k16(d, a0, a0r8, a1, a1r8, hi[0], hi[1]);
-  mma_bf16_m16n8k16(d, a2, a2r8, a3, a3r8, hi[2], hi[3]);
-  if constexpr (kXF32) {
-    mma_bf16_m16n8k16(d, a0, a0r8, a1, a1r8, lo[0], lo[1]);
-    mma_bf16_m16n8k16(d, a2, a2r8, a3, a3r8, lo[2], lo[3]);
-  }
-}
-
 // Producer: expect chunk c's bytes on stage st's barrier and issue its boxes.
 // Rows past N, inputs past K and groups past K/64 are zero-filled by the copy
 // engine and still counted in the transaction bytes.
+template <bool kStream>
 __device__ __forceinline__ void issue_stage(const QmvArgs &a, const CUtensorMap *wmap,
                                             const CUtensorMap *smap, const CUtensorMap *bmap,
                                             uint32_t stage_addr, uint32_t bar, int c, int n0,
@@ -252,19 +122,21 @@ __device__ __forceinline__ void issue_stage(const QmvArgs &a, const CUtensorMap 
   const int k0 = c * kStageInputs;
   const int kn = min(kStageInputs, a.K - k0);
   const int boxes = (kn + kBoxWords * 8 - 1) / (kBoxWords * 8);
-  const uint32_t bytes = (uint32_t)(boxes * kRows * 128 + (a.sb_stream ? 2 * kRows * 16 : 0));
+  const uint32_t bytes = (uint32_t)(boxes * kRows * 128 + (kStream ? 2 * kRows * 16 : 0));
   mbar_arrive_expect_tx_u32(bar, bytes);
   for (int bx = 0; bx < boxes; ++bx)
     tma_load_2d(stage_addr + bx * kRows * 128, wmap, k0 / 8 + bx * kBoxWords, n0, bar, policy);
-  if (a.sb_stream) {
+  if (kStream) {
     tma_load_2d(stage_addr + kSbOff, smap, k0 / 64, n0, bar, policy);
     tma_load_2d(stage_addr + kSbOff + kRows * 16, bmap, k0 / 64, n0, bar, policy);
   }
 }
 
-// three CTAs per SM (<= 75 registers per thread) keep 24 consumer warps resident
-template <bool kXF32>
-__global__ void __launch_bounds__(kThreads, 3)
+// kStream: K % 512 == 0, scales and biases stream with the stages and every
+// group of every stage is real; otherwise the tile's whole scale block is
+// loaded once and groups past K/64 are skipped.
+template <bool kXF32, bool kStream>
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     qmv_smallm_kernel(const __grid_constant__ CUtensorMap wmap,
                       const __grid_constant__ CUtensorMap smap,
                       const __grid_constant__ CUtensorMap bmap, const QmvArgs a) {
@@ -283,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int c_begin = (int)((long long)split * n_chunks / splits);
   const int c_end = (int)((long long)(split + 1) * n_chunks / splits);
   const int stages = a.stages;
-  const Layout L = qmv_layout(groups, stages, a.sb_stream != 0);
+  const Layout L = qmv_layout(groups, stages, kStream);
   const uint32_t full0 = base + L.bar;          // full[i]  = full0 + 8 i
   const uint32_t empty0 = full0 + 8u * stages;  // empty[i] = empty0 + 8 i
   const uint32_t sb_bar = empty0 + 8u * stages;
@@ -310,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     uint16_t *b_sm = s_sm + kRows * groups;
     uint64_t *sb_bar_p = reinterpret_cast<uint64_t *>(smem + (sb_bar - base));
     const uint32_t sb_bytes = (uint32_t)rows * groups * 2;
-    if (a.sb_stream) {
+    if (kStream) {
       mbar_arrive_u32(sb_bar);
     } else if (sb_bytes % 16u == 0) {
       if (lane == 0) {
@@ -339,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                                 ((i - c_begin) / stages) & 1);
           break;
         }
-        issue_stage(a, &wmap, &smap, &bmap, base + st * L.stage, full0 + 8u * st, c, n0,
+        issue_stage<kStream>(a, &wmap, &smap, &bmap, base + st * L.stage, full0 + 8u * st, c, n0,
                     policy);
         if (++st == stages) {
           st = 0;
@@ -352,20 +224,14 @@ __global__ void __launch_bounds__(kThreads, 3)
   } else {
     // ------------------------------ consumers -----------------------------
     const int g8 = lane >> 2, t = lane & 3;  // fragment row (= activation row m) and column
-    const bool m_valid = g8 < a.M;
     const int gl = warp;  // the stage's group this warp reduces
-    // ldmatrix.x4 addresses: lane L reads row ((L >> 3) & 1) * 8 + (L & 7) of
-    // an MMA tile, 16-byte chunk 2 * (gl % 4) + (L >> 4) of the 128-byte box
-    // row, at its swizzled position (chunk ^ row % 8)
-    const int lrow = ((lane >> 3) & 1) * 8 + (lane & 7);
-    const int lchunk = ((gl & 3) << 1) + (lane >> 4);
-    const uint32_t ldm_off =
-        (uint32_t)((gl >> 2) * kRows * 128 + lrow * 128 + ((lchunk ^ (lrow & 7)) << 4));
+    const uint32_t ldm_off = ldmatrix_offset(gl, lane);
     // scale / bias of rows g8 and g8+8 of tile 0, group gl (streamed layout)
     const uint32_t sb_off = kSbOff + (uint32_t)(g8 * 16 + gl * 2);
     const uint32_t blk = base + L.sb;  // whole-tile block (not streamed)
+    // lanes of padding columns (m >= M) read row 0; their sums are never stored
     const void *xrow = static_cast<const uint8_t *>(a.x) +
-                       (size_t)(m_valid ? g8 : 0) * a.K * (kXF32 ? 4 : 2);
+                       (size_t)(g8 < a.M ? g8 : 0) * a.K * (kXF32 ? 4 : 2);
     float acc[kTiles][4];
 #pragma unroll
     for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -373,60 +239,26 @@ __global__ void __launch_bounds__(kThreads, 3)
     ok = __all_sync(0xffffffffu, mbar_wait_u32(sb_bar, 0));
     pdl_wait();  // x and y belong to the preceding kernel until here
     int g = c_begin * kConsumerWarps + gl;
-    XRaw<kXF32> xnext = load_x<kXF32>(xrow, m_valid && g < groups, g, t);
+    // groups past K/64 (last stage of a ragged K) read a real group's
+    // activations; their weights are skipped
+    XRaw<kXF32> xnext = load_x<kXF32>(xrow, true, kStream ? g : min(g, groups - 1), t);
     int st = 0, ph = 0;  // stage of chunk c and the parity of its fill
     for (int c = c_begin; ok && c < c_end; ++c, g += kConsumerWarps) {
       const XRaw<kXF32> xcur = xnext;
-      const int gn = g + kConsumerWarps;  // next stage's group: its loads fly during the wait
-      if (c + 1 < c_end) xnext = load_x<kXF32>(xrow, m_valid && gn < groups, gn, t);
-      if (!__all_sync(0xffffffffu, mbar_wait_u32(full0 + 8u * st, ph))) {
+      // next stage's activations: the loads fly during this stage's work
+      const int gn = min(g + kConsumerWarps, groups - 1);
+      xnext = load_x<kXF32>(xrow, true, gn, t);
+      if (!warp_wait_stage(full0 + 8u * st, ph)) {
         ok = false;
         break;
       }
       const uint32_t stage = base + st * L.stage;
-      if (g < groups) {
-        uint32_t hi[8], lo[8];
-        b_fragments<kXF32>(xcur, hi, lo);
-        float xs[4] = {0.f, 0.f, 0.f, 0.f};  // sum of x over the group, cols 2t, 2t+1
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          mma_bf16_m16n8k16(xs, kBf16One2, kBf16One2, kBf16One2, kBf16One2, hi[2 * s],
-                            hi[2 * s + 1]);
-          if constexpr (kXF32)
-            mma_bf16_m16n8k16(xs, kBf16One2, kBf16One2, kBf16One2, kBf16One2, lo[2 * s],
-                              lo[2 * s + 1]);
-        }
-#pragma unroll
-        for (int rt = 0; rt < kTiles; ++rt) {
-          // words t, 4+t of the group for rows g8 and g8+8 of MMA tile rt
-          uint32_t w[4];
-          ldmatrix_x4(w, stage + ldm_off + rt * 16 * 128);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_word<kXF32>(d, w[0], w[1], hi, lo);
-          mma_word<kXF32>(d, w[2], w[3], hi + 4, lo + 4);
-          uint32_t sr, s8, br, b8;
-          if (a.sb_stream) {  // [64][8] scales then [64][8] biases of this stage
-            const uint32_t p = stage + sb_off + rt * 16 * 16;
-            sr = lds_u16(p);
-            s8 = lds_u16(p + 8 * 16);
-            br = lds_u16(p + kRows * 16);
-            b8 = lds_u16(p + kRows * 16 + 8 * 16);
-          } else {
-            const uint32_t p = blk + (uint32_t)(((rt * 16 + g8) * groups + g) * 2);
-            const uint32_t q = p + (uint32_t)(kRows * groups * 2);
-            sr = lds_u16(p);
-            s8 = lds_u16(p + 8 * groups * 2);
-            br = lds_u16(q);
-            b8 = lds_u16(q + 8 * groups * 2);
-          }
-          const float s0 = bf16_bits_to_float(sr), s1 = bf16_bits_to_float(s8);
-          const float c0 = fmaf(-128.f, s0, bf16_bits_to_float(br));
-          const float c1 = fmaf(-128.f, s1, bf16_bits_to_float(b8));
-          acc[rt][0] = fmaf(s0, d[0], fmaf(c0, xs[0], acc[rt][0]));
-          acc[rt][1] = fmaf(s0, d[1], fmaf(c0, xs[1], acc[rt][1]));
-          acc[rt][2] = fmaf(s1, d[2], fmaf(c1, xs[0], acc[rt][2]));
-          acc[rt][3] = fmaf(s1, d[3], fmaf(c1, xs[1], acc[rt][3]));
-        }
+      if constexpr (kStream) {  // [64][8] scales then [64][8] biases of this stage
+        group_math<kXF32>(acc, stage + ldm_off, xcur, stage + sb_off, 16 * 16, 8 * 16, kRows * 16);
+      } else if (g < groups) {  // the tile's whole [64][groups] block
+        const uint32_t gb = (uint32_t)groups * 2;
+        group_math<kXF32>(acc, stage + ldm_off, xcur, blk + (uint32_t)(g8 * groups + g) * 2,
+                          16 * gb, 8 * gb, kRows * gb);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
@@ -495,64 +327,26 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-// cuTensorMapEncodeTiled from the driver, found through the runtime (no link
-// dependency on libcuda).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-sv_status encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *ptr,
-                    uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
-                    uint32_t box_rows, CUtensorMapSwizzle swizzle) {
-  EncodeTiledFn enc = encode_tiled();
-  if (!enc) return fail(SV_ERR_CUDA, "qmv_smallm: cuTensorMapEncodeTiled is unavailable");
-  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(SV_ERR_CUDA, "qmv_smallm: tensor map encode failed (%d)", (int)r);
-  return SV_OK;
-}
-
 // Co-resident CTAs per SM allowed by registers and threads (cached per device).
-template <bool kXF32>
+template <bool kXF32, bool kStream>
 int occupancy_without_smem(int dev) {
   static int cached[64] = {};
   if (dev < 0 || dev >= 64) return 1;
   if (cached[dev] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmv_smallm_kernel<kXF32>, kThreads,
-                                                      0) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmv_smallm_kernel<kXF32, kStream>,
+                                                      kThreads, 0) != cudaSuccess || n < 1)
       n = 1;
     cached[dev] = n;
   }
   return cached[dev];
 }
 
-template <bool kXF32>
+template <bool kXF32, bool kStream>
 sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   static bool configured[64] = {};
   const int dev = current_device();
-  auto kern = qmv_smallm_kernel<kXF32>;
+  auto kern = qmv_smallm_kernel<kXF32, kStream>;
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
@@ -565,11 +359,11 @@ sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   const int tiles = (args.N + kRows - 1) / kRows;
   const int n_chunks = (args.K + kStageInputs - 1) / kStageInputs;
   const int sms = device_sm_count();
-  const int occ = occupancy_without_smem<kXF32>(dev);
+  const int occ = occupancy_without_smem<kXF32, kStream>(dev);
   // split K over a cluster when the row tiles alone would leave CTA slots
   // idle, as far as the grid still fits in one wave of resident CTAs
   int splits = 1;
-  if (args.sb_stream) {
+  if (kStream) {
     const int fit = (occ * sms) / tiles;
     splits = std::max(1, std::min({fit, kMaxSplits, n_chunks}));
   }
@@ -581,7 +375,7 @@ sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (smem_sm <= 0) smem_sm = 228 * 1024;
   const uint32_t budget = (uint32_t)smem_sm / per_sm - 1024u;  // 1 KB reserved per CTA
-  const bool sbs = args.sb_stream != 0;
+  const bool sbs = kStream;
   const int per_cta_chunks = (n_chunks + splits - 1) / splits;
   const int max_stages = std::min(32, std::max(2, per_cta_chunks));
   int stages = 2;
@@ -683,5 +477,9 @@ extern "C" sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales
   // scale/bias rows are 16-byte aligned for the copy engine when K % 512 == 0
   QmvArgs args{scales, biases, x, y, M, N, K, 0, 1, K % 512 == 0 ? 1 : 0};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return x_dtype == SV_BF16 ? launch<false>(w_packed, args, s) : launch<true>(w_packed, args, s);
+  if (args.sb_stream)
+    return x_dtype == SV_BF16 ? launch<false, true>(w_packed, args, s)
+                              : launch<true, true>(w_packed, args, s);
+  return x_dtype == SV_BF16 ? launch<false, false>(w_packed, args, s)
+                            : launch<true, false>(w_packed, args, s);
 }
