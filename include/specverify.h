@@ -13,6 +13,7 @@
  *
  * This library provides the data-parallel steps of that cycle:
  *   qmv_smallm        the target's 4-bit small-M quantised mat-vec (M = 1..8)
+ *   qmv_plan_*        an ordered list of those mat-vecs in one persistent launch
  *   spec_accept       fp32 acceptance, residual resampling and bonus token
  *   gdn_tape_capture  GatedDeltaNet recurrence over the verify tokens, with a
  *                     (gate, innovation, key) tape per token and head
@@ -20,8 +21,9 @@
  *
  * Conventions (all entry points):
  *  - Every tensor argument is a DEVICE pointer owned by the caller, to
- *    contiguous row-major memory.  The library keeps no pointer after a call
- *    returns and allocates no device memory.
+ *    contiguous row-major memory.  The library allocates no device memory and
+ *    keeps no pointer after a call returns, except a qmv plan (below), which
+ *    holds the pointers it was created with.
  *  - Calls are asynchronous on `stream` (NULL = the legacy default stream) and
  *    never synchronise with the host.
  *  - Arguments are validated on the host before any launch.  A nonzero status
@@ -108,6 +110,59 @@ sv_status sv_device_status(void);
 sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales, const uint16_t *biases,
                      const void *x, sv_dtype x_dtype, float *y, int M, int N, int K,
                      int group_size, int bits, sv_stream_t stream);
+
+/* qmv plan: an ordered list of qmv_smallm problems run by one launch.
+ * Sources: "MTPLX 2.24x faster TPS", section "Layer 0: MLX Runtime" (the
+ * verify forward streams every 4-bit projection of the target model for M =
+ * K+1 rows) and "MTP in llama.cpp", section "Theoretical maximum tg t/s" (a
+ * decode step is bounded by streaming the active weights once at memory
+ * bandwidth).  A verify forward is hundreds of projections; as separate
+ * launches each pays a launch and the latency of its first weight stage, so
+ * the weight stream stalls at every boundary.  A plan runs the whole list in
+ * one persistent launch whose weight stream never stops: problem i reads its
+ * activations x only after every earlier problem has written y when
+ * `after` is set (x is an earlier output), and at once otherwise.
+ *
+ * Each problem: Y[M][N] (fp32) = X[M][K] . W^T with W as in qmv_smallm
+ * (w_packed uint32 [N][K/8], scales and biases bf16 [N][K/64], group 64,
+ * 4 bits); K % 512 == 0; pointers 16-byte aligned (y 4-byte); y may not
+ * overlap the problem's inputs, and a problem may read an earlier output
+ * only if `after` is set on it or on a problem between them.  M (1..8) and
+ * the activation dtype are shared by all problems.  Results equal
+ * qmv_smallm's up to fp32 summation order and are deterministic run to run.
+ *
+ * qmv_plan_device_bytes: device bytes the plan needs (0 on invalid input;
+ * see sv_last_error).  qmv_plan_create: validates, encodes the tensor maps
+ * and copies them, with zeroed counters, into `device_buffer` (caller-owned,
+ * 256-byte aligned, at least qmv_plan_device_bytes; synchronous; the device
+ * current at creation runs the plan); *plan_out is a host object freed by
+ * qmv_plan_destroy.  The buffer and every problem's tensors must stay valid
+ * while the plan is used.  qmv_plan_run: one cooperative launch on `stream`
+ * (capturable in a CUDA graph); runs of one plan must not overlap in time.
+ * A phase wait that exceeds ~1 s sets a device error word
+ * (sv_device_status) and the launch finishes with invalid results; the
+ * plan's counters are then undefined: create it again. */
+typedef struct {
+    const uint32_t *w_packed;
+    const uint16_t *scales;
+    const uint16_t *biases;
+    const void *x;  /* [M][K] of the plan's dtype */
+    float *y;       /* [M][N] */
+    int N, K;
+    int after;      /* 1: x is written by an earlier problem of the list */
+} sv_qmv_problem;
+
+typedef struct sv_qmv_plan sv_qmv_plan;
+
+size_t qmv_plan_device_bytes(const sv_qmv_problem *problems, int n_problems, int M,
+                             sv_dtype x_dtype);
+sv_status qmv_plan_create(const sv_qmv_problem *problems, int n_problems, int M,
+                          sv_dtype x_dtype, void *device_buffer, size_t device_bytes,
+                          sv_qmv_plan **plan_out);
+sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream);
+void qmv_plan_destroy(sv_qmv_plan *plan);
+/* CTAs of the plan's launch (the co-resident count), 0 for NULL. */
+int qmv_plan_grid(const sv_qmv_plan *plan);
 
 /* ------------------------------------------------------------------------ */
 /* spec_accept: probability-ratio verification of K drafts per sequence.     */

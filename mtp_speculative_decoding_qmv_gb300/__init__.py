@@ -21,7 +21,8 @@ import torch
 __all__ = [
     "SvError", "lib", "abi_version", "qmv_smallm", "spec_accept", "spec_accept_workspace_bytes",
     "make_accept_workspace", "gdn_tape_bytes", "gdn_tape_capture", "gdn_tape_replay",
-    "set_pdl", "get_pdl", "device_status", "FLAGS",
+    "set_pdl", "get_pdl", "device_status", "FLAGS", "QmvPlan", "spec_accept_noalloc",
+    "spec_accept_noalloc_scratch_bytes",
 ]
 
 _LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
@@ -41,6 +42,12 @@ class SvError(RuntimeError):
 class _Sampling(ctypes.Structure):
     _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int),
                 ("top_p", ctypes.c_float)]
+
+
+class _QmvProblem(ctypes.Structure):
+    _fields_ = [("w_packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int), ("K", ctypes.c_int), ("after", ctypes.c_int)]
 
 
 _lib = None
@@ -73,6 +80,17 @@ def lib() -> ctypes.CDLL:
         L.spec_accept_noalloc_scratch_bytes.restype = Z
         L.spec_accept_noalloc.argtypes = [P, P, P, P, P, I, I, I, _Sampling, P, P, P, P]
         L.spec_accept_noalloc.restype = I
+        L.qmv_plan_device_bytes.argtypes = [ctypes.POINTER(_QmvProblem), I, I, I]
+        L.qmv_plan_device_bytes.restype = Z
+        L.qmv_plan_create.argtypes = [ctypes.POINTER(_QmvProblem), I, I, I, P, Z,
+                                      ctypes.POINTER(P)]
+        L.qmv_plan_create.restype = I
+        L.qmv_plan_run.argtypes = [P, P]
+        L.qmv_plan_run.restype = I
+        L.qmv_plan_destroy.argtypes = [P]
+        L.qmv_plan_destroy.restype = None
+        L.qmv_plan_grid.argtypes = [P]
+        L.qmv_plan_grid.restype = I
         L.gdn_tape_bytes.argtypes = [I, I, I, I, I]
         L.gdn_tape_bytes.restype = Z
         L.gdn_tape_capture.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P]
@@ -162,6 +180,66 @@ def qmv_smallm(w_packed: torch.Tensor, scales: torch.Tensor, biases: torch.Tenso
                           M, N, K, 64, 4, _stream(dev))
     _check(st, "qmv_smallm")
     return y
+
+
+class QmvPlan:
+    """An ordered list of qmv_smallm problems run by one persistent launch.
+
+    ``problems``: sequence of (w_packed, scales, biases, x, y, after) with the
+    shapes of :func:`qmv_smallm`; ``after`` = True when x is the output of an
+    earlier problem of the list.  All x share dtype and M.  The plan keeps
+    references to every tensor and to its device buffer."""
+
+    def __init__(self, problems):
+        if not problems:
+            raise ValueError("a plan needs at least one problem")
+        x0 = problems[0][3]
+        dev = x0.device
+        M = x0.shape[0]
+        arr = (_QmvProblem * len(problems))()
+        for i, (w, s_, b_, x, y, after) in enumerate(problems):
+            N, K8 = w.shape
+            K = K8 * 8
+            _need(w, f"problems[{i}].w_packed", torch.int32, (N, K8), dev)
+            _need(s_, f"problems[{i}].scales", torch.bfloat16, (N, K // 64), dev)
+            _need(b_, f"problems[{i}].biases", torch.bfloat16, (N, K // 64), dev)
+            _need(x, f"problems[{i}].x", x0.dtype, (M, K), dev)
+            _need(y, f"problems[{i}].y", torch.float32, (M, N), dev)
+            arr[i] = _QmvProblem(w.data_ptr(), s_.data_ptr(), b_.data_ptr(), x.data_ptr(),
+                                 y.data_ptr(), N, K, 1 if after else 0)
+        dt = SV_BF16 if x0.dtype == torch.bfloat16 else SV_F32
+        with torch.cuda.device(dev):
+            n = int(lib().qmv_plan_device_bytes(arr, len(problems), M, dt))
+            if n == 0:  # invalid: qmv_plan_create reports why, with its status
+                h = ctypes.c_void_p()
+                _check(lib().qmv_plan_create(arr, len(problems), M, dt, None, 0,
+                                             ctypes.byref(h)), "qmv_plan_create")
+                raise SvError(SV_ERR_INVALID_ARG, "qmv_plan_device_bytes",
+                              lib().sv_last_error().decode())
+            self.buffer = torch.empty(n + 256, dtype=torch.uint8, device=dev)
+            off = (-self.buffer.data_ptr()) % 256
+            h = ctypes.c_void_p()
+            _check(lib().qmv_plan_create(arr, len(problems), M, dt,
+                                         ctypes.c_void_p(self.buffer.data_ptr() + off),
+                                         n, ctypes.byref(h)), "qmv_plan_create")
+        self._h = h
+        self.device = dev
+        self.problems = list(problems)  # keep the tensors alive
+        self.grid = int(lib().qmv_plan_grid(h))
+
+    def run(self) -> None:
+        _check(lib().qmv_plan_run(self._h, _stream(self.device)), "qmv_plan_run")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().qmv_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def spec_accept_workspace_bytes(B: int, K: int, V: int) -> int:

@@ -1,0 +1,665 @@
+// qmv_plan.cu -- an ordered list of 4-bit small-M mat-vecs run by ONE
+// persistent launch, sm_103a.
+//
+// Source: "MTPLX 2.24x faster TPS", section "Layer 0: MLX Runtime" (the verify
+// forward runs M = K+1 rows through every 4-bit projection of the target
+// model) and "MTP in llama.cpp", section "Theoretical maximum tg t/s" (a
+// decode step is bounded by streaming the active weights once at memory
+// bandwidth).
+//
+// A verify forward is hundreds of small projections in a row.  Launched one
+// by one, each pays the launch and the latency of its first weight stage
+// (several microseconds on this part, as much as streaming a 50 MB
+// projection takes), so the weight stream stops at every boundary.  Here the
+// whole list is one cooperative launch of exactly the co-resident CTAs:
+//  * the list is cut into phases at every problem flagged `after` (its
+//    activations are an earlier problem's output); inside a phase the
+//    problems are independent;
+//  * the (problem, 64-row tile, 512-input stage) work of a phase is laid out
+//    flat and every CTA takes one equal contiguous run of it (stream-K
+//    style), so every SM has the same number of stages in every phase;
+//  * each CTA's producer warp streams the weight stages of all its runs, phase
+//    after phase, through the shared-memory ring without ever waiting on
+//    other CTAs: the weights of the next phase are in flight while the
+//    current phase finishes;
+//  * consumers read a phase's activations only after the device-wide count
+//    of finished tiles says every tile of the earlier phases has been
+//    written (one acquire load by one thread, bounded wait);
+//  * a tile whose stages fall in several CTAs' runs is reduced by the last of
+//    them to finish, summing the partials in run order -- deterministic;
+//  * counters are left at zero by the last CTA / last arriver, so the plan
+//    is ready for the next launch.
+// The per-group math (nibble widening, bf16 MMA, scale/bias epilogue) is the
+// one of qmv_smallm (qmv_common.cuh).
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "qmv_common.cuh"
+
+namespace sv {
+namespace {
+using namespace qmv;
+
+constexpr int kPartial = kRows * 8;  // floats per partial tile: 64 rows x 8 columns
+constexpr int kPlanCtasPerSm = 2;    // co-resident CTAs per SM (register budget)
+
+__device__ unsigned int g_plan_device_error;
+
+// One problem of the plan, in device memory (tensor maps 64-byte aligned).
+struct PlanProblem {  // CUtensorMap's own alignment (>= 64 bytes) carries over
+  CUtensorMap wmap, smap, bmap;
+  const void *x;
+  float *y;
+  int N, K;
+  int tiles, chunks;  // 64-row tiles, 512-input stages
+  int chunk_off;      // first flat stage index in its phase
+  int tile_off;       // first tile index in its phase
+};
+
+struct PlanPhase {
+  int first, count;     // problems
+  long long work;       // stages in the phase
+  int tiles_before;     // tiles of all earlier phases
+  int wait;             // 1: activations are earlier outputs
+  int max_splits;       // partial slots per tile
+};
+
+struct PlanParams {
+  const PlanProblem *problems;
+  const PlanPhase *phases;
+  float *partials;      // [tiles of a phase][max_splits][kPartial]
+  int *tile_count;      // [tiles of a phase] arrivals
+  int *done_tiles;      // tiles written (all phases so far)
+  int *done_ctas;
+  int n_phases;
+  int M;
+  int stages;
+};
+
+struct PlanLayout {
+  uint32_t ring, red, bar, total;
+};
+__host__ __device__ inline PlanLayout plan_layout(int stages) {
+  PlanLayout L;
+  L.ring = (uint32_t)stages * kStageBytesStream;
+  L.red = L.ring;
+  L.bar = L.red + kRedBytes;
+  L.total = L.bar + (uint32_t)(2 * stages) * 8u + 1024u;
+  return L;
+}
+
+// Runs of a phase of W stages over G CTAs: with W >= G, CTA c takes
+// [floor(c W / G), floor((c+1) W / G)) (never empty); with W < G, CTA c < W
+// takes stage c alone and the others none.  So the CTAs whose runs meet a
+// tile are consecutive and every one of them holds part of it.
+__device__ __forceinline__ long long run_begin(int c, long long W, int G) {
+  return W >= G ? (long long)c * W / G : (c < W ? c : W);
+}
+__device__ __forceinline__ int owner(long long j, long long W, int G) {
+  if (W < G) return (int)j;
+  long long c = j * G / W;
+  while (c + 1 < G && (c + 1) * W / G <= j) ++c;
+  while (c > 0 && c * W / G > j) --c;
+  return (int)c;
+}
+
+// A run of consecutive stages of one tile inside a CTA's range.
+struct Segment {
+  int p;            // problem
+  int tile;
+  int c0, c1;       // stages [c0, c1) of the tile
+  int split, n_splits;
+  int tile_in_phase;
+};
+
+// Walks the segments of this CTA's run in one phase.
+struct SegmentWalker {
+  const PlanProblem *probs;
+  PlanPhase ph;
+  long long j, end;
+  int p;  // current problem (absolute index)
+  int G, cta;
+
+  __device__ void begin(const PlanParams &P, int phase, int cta_, int G_) {
+    probs = P.problems;
+    ph = P.phases[phase];
+    G = G_;
+    cta = cta_;
+    j = run_begin(cta, ph.work, G);
+    end = run_begin(cta + 1, ph.work, G);
+    p = ph.first;
+  }
+  __device__ bool next(Segment &s) {
+    if (j >= end) return false;
+    while (true) {
+      const PlanProblem &q = probs[p];
+      const long long lo = q.chunk_off, hi = lo + (long long)q.tiles * q.chunks;
+      if (j < hi) break;
+      ++p;
+    }
+    const PlanProblem &q = probs[p];
+    const long long rel = j - q.chunk_off;
+    s.p = p;
+    s.tile = (int)(rel / q.chunks);
+    s.c0 = (int)(rel % q.chunks);
+    const long long tile_start = q.chunk_off + (long long)s.tile * q.chunks;
+    const long long tile_end = tile_start + q.chunks;
+    const long long seg_end = tile_end < end ? tile_end : end;
+    s.c1 = s.c0 + (int)(seg_end - j);
+    const int first = owner(tile_start, ph.work, G);
+    const int last = owner(tile_end - 1, ph.work, G);
+    s.split = cta - first;
+    s.n_splits = last - first + 1;
+    s.tile_in_phase = q.tile_off + s.tile;
+    j = seg_end;
+    return true;
+  }
+};
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *p >= target (one thread).  False after the limit.
+__device__ bool wait_count(const int *p, int target) {
+  if (ld_acquire(p) >= target) return true;
+  const unsigned long long t0 = global_timer_ns();
+  unsigned ns = 64;
+  for (;;) {
+    __nanosleep(ns);
+    if (ns < 1024) ns <<= 1;
+    if (ld_acquire(p) >= target) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+template <bool kXF32>
+__device__ __forceinline__ XRaw<kXF32> load_x_l2(const void *xrow, int g, int t) {
+  // activations may have been written by other CTAs of this launch: read
+  // them at L2 (no stale L1 lines)
+  XRaw<kXF32> r;
+  if constexpr (!kXF32) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(xrow) +
+                                                     g * 64 + 8 * t);
+    r.v[0] = __ldcg(p);
+    r.v[1] = __ldcg(p + 4);
+  } else {
+    const uint4 *p =
+        reinterpret_cast<const uint4 *>(static_cast<const float *>(xrow) + g * 64 + 8 * t);
+    r.v[0] = __ldcg(p);
+    r.v[1] = __ldcg(p + 1);
+    r.v[2] = __ldcg(p + 8);
+    r.v[3] = __ldcg(p + 9);
+  }
+  return r;
+}
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+}
+
+template <bool kXF32>
+__global__ void __launch_bounds__(kThreads, kPlanCtasPerSm) qmv_plan_kernel(const PlanParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t *smem = smem_raw + (base - raw);
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int stages = P.stages;
+  const PlanLayout L = plan_layout(stages);
+  const uint32_t full0 = base + L.bar;
+  const uint32_t empty0 = full0 + 8u * stages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init_u32(full0 + 8u * i, 1);
+      mbar_init_u32(empty0 + 8u * i, kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      int st = 0, ph = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int f = 0; ok && f < P.n_phases; ++f) {
+        SegmentWalker wk;
+        wk.begin(P, f, cta, G);
+        Segment s;
+        while (ok && wk.next(s)) {
+          const PlanProblem &q = P.problems[s.p];
+          const int n0 = s.tile * kRows;
+          for (int c = s.c0; c < s.c1; ++c) {
+            if (issued >= stages && !mbar_wait_u32(empty0 + 8u * st, ph ^ 1)) {
+              atomicOr(&g_plan_device_error, 1u);
+              ok = false;
+              break;
+            }
+            const uint32_t stage = base + st * kStageBytesStream, bar = full0 + 8u * st;
+            const int k0 = c * kStageInputs;
+            mbar_arrive_expect_tx_u32(bar, kSbOff + 2 * kRows * 16);
+            tma_load_2d(stage, &q.wmap, k0 / 8, n0, bar, policy);
+            tma_load_2d(stage + kRows * 128, &q.wmap, k0 / 8 + kBoxWords, n0, bar, policy);
+            tma_load_2d(stage + kSbOff, &q.smap, k0 / 64, n0, bar, policy);
+            tma_load_2d(stage + kSbOff + kRows * 16, &q.bmap, k0 / 64, n0, bar, policy);
+            ++issued;
+            if (++st == stages) {
+              st = 0;
+              ph ^= 1;
+            }
+          }
+        }
+      }
+      // every copy issued has landed before the CTA may exit (normally the
+      // consumers have waited for all of them already)
+      for (long long i = std::max(0ll, issued - stages); i < issued; ++i)
+        (void)mbar_wait_u32(full0 + 8u * (uint32_t)(i % stages), (uint32_t)((i / stages) & 1));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ consumers -----------------------------
+    const int g8 = lane >> 2, t = lane & 3;
+    const int gl = warp;
+    const uint32_t ldm_off = ldmatrix_offset(gl, lane);
+    const uint32_t sb_off = kSbOff + (uint32_t)(g8 * 16 + gl * 2);
+    float *red = reinterpret_cast<float *>(smem + L.red);
+    __shared__ int s_last;
+    const int xm = g8 < P.M ? g8 : 0;  // padding columns read row 0, never stored
+    bool ok = true;
+    int st = 0, ph = 0;
+    for (int f = 0; f < P.n_phases; ++f) {
+      SegmentWalker wk;
+      wk.begin(P, f, cta, G);
+      if (wk.ph.wait) {
+        // every tile of the earlier phases is written before x is read
+        if (threadIdx.x == 0 && !wait_count(P.done_tiles, wk.ph.tiles_before)) {
+          atomicOr(&g_plan_device_error, 4u);
+        }
+        consumer_bar();
+      }
+      Segment s;
+      while (wk.next(s)) {
+        const PlanProblem &q = P.problems[s.p];
+        const int K = q.K, N = q.N;
+        const void *xrow =
+            static_cast<const uint8_t *>(q.x) + (size_t)xm * K * (kXF32 ? 4 : 2);
+        float acc[kTiles][4];
+#pragma unroll
+        for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        int g = s.c0 * kConsumerWarps + gl;
+        XRaw<kXF32> xnext = load_x_l2<kXF32>(xrow, g, t);
+        for (int c = s.c0; c < s.c1; ++c, g += kConsumerWarps) {
+          const XRaw<kXF32> xcur = xnext;
+          if (c + 1 < s.c1) xnext = load_x_l2<kXF32>(xrow, g + kConsumerWarps, t);
+          if (ok && !warp_wait_stage(full0 + 8u * st, ph)) {
+            ok = false;
+            if (lane == 0) atomicOr(&g_plan_device_error, 2u);
+          }
+          if (ok) {
+            const uint32_t stage = base + st * kStageBytesStream;
+            group_math<kXF32>(acc, stage + ldm_off, xcur, stage + sb_off, 16 * 16, 8 * 16,
+                              kRows * 16);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
+          if (++st == stages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        // cross-warp reduction in a fixed order: red[warp][row][col]
+        consumer_bar();  // the previous segment's reads of red are done
+#pragma unroll
+        for (int rt = 0; rt < kTiles; ++rt) {
+          float *r = red + ((size_t)warp * kRows + rt * 16) * 8;
+          r[g8 * 8 + 2 * t] = acc[rt][0];
+          r[g8 * 8 + 2 * t + 1] = acc[rt][1];
+          r[(g8 + 8) * 8 + 2 * t] = acc[rt][2];
+          r[(g8 + 8) * 8 + 2 * t + 1] = acc[rt][3];
+        }
+        consumer_bar();
+        float v[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int e = threadIdx.x + h * kConsumerWarps * 32;  // e = row * 8 + col
+          float sum = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) sum += red[(size_t)w * kPartial + e];
+          v[h] = sum;
+        }
+        const int n0 = s.tile * kRows;
+        if (s.n_splits == 1) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = threadIdx.x + h * kConsumerWarps * 32;
+            const int row = e >> 3, col = e & 7;
+            if (col < P.M && n0 + row < N) q.y[(size_t)col * N + n0 + row] = v[h];
+          }
+          consumer_bar();
+          if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(P.done_tiles, 1);
+          }
+          continue;
+        }
+        float *slots = P.partials + (size_t)s.tile_in_phase * wk.ph.max_splits * kPartial;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          __stcg(&slots[(size_t)s.split * kPartial + threadIdx.x + h * kConsumerWarps * 32],
+                 v[h]);
+        consumer_bar();  // the CTA's partial is written ...
+        if (threadIdx.x == 0) {
+          __threadfence();  // ... and published before the arrival is counted
+          const int prev = atomicAdd(&P.tile_count[s.tile_in_phase], 1);
+          __threadfence();  // the other runs' partials are visible after the count
+          s_last = prev == s.n_splits - 1;
+        }
+        consumer_bar();
+        if (s_last) {  // the tile's partials are all written: sum them in run order
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = threadIdx.x + h * kConsumerWarps * 32;
+            float sum = 0.f;
+            for (int r = 0; r < s.n_splits; ++r) sum += __ldcg(&slots[(size_t)r * kPartial + e]);
+            const int row = e >> 3, col = e & 7;
+            if (col < P.M && n0 + row < N) q.y[(size_t)col * N + n0 + row] = sum;
+          }
+          consumer_bar();
+          if (threadIdx.x == 0) {
+            P.tile_count[s.tile_in_phase] = 0;  // ready for the next launch
+            __threadfence();
+            atomicAdd(P.done_tiles, 1);
+          }
+        }
+      }
+    }
+  }
+
+  // the last CTA to finish leaves the counters at zero for the next launch
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(P.done_ctas, 1) == G - 1) {
+      *P.done_tiles = 0;
+      *P.done_ctas = 0;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+unsigned take_device_error_plan() {
+  unsigned v = 0, zero = 0;
+  cudaMemcpyFromSymbol(&v, g_plan_device_error, sizeof v);
+  cudaMemcpyToSymbol(g_plan_device_error, &zero, sizeof zero);
+  return v;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+struct sv_qmv_plan {
+  int M;
+  sv_dtype x_dtype;
+  int grid, stages;
+  uint32_t smem;
+  PlanParams params;
+};
+
+namespace {
+
+struct PlanShape {
+  std::vector<PlanProblem> probs;
+  std::vector<PlanPhase> phases;
+  size_t off_phases, off_partials, off_counts, off_done, total;
+  int max_phase_tiles;
+};
+
+// Phases, stage offsets and partial slots for `G` CTAs; device buffer layout.
+sv_status plan_shape(const sv_qmv_problem *pr, int n, int G, PlanShape &S) {
+  S.probs.assign(n, PlanProblem{});
+  S.phases.clear();
+  int tiles_before = 0;
+  S.max_phase_tiles = 1;
+  size_t partial_floats = kPartial;
+  for (int i = 0; i < n;) {
+    PlanPhase ph{};
+    ph.first = i;
+    ph.wait = (i > 0 && pr[i].after) ? 1 : 0;
+    ph.tiles_before = tiles_before;
+    long long work = 0;
+    int tiles = 0, min_chunks = 1 << 30;
+    int j = i;
+    do {
+      PlanProblem &q = S.probs[j];
+      q.N = pr[j].N;
+      q.K = pr[j].K;
+      q.x = pr[j].x;
+      q.y = pr[j].y;
+      q.tiles = (q.N + kRows - 1) / kRows;
+      q.chunks = q.K / kStageInputs;
+      q.chunk_off = (int)work;
+      q.tile_off = tiles;
+      work += (long long)q.tiles * q.chunks;
+      tiles += q.tiles;
+      min_chunks = std::min(min_chunks, q.chunks);
+      ++j;
+    } while (j < n && !pr[j].after);
+    ph.count = j - i;
+    ph.work = work;
+    if (work > (1ll << 31) - 1)
+      return fail(SV_ERR_UNSUPPORTED, "qmv_plan_create: a phase has more than 2^31 stages");
+    // a tile of C stages meets at most ceil(C / q) + 1 runs of >= q stages
+    const long long q_min = work / G;
+    int max_chunks = 0;
+    for (int k = i; k < j; ++k) max_chunks = std::max(max_chunks, S.probs[k].chunks);
+    ph.max_splits = q_min > 0 ? (int)std::min<long long>(G, (max_chunks + q_min - 1) / q_min + 1)
+                              : std::min(G, max_chunks);
+    partial_floats = std::max(partial_floats, (size_t)tiles * ph.max_splits * kPartial);
+    S.max_phase_tiles = std::max(S.max_phase_tiles, tiles);
+    tiles_before += tiles;
+    S.phases.push_back(ph);
+    i = j;
+  }
+  if (tiles_before >= (1 << 30))
+    return fail(SV_ERR_UNSUPPORTED, "qmv_plan_create: too many tiles");
+  auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
+  size_t off = up((size_t)n * sizeof(PlanProblem), 256);
+  S.off_phases = off;
+  off = up(off + S.phases.size() * sizeof(PlanPhase), 256);
+  S.off_partials = off;
+  off = up(off + partial_floats * 4, 256);
+  S.off_counts = off;
+  off = up(off + (size_t)S.max_phase_tiles * 4, 256);
+  S.off_done = off;
+  S.total = off + 256;
+  return SV_OK;
+}
+
+template <bool kXF32>
+sv_status plan_config(int dev, int &grid, int &stages, uint32_t &smem) {
+  int optin = 0, smem_sm = 0, sms = device_sm_count();
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaFuncAttributes fa = {};
+  if (cudaFuncGetAttributes(&fa, qmv_plan_kernel<kXF32>) != cudaSuccess)
+    return fail(SV_ERR_CUDA, "qmv_plan: cudaFuncGetAttributes failed");
+  if (cudaFuncSetAttribute(qmv_plan_kernel<kXF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           optin - (int)fa.sharedSizeBytes) != cudaSuccess)
+    return fail(SV_ERR_CUDA, "qmv_plan: cudaFuncSetAttribute failed: %s",
+                cudaGetErrorString(cudaGetLastError()));
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qmv_plan_kernel<kXF32>, kThreads, 0) !=
+          cudaSuccess ||
+      occ < 1)
+    return fail(SV_ERR_CUDA, "qmv_plan: occupancy query failed");
+  const int per_sm = std::min(occ, kPlanCtasPerSm);
+  // 1 KB per CTA is reserved by the system; static shared memory comes first
+  const uint32_t budget = (uint32_t)smem_sm / per_sm - 1024u - (uint32_t)fa.sharedSizeBytes;
+  stages = 2;
+  const uint32_t cap = std::min<uint32_t>(budget, (uint32_t)optin - (uint32_t)fa.sharedSizeBytes);
+  while (stages < 16 && plan_layout(stages + 1).total <= cap) ++stages;
+  smem = plan_layout(stages).total;
+  if (smem > (uint32_t)optin) return fail(SV_ERR_UNSUPPORTED, "qmv_plan: shared memory");
+  int fit = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, qmv_plan_kernel<kXF32>, kThreads,
+                                                    smem) != cudaSuccess ||
+      fit < 1)
+    return fail(SV_ERR_CUDA, "qmv_plan: occupancy query failed");
+  grid = std::min(fit, per_sm) * sms;
+  return SV_OK;
+}
+
+sv_status validate_problems(const sv_qmv_problem *pr, int n, int M, sv_dtype x_dtype) {
+  if (n < 1 || !pr) return fail(SV_ERR_INVALID_ARG, "qmv_plan: need n_problems >= 1");
+  if (M < 1 || M > 8) return fail(SV_ERR_UNSUPPORTED, "qmv_plan: M=%d outside [1, 8]", M);
+  if (x_dtype != SV_F32 && x_dtype != SV_BF16)
+    return fail(SV_ERR_INVALID_ARG, "qmv_plan: unknown x_dtype %d", (int)x_dtype);
+  int phase_start = 0;
+  for (int i = 0; i < n; ++i) {
+    const sv_qmv_problem &q = pr[i];
+    if (q.N < 1 || q.K < 1)
+      return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d: need N, K >= 1", i);
+    if (q.K % kStageInputs)
+      return fail(SV_ERR_UNSUPPORTED, "qmv_plan: problem %d: K=%d is not a multiple of %d", i,
+                  q.K, kStageInputs);
+    if (q.N > (1 << 30) || q.K > (1 << 30))
+      return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d too large", i);
+    if (!q.w_packed || !q.scales || !q.biases || !q.x || !q.y)
+      return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d: null pointer", i);
+    if (!aligned(q.w_packed, 16) || !aligned(q.scales, 16) || !aligned(q.biases, 16) ||
+        !aligned(q.x, 16) || !aligned(q.y, 4))
+      return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d: misaligned pointer", i);
+    const size_t wb = (size_t)q.N * q.K / 2, sbb = (size_t)q.N * (q.K / 64) * 2;
+    const size_t xb = (size_t)M * q.K * (x_dtype == SV_F32 ? 4 : 2), yb = (size_t)M * q.N * 4;
+    if (overlaps(q.y, yb, q.w_packed, wb) || overlaps(q.y, yb, q.scales, sbb) ||
+        overlaps(q.y, yb, q.biases, sbb) || overlaps(q.y, yb, q.x, xb))
+      return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d: y overlaps an input", i);
+    // an output read later in the same phase would be read before it is written
+    if (i == 0 || q.after) phase_start = i;
+    for (int j = phase_start; j < i; ++j)
+      if (overlaps(pr[j].y, (size_t)M * pr[j].N * 4, q.x, xb))
+        return fail(SV_ERR_INVALID_ARG,
+                    "qmv_plan: problem %d reads problem %d's output without `after`", i, j);
+  }
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" size_t qmv_plan_device_bytes(const sv_qmv_problem *problems, int n_problems, int M,
+                                        sv_dtype x_dtype) {
+  clear_error();
+  if (validate_problems(problems, n_problems, M, x_dtype) != SV_OK) return 0;
+  int grid = 0, stages = 0;
+  uint32_t smem = 0;
+  const int dev = current_device();
+  const sv_status st = x_dtype == SV_BF16 ? plan_config<false>(dev, grid, stages, smem)
+                                          : plan_config<true>(dev, grid, stages, smem);
+  if (st != SV_OK) return 0;
+  PlanShape S;
+  if (plan_shape(problems, n_problems, grid, S) != SV_OK) return 0;
+  return S.total;
+}
+
+extern "C" sv_status qmv_plan_create(const sv_qmv_problem *problems, int n_problems, int M,
+                                     sv_dtype x_dtype, void *device_buffer, size_t device_bytes,
+                                     sv_qmv_plan **plan_out) {
+  clear_error();
+  if (!plan_out) return fail(SV_ERR_INVALID_ARG, "qmv_plan_create: null plan_out");
+  *plan_out = nullptr;
+  sv_status st = validate_problems(problems, n_problems, M, x_dtype);
+  if (st != SV_OK) return st;
+  const int dev = current_device();
+  int grid = 0, stages = 0;
+  uint32_t smem = 0;
+  st = x_dtype == SV_BF16 ? plan_config<false>(dev, grid, stages, smem)
+                          : plan_config<true>(dev, grid, stages, smem);
+  if (st != SV_OK) return st;
+  PlanShape S;
+  st = plan_shape(problems, n_problems, grid, S);
+  if (st != SV_OK) return st;
+  if (!device_buffer || !aligned(device_buffer, 256))
+    return fail(SV_ERR_INVALID_ARG, "qmv_plan_create: device_buffer must be 256-byte aligned");
+  if (device_bytes < S.total)
+    return fail(SV_ERR_INVALID_ARG, "qmv_plan_create: device buffer of %zu bytes, need %zu",
+                device_bytes, S.total);
+  for (int i = 0; i < n_problems; ++i) {
+    const sv_qmv_problem &q = problems[i];
+    PlanProblem &d = S.probs[i];
+    const int groups = q.K / 64;
+    st = encode_2d(&d.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, q.w_packed, (uint64_t)q.K / 8,
+                   (uint64_t)q.N, (uint64_t)q.K / 2, kBoxWords, kRows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == SV_OK)
+      st = encode_2d(&d.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, q.scales, (uint64_t)groups,
+                     (uint64_t)q.N, (uint64_t)groups * 2, 8, kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st == SV_OK)
+      st = encode_2d(&d.bmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, q.biases, (uint64_t)groups,
+                     (uint64_t)q.N, (uint64_t)groups * 2, 8, kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != SV_OK) return st;
+  }
+  // descriptors, phases, then zeroed partial counters and done counters
+  std::vector<uint8_t> host(S.off_partials, 0);
+  std::memcpy(host.data(), S.probs.data(), S.probs.size() * sizeof(PlanProblem));
+  std::memcpy(host.data() + S.off_phases, S.phases.data(), S.phases.size() * sizeof(PlanPhase));
+  uint8_t *dbuf = static_cast<uint8_t *>(device_buffer);
+  if (cudaMemcpy(dbuf, host.data(), host.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(dbuf + S.off_counts, 0, S.total - S.off_counts) != cudaSuccess)
+    return fail(SV_ERR_CUDA, "qmv_plan_create: copying the plan to the device failed");
+  sv_qmv_plan *plan = new (std::nothrow) sv_qmv_plan;
+  if (!plan) return fail(SV_ERR_INVALID_ARG, "qmv_plan_create: out of host memory");
+  plan->M = M;
+  plan->x_dtype = x_dtype;
+  plan->grid = grid;
+  plan->stages = stages;
+  plan->smem = smem;
+  PlanParams &P = plan->params;
+  P.problems = reinterpret_cast<const PlanProblem *>(dbuf);
+  P.phases = reinterpret_cast<const PlanPhase *>(dbuf + S.off_phases);
+  P.partials = reinterpret_cast<float *>(dbuf + S.off_partials);
+  P.tile_count = reinterpret_cast<int *>(dbuf + S.off_counts);
+  P.done_tiles = reinterpret_cast<int *>(dbuf + S.off_done);
+  P.done_ctas = P.done_tiles + 1;
+  P.n_phases = (int)S.phases.size();
+  P.M = M;
+  P.stages = stages;
+  *plan_out = plan;
+  return SV_OK;
+}
+
+extern "C" sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream) {
+  clear_error();
+  if (!plan) return fail(SV_ERR_INVALID_ARG, "qmv_plan_run: null plan");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan->grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = plan->smem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the phase waits need it
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      plan->x_dtype == SV_BF16
+          ? cudaLaunchKernelEx(&cfg, qmv_plan_kernel<false>, plan->params)
+          : cudaLaunchKernelEx(&cfg, qmv_plan_kernel<true>, plan->params);
+  if (e != cudaSuccess)
+    return fail(SV_ERR_CUDA, "qmv_plan_run: launch failed: %s", cudaGetErrorString(e));
+  return check_launch("qmv_plan_run");
+}
+
+extern "C" void qmv_plan_destroy(sv_qmv_plan *plan) { delete plan; }
+
+extern "C" int qmv_plan_grid(const sv_qmv_plan *plan) { return plan ? plan->grid : 0; }

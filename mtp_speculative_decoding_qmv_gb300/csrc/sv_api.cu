@@ -78,7 +78,9 @@ extern "C" sv_status sv_device_status(void) {
   const unsigned q = sv::take_device_error_qmv();
   const unsigned a = sv::take_device_error_accept();
   const unsigned g = sv::take_device_error_gdn();
-  if (q | a | g)
-    return sv::fail(SV_ERR_DEVICE_FLAG, "device error words: qmv=%u accept=%u gdn=%u", q, a, g);
+  const unsigned p = sv::take_device_error_plan();
+  if (q | a | g | p)
+    return sv::fail(SV_ERR_DEVICE_FLAG, "device error words: qmv=%u accept=%u gdn=%u plan=%u", q,
+                    a, g, p);
   return SV_OK;
 }

@@ -33,5 +33,6 @@ sv_status check_launch(const char *what);
 unsigned take_device_error_qmv();
 unsigned take_device_error_accept();
 unsigned take_device_error_gdn();
+unsigned take_device_error_plan();
 
 }  // namespace sv
