@@ -72,7 +72,8 @@ const char *sv_status_string(int status);
 /* Message describing the most recent failure on the calling thread ("" if none). */
 const char *sv_last_error(void);
 
-/* Programmatic dependent launch (PDL) for qmv_smallm, process-wide, default 0.
+/* Programmatic dependent launch (PDL) for qmv_smallm and qmv_plan_run,
+ * process-wide, default 0.
  * When enabled, a qmv_smallm kernel may start while the kernel enqueued
  * before it on the same stream is still running, and may read w_packed,
  * scales and biases before that kernel has finished (x is read, and y
@@ -139,6 +140,9 @@ sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales, const uin
  * qmv_plan_destroy.  The buffer and every problem's tensors must stay valid
  * while the plan is used.  qmv_plan_run: one cooperative launch on `stream`
  * (capturable in a CUDA graph); runs of one plan must not overlap in time.
+ * With sv_set_pdl(1) the launch may start while the preceding kernel runs:
+ * weights are streamed at once, while x, y and the plan's counters are
+ * touched only after that kernel has finished.
  * A phase wait that exceeds ~1 s sets a device error word
  * (sv_device_status) and the launch finishes with invalid results; the
  * plan's counters are then undefined: create it again. */

@@ -45,6 +45,11 @@ using namespace qmv;
 
 constexpr int kPartial = kRows * 8;  // floats per partial tile: 64 rows x 8 columns
 constexpr int kPlanCtasPerSm = 2;    // co-resident CTAs per SM (register budget)
+constexpr int kEpilogueWarp = kConsumerWarps + 1;   // after the producer warp
+constexpr int kPlanThreads = (kConsumerWarps + 2) * 32;
+// suspend-time hint of the epilogue warp's waits: it signals tiles that other
+// CTAs may be waiting for, so it must resume promptly
+constexpr uint32_t kEpilogueSuspendNs = 256;
 
 __device__ unsigned int g_plan_device_error;
 
@@ -64,6 +69,7 @@ struct PlanPhase {
   long long work;       // stages in the phase
   int tiles_before;     // tiles of all earlier phases
   int wait;             // 1: activations are earlier outputs
+  int signal;           // 1: a later phase waits for this one's tiles
   int max_splits;       // partial slots per tile
 };
 
@@ -87,7 +93,7 @@ __host__ __device__ inline PlanLayout plan_layout(int stages) {
   L.ring = (uint32_t)stages * kStageBytesStream;
   L.red = L.ring;
   L.bar = L.red + kRedBytes;
-  L.total = L.bar + (uint32_t)(2 * stages) * 8u + 1024u;
+  L.total = L.bar + (uint32_t)(2 * stages + 2) * 8u + 1024u;
   return L;
 }
 
@@ -159,6 +165,15 @@ struct SegmentWalker {
   }
 };
 
+__device__ __forceinline__ int atom_add_acq_rel(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_release(int *p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -169,10 +184,10 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
 __device__ bool wait_count(const int *p, int target) {
   if (ld_acquire(p) >= target) return true;
   const unsigned long long t0 = global_timer_ns();
-  unsigned ns = 64;
+  unsigned ns = 32;
   for (;;) {
     __nanosleep(ns);
-    if (ns < 1024) ns <<= 1;
+    if (ns < 128) ns <<= 1;
     if (ld_acquire(p) >= target) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
@@ -204,7 +219,8 @@ __device__ __forceinline__ void consumer_bar() {
 }
 
 template <bool kXF32>
-__global__ void __launch_bounds__(kThreads, kPlanCtasPerSm) qmv_plan_kernel(const PlanParams P) {
+__global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
+    qmv_plan_kernel(const PlanParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -214,18 +230,25 @@ __global__ void __launch_bounds__(kThreads, kPlanCtasPerSm) qmv_plan_kernel(cons
   const PlanLayout L = plan_layout(stages);
   const uint32_t full0 = base + L.bar;
   const uint32_t empty0 = full0 + 8u * stages;
+  const uint32_t red_full = empty0 + 8u * stages;  // consumers' tile sums are in red
+  const uint32_t red_empty = red_full + 8u;        // the epilogue warp has read them
+  float *red = reinterpret_cast<float *>(smem + L.red);  // [warp][row * 8 + col]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init_u32(full0 + 8u * i, 1);
       mbar_init_u32(empty0 + 8u * i, kConsumerWarps);
     }
+    mbar_init_u32(red_full, kConsumerWarps * 32);
+    mbar_init_u32(red_empty, 32);
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
+    // weights do not depend on earlier kernels: no griddepcontrol.wait here
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_first();
       int st = 0, ph = 0;
@@ -265,41 +288,143 @@ __global__ void __launch_bounds__(kThreads, kPlanCtasPerSm) qmv_plan_kernel(cons
         (void)mbar_wait_u32(full0 + 8u * (uint32_t)(i % stages), (uint32_t)((i / stages) & 1));
     }
     __syncwarp();
+  } else if (warp == kEpilogueWarp) {
+    // ------------------------------ epilogue ------------------------------
+    // Per tile run: sum the eight warps' partials in warp order (lane = rows
+    // lane and lane + 32, all eight columns), free red, then write y (or
+    // this run's partial; the last run of a split tile sums the partials in
+    // run order) and count the tile when a later phase waits for it.
+    unsigned nseg = 0;
+    const float4 *red4 = reinterpret_cast<const float4 *>(red);
+    pdl_wait();  // y and the plan's counters belong to the preceding kernel until here
+    for (int f = 0; f < P.n_phases; ++f) {
+      SegmentWalker wk;
+      wk.begin(P, f, cta, G);
+      Segment s;
+      while (wk.next(s)) {
+        if (!mbar_wait_u32(red_full, nseg & 1, kEpilogueSuspendNs))
+          atomicOr(&g_plan_device_error, 8u);
+        float4 v[4];  // rows lane (v[0], v[1]) and lane + 32 (v[2], v[3]); 8 columns each
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 a = red4[w * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)];
+            v[i].x += a.x;
+            v[i].y += a.y;
+            v[i].z += a.z;
+            v[i].w += a.w;
+          }
+        }
+        mbar_arrive_u32(red_empty);
+        ++nseg;
+        const PlanProblem &q = P.problems[s.p];
+        const int N = q.N, n0 = s.tile * kRows;
+        bool write = true;
+        float4 *slots = nullptr;
+        if (s.n_splits > 1) {
+          slots = reinterpret_cast<float4 *>(P.partials) +
+                  (size_t)s.tile_in_phase * wk.ph.max_splits * (kPartial / 4);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            __stcg(&slots[(size_t)s.split * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)],
+                   v[i]);
+          __syncwarp();
+          int last = 0;
+          if (lane == 0)  // publishes this run's partial, sees the others' if last
+            last = atom_add_acq_rel(&P.tile_count[s.tile_in_phase], 1) == s.n_splits - 1;
+          write = __shfl_sync(0xffffffffu, last, 0) != 0;
+          if (write) {
+            __syncwarp();  // the other lanes read after lane 0's acquire
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < s.n_splits; ++r) {
+              float4 a[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                a[i] = __ldcg(&slots[(size_t)r * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)]);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                v[i].x += a[i].x;
+                v[i].y += a[i].y;
+                v[i].z += a[i].z;
+                v[i].w += a[i].w;
+              }
+            }
+          }
+        }
+        if (write) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = n0 + lane + 32 * h;
+            if (row < N) {
+              const float c[8] = {v[2 * h].x, v[2 * h].y, v[2 * h].z, v[2 * h].w,
+                                  v[2 * h + 1].x, v[2 * h + 1].y, v[2 * h + 1].z, v[2 * h + 1].w};
+#pragma unroll
+              for (int col = 0; col < 8; ++col)
+                if (col < P.M) q.y[(size_t)col * N + row] = c[col];
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {
+            if (slots) P.tile_count[s.tile_in_phase] = 0;  // ready for the next launch
+            if (wk.ph.signal) red_add_release(P.done_tiles, 1);
+          }
+        }
+      }
+    }
   } else {
     // ------------------------------ consumers -----------------------------
     const int g8 = lane >> 2, t = lane & 3;
     const int gl = warp;
     const uint32_t ldm_off = ldmatrix_offset(gl, lane);
     const uint32_t sb_off = kSbOff + (uint32_t)(g8 * 16 + gl * 2);
-    float *red = reinterpret_cast<float *>(smem + L.red);
-    __shared__ int s_last;
     const int xm = g8 < P.M ? g8 : 0;  // padding columns read row 0, never stored
+    const size_t xbytes = kXF32 ? 4 : 2;
     bool ok = true;
     int st = 0, ph = 0;
+    unsigned nseg = 0;
+    pdl_wait();  // x and the plan's counters belong to the preceding kernel until here
+    float acc[kTiles][4];
+#pragma unroll
+    for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     for (int f = 0; f < P.n_phases; ++f) {
       SegmentWalker wk;
       wk.begin(P, f, cta, G);
       if (wk.ph.wait) {
         // every tile of the earlier phases is written before x is read
-        if (threadIdx.x == 0 && !wait_count(P.done_tiles, wk.ph.tiles_before)) {
+        if (threadIdx.x == 0 && !wait_count(P.done_tiles, wk.ph.tiles_before))
           atomicOr(&g_plan_device_error, 4u);
-        }
         consumer_bar();
       }
       Segment s;
-      while (wk.next(s)) {
+      bool have = wk.next(s);
+      XRaw<kXF32> xnext;
+      if (have) {
         const PlanProblem &q = P.problems[s.p];
-        const int K = q.K, N = q.N;
-        const void *xrow =
-            static_cast<const uint8_t *>(q.x) + (size_t)xm * K * (kXF32 ? 4 : 2);
-        float acc[kTiles][4];
-#pragma unroll
-        for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        xnext = load_x_l2<kXF32>(static_cast<const uint8_t *>(q.x) + (size_t)xm * q.K * xbytes,
+                                 s.c0 * kConsumerWarps + gl, t);
+      }
+      while (have) {
+        const PlanProblem &q = P.problems[s.p];
+        const void *xrow = static_cast<const uint8_t *>(q.x) + (size_t)xm * q.K * xbytes;
+        SegmentWalker la = wk;  // the next run of this phase, for the activation prefetch
+        Segment s2;
+        const bool have2 = la.next(s2);
+        const void *xrow2 = nullptr;
+        if (have2) {
+          const PlanProblem &q2 = P.problems[s2.p];
+          xrow2 = static_cast<const uint8_t *>(q2.x) + (size_t)xm * q2.K * xbytes;
+        }
         int g = s.c0 * kConsumerWarps + gl;
-        XRaw<kXF32> xnext = load_x_l2<kXF32>(xrow, g, t);
         for (int c = s.c0; c < s.c1; ++c, g += kConsumerWarps) {
           const XRaw<kXF32> xcur = xnext;
-          if (c + 1 < s.c1) xnext = load_x_l2<kXF32>(xrow, g + kConsumerWarps, t);
+          if (c + 1 < s.c1)
+            xnext = load_x_l2<kXF32>(xrow, g + kConsumerWarps, t);
+          else if (have2)
+            xnext = load_x_l2<kXF32>(xrow2, s2.c0 * kConsumerWarps + gl, t);
           if (ok && !warp_wait_stage(full0 + 8u * st, ph)) {
             ok = false;
             if (lane == 0) atomicOr(&g_plan_device_error, 2u);
@@ -316,70 +441,24 @@ __global__ void __launch_bounds__(kThreads, kPlanCtasPerSm) qmv_plan_kernel(cons
             ph ^= 1;
           }
         }
-        // cross-warp reduction in a fixed order: red[warp][row][col]
-        consumer_bar();  // the previous segment's reads of red are done
+        // hand the run's sums to the epilogue warp: red[warp][row][col]
+        if (nseg > 0 && !__all_sync(0xffffffffu, mbar_wait_u32(red_empty, (nseg - 1) & 1)) &&
+            lane == 0)
+          atomicOr(&g_plan_device_error, 16u);
+        float *r = red + warp * kPartial;
 #pragma unroll
         for (int rt = 0; rt < kTiles; ++rt) {
-          float *r = red + ((size_t)warp * kRows + rt * 16) * 8;
-          r[g8 * 8 + 2 * t] = acc[rt][0];
-          r[g8 * 8 + 2 * t + 1] = acc[rt][1];
-          r[(g8 + 8) * 8 + 2 * t] = acc[rt][2];
-          r[(g8 + 8) * 8 + 2 * t + 1] = acc[rt][3];
+          const int r0 = rt * 16 + g8;
+          *reinterpret_cast<float2 *>(&r[r0 * 8 + 2 * t]) = make_float2(acc[rt][0], acc[rt][1]);
+          *reinterpret_cast<float2 *>(&r[(r0 + 8) * 8 + 2 * t]) =
+              make_float2(acc[rt][2], acc[rt][3]);
+          acc[rt][0] = acc[rt][1] = acc[rt][2] = acc[rt][3] = 0.f;
         }
-        consumer_bar();
-        float v[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int e = threadIdx.x + h * kConsumerWarps * 32;  // e = row * 8 + col
-          float sum = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) sum += red[(size_t)w * kPartial + e];
-          v[h] = sum;
-        }
-        const int n0 = s.tile * kRows;
-        if (s.n_splits == 1) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = threadIdx.x + h * kConsumerWarps * 32;
-            const int row = e >> 3, col = e & 7;
-            if (col < P.M && n0 + row < N) q.y[(size_t)col * N + n0 + row] = v[h];
-          }
-          consumer_bar();
-          if (threadIdx.x == 0) {
-            __threadfence();
-            atomicAdd(P.done_tiles, 1);
-          }
-          continue;
-        }
-        float *slots = P.partials + (size_t)s.tile_in_phase * wk.ph.max_splits * kPartial;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          __stcg(&slots[(size_t)s.split * kPartial + threadIdx.x + h * kConsumerWarps * 32],
-                 v[h]);
-        consumer_bar();  // the CTA's partial is written ...
-        if (threadIdx.x == 0) {
-          __threadfence();  // ... and published before the arrival is counted
-          const int prev = atomicAdd(&P.tile_count[s.tile_in_phase], 1);
-          __threadfence();  // the other runs' partials are visible after the count
-          s_last = prev == s.n_splits - 1;
-        }
-        consumer_bar();
-        if (s_last) {  // the tile's partials are all written: sum them in run order
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = threadIdx.x + h * kConsumerWarps * 32;
-            float sum = 0.f;
-            for (int r = 0; r < s.n_splits; ++r) sum += __ldcg(&slots[(size_t)r * kPartial + e]);
-            const int row = e >> 3, col = e & 7;
-            if (col < P.M && n0 + row < N) q.y[(size_t)col * N + n0 + row] = sum;
-          }
-          consumer_bar();
-          if (threadIdx.x == 0) {
-            P.tile_count[s.tile_in_phase] = 0;  // ready for the next launch
-            __threadfence();
-            atomicAdd(P.done_tiles, 1);
-          }
-        }
+        mbar_arrive_u32(red_full);
+        ++nseg;
+        s = s2;
+        have = have2;
+        wk = la;
       }
     }
   }
@@ -472,6 +551,8 @@ sv_status plan_shape(const sv_qmv_problem *pr, int n, int G, PlanShape &S) {
     S.phases.push_back(ph);
     i = j;
   }
+  // every phase but the first waits for all the tiles before it
+  for (size_t k = 0; k + 1 < S.phases.size(); ++k) S.phases[k].signal = 1;
   if (tiles_before >= (1 << 30))
     return fail(SV_ERR_UNSUPPORTED, "qmv_plan_create: too many tiles");
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
@@ -500,7 +581,7 @@ sv_status plan_config(int dev, int &grid, int &stages, uint32_t &smem) {
     return fail(SV_ERR_CUDA, "qmv_plan: cudaFuncSetAttribute failed: %s",
                 cudaGetErrorString(cudaGetLastError()));
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qmv_plan_kernel<kXF32>, kThreads, 0) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qmv_plan_kernel<kXF32>, kPlanThreads, 0) !=
           cudaSuccess ||
       occ < 1)
     return fail(SV_ERR_CUDA, "qmv_plan: occupancy query failed");
@@ -513,7 +594,7 @@ sv_status plan_config(int dev, int &grid, int &stages, uint32_t &smem) {
   smem = plan_layout(stages).total;
   if (smem > (uint32_t)optin) return fail(SV_ERR_UNSUPPORTED, "qmv_plan: shared memory");
   int fit = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, qmv_plan_kernel<kXF32>, kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, qmv_plan_kernel<kXF32>, kPlanThreads,
                                                     smem) != cudaSuccess ||
       fit < 1)
     return fail(SV_ERR_CUDA, "qmv_plan: occupancy query failed");
@@ -643,14 +724,20 @@ extern "C" sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream) {
   if (!plan) return fail(SV_ERR_INVALID_ARG, "qmv_plan_run: null plan");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan->grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kPlanThreads);
   cfg.dynamicSmemBytes = plan->smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the phase waits need it
   attr[0].val.cooperative = 1;
+  int na = 1;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   const cudaError_t e =
       plan->x_dtype == SV_BF16
           ? cudaLaunchKernelEx(&cfg, qmv_plan_kernel<false>, plan->params)

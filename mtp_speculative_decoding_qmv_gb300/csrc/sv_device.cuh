@@ -88,11 +88,12 @@ __device__ __forceinline__ bool mbar_try_wait_u32(uint32_t bar, uint32_t parity,
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_u32(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait_u32(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait_u32(uint32_t bar, uint32_t parity,
+                                              uint32_t suspend_ns = 1000000u) {
+  if (mbar_try_wait_u32(bar, parity, suspend_ns)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
-    if (mbar_try_wait_u32(bar, parity)) return true;
+    if (mbar_try_wait_u32(bar, parity, suspend_ns)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
