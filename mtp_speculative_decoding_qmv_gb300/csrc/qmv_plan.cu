@@ -66,16 +66,33 @@ struct PlanProblem {  // CUtensorMap's own alignment (>= 64 bytes) carries over
 
 struct PlanPhase {
   int first, count;     // problems
-  long long work;       // stages in the phase
+  int work;             // stages in the phase (< 2^31)
+  int run_q, run_r;     // runs: work = run_q * G + run_r (see run_begin)
   int tiles_before;     // tiles of all earlier phases
   int wait;             // 1: activations are earlier outputs
   int signal;           // 1: a later phase waits for this one's tiles
   int max_splits;       // partial slots per tile
 };
 
+// One run of consecutive stages of one tile inside a CTA's range of a
+// phase; each CTA's records are contiguous and in order (built on the host).
+struct PlanSeg {
+  const void *x;        // the problem's activations
+  int K;                // the problem's input size
+  int p;                // problem
+  int tile;             // 64-row tile of the problem
+  int c0, c1;           // stages [c0, c1) of the tile
+  int split, n_splits;  // this run's place among the runs of the tile
+  int tile_in_phase;
+  int phase;
+  int pad;
+};
+
 struct PlanParams {
   const PlanProblem *problems;
   const PlanPhase *phases;
+  const PlanSeg *segs;  // [seg_off[G]]
+  const int *seg_off;   // [G + 1]: CTA c runs segs[seg_off[c] .. seg_off[c+1])
   float *partials;      // [tiles of a phase][max_splits][kPartial]
   int *tile_count;      // [tiles of a phase] arrivals
   int *done_tiles;      // tiles written (all phases so far)
@@ -96,74 +113,6 @@ __host__ __device__ inline PlanLayout plan_layout(int stages) {
   L.total = L.bar + (uint32_t)(2 * stages + 2) * 8u + 1024u;
   return L;
 }
-
-// Runs of a phase of W stages over G CTAs: with W >= G, CTA c takes
-// [floor(c W / G), floor((c+1) W / G)) (never empty); with W < G, CTA c < W
-// takes stage c alone and the others none.  So the CTAs whose runs meet a
-// tile are consecutive and every one of them holds part of it.
-__device__ __forceinline__ long long run_begin(int c, long long W, int G) {
-  return W >= G ? (long long)c * W / G : (c < W ? c : W);
-}
-__device__ __forceinline__ int owner(long long j, long long W, int G) {
-  if (W < G) return (int)j;
-  long long c = j * G / W;
-  while (c + 1 < G && (c + 1) * W / G <= j) ++c;
-  while (c > 0 && c * W / G > j) --c;
-  return (int)c;
-}
-
-// A run of consecutive stages of one tile inside a CTA's range.
-struct Segment {
-  int p;            // problem
-  int tile;
-  int c0, c1;       // stages [c0, c1) of the tile
-  int split, n_splits;
-  int tile_in_phase;
-};
-
-// Walks the segments of this CTA's run in one phase.
-struct SegmentWalker {
-  const PlanProblem *probs;
-  PlanPhase ph;
-  long long j, end;
-  int p;  // current problem (absolute index)
-  int G, cta;
-
-  __device__ void begin(const PlanParams &P, int phase, int cta_, int G_) {
-    probs = P.problems;
-    ph = P.phases[phase];
-    G = G_;
-    cta = cta_;
-    j = run_begin(cta, ph.work, G);
-    end = run_begin(cta + 1, ph.work, G);
-    p = ph.first;
-  }
-  __device__ bool next(Segment &s) {
-    if (j >= end) return false;
-    while (true) {
-      const PlanProblem &q = probs[p];
-      const long long lo = q.chunk_off, hi = lo + (long long)q.tiles * q.chunks;
-      if (j < hi) break;
-      ++p;
-    }
-    const PlanProblem &q = probs[p];
-    const long long rel = j - q.chunk_off;
-    s.p = p;
-    s.tile = (int)(rel / q.chunks);
-    s.c0 = (int)(rel % q.chunks);
-    const long long tile_start = q.chunk_off + (long long)s.tile * q.chunks;
-    const long long tile_end = tile_start + q.chunks;
-    const long long seg_end = tile_end < end ? tile_end : end;
-    s.c1 = s.c0 + (int)(seg_end - j);
-    const int first = owner(tile_start, ph.work, G);
-    const int last = owner(tile_end - 1, ph.work, G);
-    s.split = cta - first;
-    s.n_splits = last - first + 1;
-    s.tile_in_phase = q.tile_off + s.tile;
-    j = seg_end;
-    return true;
-  }
-};
 
 __device__ __forceinline__ int atom_add_acq_rel(int *p, int v) {
   int old;
@@ -254,11 +203,10 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
       int st = 0, ph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int f = 0; ok && f < P.n_phases; ++f) {
-        SegmentWalker wk;
-        wk.begin(P, f, cta, G);
-        Segment s;
-        while (ok && wk.next(s)) {
+      const int i_end = P.seg_off[cta + 1];
+      for (int i = P.seg_off[cta]; ok && i < i_end; ++i) {
+        const PlanSeg s = P.segs[i];
+        {
           const PlanProblem &q = P.problems[s.p];
           const int n0 = s.tile * kRows;
           for (int c = s.c0; c < s.c1; ++c) {
@@ -297,11 +245,16 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     unsigned nseg = 0;
     const float4 *red4 = reinterpret_cast<const float4 *>(red);
     pdl_wait();  // y and the plan's counters belong to the preceding kernel until here
-    for (int f = 0; f < P.n_phases; ++f) {
-      SegmentWalker wk;
-      wk.begin(P, f, cta, G);
-      Segment s;
-      while (wk.next(s)) {
+    int cur_phase = -1, max_splits = 1, signal = 0;
+    const int i_end = P.seg_off[cta + 1];
+    for (int i = P.seg_off[cta]; i < i_end; ++i) {
+      const PlanSeg s = P.segs[i];
+      if (s.phase != cur_phase) {
+        cur_phase = s.phase;
+        max_splits = P.phases[cur_phase].max_splits;
+        signal = P.phases[cur_phase].signal;
+      }
+      {
         if (!mbar_wait_u32(red_full, nseg & 1, kEpilogueSuspendNs))
           atomicOr(&g_plan_device_error, 8u);
         float4 v[4];  // rows lane (v[0], v[1]) and lane + 32 (v[2], v[3]); 8 columns each
@@ -326,7 +279,7 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
         float4 *slots = nullptr;
         if (s.n_splits > 1) {
           slots = reinterpret_cast<float4 *>(P.partials) +
-                  (size_t)s.tile_in_phase * wk.ph.max_splits * (kPartial / 4);
+                  (size_t)s.tile_in_phase * max_splits * (kPartial / 4);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             __stcg(&slots[(size_t)s.split * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)],
@@ -370,7 +323,7 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
           __syncwarp();
           if (lane == 0) {
             if (slots) P.tile_count[s.tile_in_phase] = 0;  // ready for the next launch
-            if (wk.ph.signal) red_add_release(P.done_tiles, 1);
+            if (signal) red_add_release(P.done_tiles, 1);
           }
         }
       }
@@ -390,76 +343,74 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     float acc[kTiles][4];
 #pragma unroll
     for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    for (int f = 0; f < P.n_phases; ++f) {
-      SegmentWalker wk;
-      wk.begin(P, f, cta, G);
-      if (wk.ph.wait) {
-        // every tile of the earlier phases is written before x is read
-        if (threadIdx.x == 0 && !wait_count(P.done_tiles, wk.ph.tiles_before))
-          atomicOr(&g_plan_device_error, 4u);
-        consumer_bar();
-      }
-      Segment s;
-      bool have = wk.next(s);
-      XRaw<kXF32> xnext;
-      if (have) {
-        const PlanProblem &q = P.problems[s.p];
-        xnext = load_x_l2<kXF32>(static_cast<const uint8_t *>(q.x) + (size_t)xm * q.K * xbytes,
-                                 s.c0 * kConsumerWarps + gl, t);
-      }
-      while (have) {
-        const PlanProblem &q = P.problems[s.p];
-        const void *xrow = static_cast<const uint8_t *>(q.x) + (size_t)xm * q.K * xbytes;
-        SegmentWalker la = wk;  // the next run of this phase, for the activation prefetch
-        Segment s2;
-        const bool have2 = la.next(s2);
-        const void *xrow2 = nullptr;
-        if (have2) {
-          const PlanProblem &q2 = P.problems[s2.p];
-          xrow2 = static_cast<const uint8_t *>(q2.x) + (size_t)xm * q2.K * xbytes;
+    const int i_end = P.seg_off[cta + 1];
+    int i = P.seg_off[cta];
+    int cur_phase = -1;
+    bool have_x = false;  // xnext holds the first stage of segment i
+    XRaw<kXF32> xnext;
+    PlanSeg s;
+    if (i < i_end) s = P.segs[i];
+    while (i < i_end) {
+      if (s.phase != cur_phase) {
+        cur_phase = s.phase;
+        const PlanPhase &pp = P.phases[cur_phase];
+        if (pp.wait) {
+          // every tile of the earlier phases is written before x is read
+          if (threadIdx.x == 0 && !wait_count(P.done_tiles, pp.tiles_before))
+            atomicOr(&g_plan_device_error, 4u);
+          consumer_bar();
         }
-        int g = s.c0 * kConsumerWarps + gl;
-        for (int c = s.c0; c < s.c1; ++c, g += kConsumerWarps) {
-          const XRaw<kXF32> xcur = xnext;
-          if (c + 1 < s.c1)
-            xnext = load_x_l2<kXF32>(xrow, g + kConsumerWarps, t);
-          else if (have2)
-            xnext = load_x_l2<kXF32>(xrow2, s2.c0 * kConsumerWarps + gl, t);
-          if (ok && !warp_wait_stage(full0 + 8u * st, ph)) {
-            ok = false;
-            if (lane == 0) atomicOr(&g_plan_device_error, 2u);
-          }
-          if (ok) {
-            const uint32_t stage = base + st * kStageBytesStream;
-            group_math<kXF32>(acc, stage + ldm_off, xcur, stage + sb_off, 16 * 16, 8 * 16,
-                              kRows * 16);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
-          if (++st == stages) {
-            st = 0;
-            ph ^= 1;
-          }
+        have_x = false;
+      }
+      const void *xrow = static_cast<const uint8_t *>(s.x) + (size_t)xm * s.K * xbytes;
+      if (!have_x) xnext = load_x_l2<kXF32>(xrow, s.c0 * kConsumerWarps + gl, t);
+      // the next run, for the activation prefetch (same phase only)
+      const bool have2 = i + 1 < i_end;
+      PlanSeg s2 = s;
+      if (have2) s2 = P.segs[i + 1];
+      const bool same = have2 && s2.phase == s.phase;
+      int g = s.c0 * kConsumerWarps + gl;
+      for (int c = s.c0; c < s.c1; ++c, g += kConsumerWarps) {
+        const XRaw<kXF32> xcur = xnext;
+        if (c + 1 < s.c1)
+          xnext = load_x_l2<kXF32>(xrow, g + kConsumerWarps, t);
+        else if (same)
+          xnext = load_x_l2<kXF32>(static_cast<const uint8_t *>(s2.x) + (size_t)xm * s2.K * xbytes,
+                                   s2.c0 * kConsumerWarps + gl, t);
+        if (ok && !warp_wait_stage(full0 + 8u * st, ph)) {
+          ok = false;
+          if (lane == 0) atomicOr(&g_plan_device_error, 2u);
         }
-        // hand the run's sums to the epilogue warp: red[warp][row][col]
-        if (nseg > 0 && !__all_sync(0xffffffffu, mbar_wait_u32(red_empty, (nseg - 1) & 1)) &&
-            lane == 0)
-          atomicOr(&g_plan_device_error, 16u);
-        float *r = red + warp * kPartial;
+        if (ok) {
+          const uint32_t stage = base + st * kStageBytesStream;
+          group_math<kXF32>(acc, stage + ldm_off, xcur, stage + sb_off, 16 * 16, 8 * 16,
+                            kRows * 16);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
+        if (++st == stages) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+      // hand the run's sums to the epilogue warp: red[warp][row][col]
+      if (nseg > 0 && !__all_sync(0xffffffffu, mbar_wait_u32(red_empty, (nseg - 1) & 1)) &&
+          lane == 0)
+        atomicOr(&g_plan_device_error, 16u);
+      float *r = red + warp * kPartial;
 #pragma unroll
-        for (int rt = 0; rt < kTiles; ++rt) {
-          const int r0 = rt * 16 + g8;
-          *reinterpret_cast<float2 *>(&r[r0 * 8 + 2 * t]) = make_float2(acc[rt][0], acc[rt][1]);
-          *reinterpret_cast<float2 *>(&r[(r0 + 8) * 8 + 2 * t]) =
-              make_float2(acc[rt][2], acc[rt][3]);
-          acc[rt][0] = acc[rt][1] = acc[rt][2] = acc[rt][3] = 0.f;
-        }
-        mbar_arrive_u32(red_full);
-        ++nseg;
-        s = s2;
-        have = have2;
-        wk = la;
+      for (int rt = 0; rt < kTiles; ++rt) {
+        const int r0 = rt * 16 + g8;
+        *reinterpret_cast<float2 *>(&r[r0 * 8 + 2 * t]) = make_float2(acc[rt][0], acc[rt][1]);
+        *reinterpret_cast<float2 *>(&r[(r0 + 8) * 8 + 2 * t]) =
+            make_float2(acc[rt][2], acc[rt][3]);
+        acc[rt][0] = acc[rt][1] = acc[rt][2] = acc[rt][3] = 0.f;
       }
+      mbar_arrive_u32(red_full);
+      ++nseg;
+      have_x = same;
+      s = s2;
+      ++i;
     }
   }
 
@@ -501,7 +452,9 @@ namespace {
 struct PlanShape {
   std::vector<PlanProblem> probs;
   std::vector<PlanPhase> phases;
-  size_t off_phases, off_partials, off_counts, off_done, total;
+  std::vector<int> seg_off;
+  std::vector<PlanSeg> segs;
+  size_t off_phases, off_seg_off, off_segs, off_partials, off_counts, off_done, total;
   int max_phase_tiles;
 };
 
@@ -536,9 +489,11 @@ sv_status plan_shape(const sv_qmv_problem *pr, int n, int G, PlanShape &S) {
       ++j;
     } while (j < n && !pr[j].after);
     ph.count = j - i;
-    ph.work = work;
-    if (work > (1ll << 31) - 1)
-      return fail(SV_ERR_UNSUPPORTED, "qmv_plan_create: a phase has more than 2^31 stages");
+    if (work > (1ll << 30))
+      return fail(SV_ERR_UNSUPPORTED, "qmv_plan_create: a phase has more than 2^30 stages");
+    ph.work = (int)work;
+    ph.run_q = (int)(work / G);
+    ph.run_r = (int)(work % G);
     // a tile of C stages meets at most ceil(C / q) + 1 runs of >= q stages
     const long long q_min = work / G;
     int max_chunks = 0;
@@ -553,12 +508,62 @@ sv_status plan_shape(const sv_qmv_problem *pr, int n, int G, PlanShape &S) {
   }
   // every phase but the first waits for all the tiles before it
   for (size_t k = 0; k + 1 < S.phases.size(); ++k) S.phases[k].signal = 1;
+  // Each CTA's runs, phase after phase: in a phase of W = q G + r stages CTA
+  // c takes [c q + min(c, r), (c+1) q + min(c+1, r)) of the flat (problem,
+  // tile, stage) order, so the first r CTAs take q+1 stages and the others q
+  // (none when q = 0 and c >= r); the CTAs whose runs meet a tile are
+  // consecutive and every one of them holds part of it.
+  auto run_begin = [](int c, int q, int r) { return c * q + std::min(c, r); };
+  auto owner = [](int j, int q, int r) {
+    const int big = r * (q + 1);
+    return j < big ? j / (q + 1) : r + (j - big) / q;
+  };
+  S.seg_off.assign(G + 1, 0);
+  S.segs.clear();
+  for (int c = 0; c < G; ++c) {
+    S.seg_off[c] = (int)S.segs.size();
+    for (int f = 0; f < (int)S.phases.size(); ++f) {
+      const PlanPhase &ph = S.phases[f];
+      int j = run_begin(c, ph.run_q, ph.run_r);
+      const int end = run_begin(c + 1, ph.run_q, ph.run_r);
+      int p = ph.first;
+      while (j < end) {
+        while (j >= S.probs[p].chunk_off + S.probs[p].tiles * S.probs[p].chunks) ++p;
+        const PlanProblem &q = S.probs[p];
+        PlanSeg g{};
+        g.x = q.x;
+        g.K = q.K;
+        g.p = p;
+        const int rel = j - q.chunk_off;
+        g.tile = rel / q.chunks;
+        g.c0 = rel - g.tile * q.chunks;
+        const int tile_start = q.chunk_off + g.tile * q.chunks;
+        const int tile_end = tile_start + q.chunks;
+        const int seg_end = std::min(tile_end, end);
+        g.c1 = g.c0 + (seg_end - j);
+        const int first = owner(tile_start, ph.run_q, ph.run_r);
+        g.split = c - first;
+        g.n_splits = owner(tile_end - 1, ph.run_q, ph.run_r) - first + 1;
+        if (g.n_splits > ph.max_splits)
+          return fail(SV_ERR_CUDA, "qmv_plan_create: internal split count error");
+        g.tile_in_phase = q.tile_off + g.tile;
+        g.phase = f;
+        S.segs.push_back(g);
+        j = seg_end;
+      }
+    }
+  }
+  S.seg_off[G] = (int)S.segs.size();
   if (tiles_before >= (1 << 30))
     return fail(SV_ERR_UNSUPPORTED, "qmv_plan_create: too many tiles");
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
   size_t off = up((size_t)n * sizeof(PlanProblem), 256);
   S.off_phases = off;
   off = up(off + S.phases.size() * sizeof(PlanPhase), 256);
+  S.off_seg_off = off;
+  off = up(off + S.seg_off.size() * sizeof(int), 256);
+  S.off_segs = off;
+  off = up(off + S.segs.size() * sizeof(PlanSeg), 256);
   S.off_partials = off;
   off = up(off + partial_floats * 4, 256);
   S.off_counts = off;
@@ -694,6 +699,8 @@ extern "C" sv_status qmv_plan_create(const sv_qmv_problem *problems, int n_probl
   std::vector<uint8_t> host(S.off_partials, 0);
   std::memcpy(host.data(), S.probs.data(), S.probs.size() * sizeof(PlanProblem));
   std::memcpy(host.data() + S.off_phases, S.phases.data(), S.phases.size() * sizeof(PlanPhase));
+  std::memcpy(host.data() + S.off_seg_off, S.seg_off.data(), S.seg_off.size() * sizeof(int));
+  std::memcpy(host.data() + S.off_segs, S.segs.data(), S.segs.size() * sizeof(PlanSeg));
   uint8_t *dbuf = static_cast<uint8_t *>(device_buffer);
   if (cudaMemcpy(dbuf, host.data(), host.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemset(dbuf + S.off_counts, 0, S.total - S.off_counts) != cudaSuccess)
@@ -708,6 +715,8 @@ extern "C" sv_status qmv_plan_create(const sv_qmv_problem *problems, int n_probl
   PlanParams &P = plan->params;
   P.problems = reinterpret_cast<const PlanProblem *>(dbuf);
   P.phases = reinterpret_cast<const PlanPhase *>(dbuf + S.off_phases);
+  P.seg_off = reinterpret_cast<const int *>(dbuf + S.off_seg_off);
+  P.segs = reinterpret_cast<const PlanSeg *>(dbuf + S.off_segs);
   P.partials = reinterpret_cast<float *>(dbuf + S.off_partials);
   P.tile_count = reinterpret_cast<int *>(dbuf + S.off_counts);
   P.done_tiles = reinterpret_cast<int *>(dbuf + S.off_done);
