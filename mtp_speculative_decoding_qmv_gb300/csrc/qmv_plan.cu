@@ -275,35 +275,52 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
         ++nseg;
         const PlanProblem &q = P.problems[s.p];
         const int N = q.N, n0 = s.tile * kRows;
+        // A split tile is summed by its first run (split 0): that CTA's run
+        // ends with the tile, so it reaches it last and the later runs,
+        // which start their CTAs' ranges with it, have usually published
+        // their partials already.  They store and count without waiting.
         bool write = true;
         float4 *slots = nullptr;
         if (s.n_splits > 1) {
           slots = reinterpret_cast<float4 *>(P.partials) +
                   (size_t)s.tile_in_phase * max_splits * (kPartial / 4);
+          int *count = &P.tile_count[s.tile_in_phase];
+          if (s.split > 0) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            __stcg(&slots[(size_t)s.split * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)],
-                   v[i]);
-          __syncwarp();
-          int last = 0;
-          if (lane == 0)  // publishes this run's partial, sees the others' if last
-            last = atom_add_acq_rel(&P.tile_count[s.tile_in_phase], 1) == s.n_splits - 1;
-          write = __shfl_sync(0xffffffffu, last, 0) != 0;
-          if (write) {
+            for (int i = 0; i < 4; ++i)
+              __stcg(&slots[(size_t)s.split * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)],
+                     v[i]);
+            __syncwarp();
+            if (lane == 0) red_add_release(count, 1);  // publishes this run's partial
+            write = false;
+          } else {
+            if (lane == 0 && !wait_count(count, s.n_splits - 1))
+              atomicOr(&g_plan_device_error, 32u);
             __syncwarp();  // the other lanes read after lane 0's acquire
+            // own partial first, then the later runs in run order
+#pragma unroll 1
+            for (int r = 1; r < s.n_splits; r += 2) {
+              float4 a[4], b[4];
+              const bool two = r + 1 < s.n_splits;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int r = 0; r < s.n_splits; ++r) {
-              float4 a[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                a[i] = __ldcg(&slots[(size_t)r * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)]);
+              for (int i = 0; i < 4; ++i) {
+                const size_t o = (size_t)(lane + 32 * (i >> 1)) * 2 + (i & 1);
+                a[i] = __ldcg(&slots[(size_t)r * (kPartial / 4) + o]);
+                b[i] = two ? __ldcg(&slots[(size_t)(r + 1) * (kPartial / 4) + o])
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 v[i].x += a[i].x;
                 v[i].y += a[i].y;
                 v[i].z += a[i].z;
                 v[i].w += a[i].w;
+                if (two) {
+                  v[i].x += b[i].x;
+                  v[i].y += b[i].y;
+                  v[i].z += b[i].z;
+                  v[i].w += b[i].w;
+                }
               }
             }
           }
