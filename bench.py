@@ -129,8 +129,10 @@ class Cycle:
     """Device buffers and the launch sequence of one verify+accept cycle."""
 
     def __init__(self, sv, torch, device, depth: int = 3, layers: int = wl.N_LAYERS,
-                 heads: int = wl.GDN_HEADS, dim: int = wl.GDN_DIM, seed: int = 0):
+                 heads: int = wl.GDN_HEADS, dim: int = wl.GDN_DIM, seed: int = 0,
+                 layout: str = "plans"):
         self.sv, self.torch, self.dev = sv, torch, device
+        self.layout = layout
         self.K = depth
         self.M = depth + 1
         self.layers = layers
@@ -185,7 +187,30 @@ class Cycle:
         self.out_tokens = torch.empty((1, self.M), device=device, dtype=torch.int32)
         self.n_acc = torch.empty((1,), device=device, dtype=torch.int32)
         self.flags = torch.empty((1,), device=device, dtype=torch.int32)
-        self.launches_per_step = len(self.qmv_calls) + layers + 2
+        self.plans = []
+        if layout == "plans":
+            self._make_plans()
+        self.qmv_launches = (len(self.plans) + 2 * layers if layout == "plans"
+                             else len(self.qmv_calls))
+        self.launches_per_step = self.qmv_launches + layers + 2
+
+    def _make_plans(self):
+        """Per layer: one plan for q, k, v and one for gate, up (projections
+        that read the same input), o and down as single launches; the LM head
+        as a plan.  Between them sit the dependency points of a decoder layer
+        (the GatedDeltaNet capture, then o, then down), so each is its own
+        launch, overlapped with its predecessor by programmatic dependent
+        launch."""
+        QmvPlan = self.sv.QmvPlan
+        names = [n for n, _, _ in wl.LAYER_PROJECTIONS]
+        n = len(names)
+        for layer in range(self.layers):
+            by = dict(zip(names, self.proj[layer * n:(layer + 1) * n]))
+            self.plans.append(QmvPlan([tuple(by[k][:5]) + (False,) for k in ("q", "k", "v")]))
+            self.plans.append(QmvPlan([tuple(by[k][:5]) + (False,) for k in ("gate", "up")]))
+        self.plans.append(QmvPlan([tuple(self.lm[:5]) + (False,)]))
+        self.plan_bytes = sum(qmv_bytes(self.M, w.shape[0], w.shape[1] * 8)
+                              for pl in self.plans for (w, *_rest) in pl.problems)
 
     def _qmv_buffers(self, N, Kin):
         t, g, d = self.torch, self.g, self.dev
@@ -197,43 +222,81 @@ class Cycle:
         y = t.empty((self.M, N), device=d, dtype=t.float32)
         return (w, s, b, x, y)
 
-    def prepare_drafts(self, noise: float = 0.5):
-        """Draft logits = target logits + N(0, noise) (once, outside timing);
-        drafts = the top token of each draft row."""
+    def prepare_drafts(self, noise: float = 0.5, logit_std: float = 3.0):
+        """Once, outside timing: the LM-head input is scaled so that the target
+        logits have standard deviation `logit_std` (3: about 70 % of drafts
+        accepted per position at T = 0.6, top-k 20, top-p 0.95); draft logits
+        = target logits + N(0, noise); drafts = the top token of each row."""
         t = self.torch
+        self.run_qmv(self.lm)
+        t.cuda.synchronize()
+        x = self.lm[3]
+        x.copy_((x.float() * (logit_std / float(self.target.std()))).to(x.dtype))
         self.run_qmv(self.lm)
         t.cuda.synchronize()
         z = self.target[:, : self.K].clone()
         z += t.randn(z.shape, generator=self.g, device=self.dev) * noise
         self.draft.copy_(z)
-        self.draft_tokens.copy_(z.argmax(dim=-1).to(t.int32))
+        # drafts drawn from the filtered draft distributions q (T 0.6, top-k
+        # 20, top-p 0.95), as the ratio test assumes
+        top, idx = (z[0] / 0.6).topk(20, dim=-1)
+        q = t.softmax(top, dim=-1)
+        keep = (q.cumsum(-1) - q) < 0.95
+        q = t.where(keep, q, t.zeros_like(q))
+        pick = t.multinomial(q / q.sum(-1, keepdim=True), 1, generator=self.g)
+        self.draft_tokens.copy_(idx.gather(-1, pick).view(1, self.K).to(t.int32))
 
     def run_qmv(self, c):
         w, s, b, x, y = c
         self.sv.qmv_smallm(w, s, b, x, y)
 
     def run(self):
+        """One cycle: per layer q, k, v -> GatedDeltaNet capture over the
+        verify tokens -> o -> gate, up -> down; LM head; spec_accept; one
+        tape replay committing the accepted prefix in every layer."""
+        self._forward(with_gdn=True)
         sv = self.sv
-        i = 0
-        for layer in range(self.layers):
-            for _ in range(4):  # q, k, v, o
-                self.run_qmv(self.proj[i])
-                i += 1
-            sv.gdn_tape_capture(self.state[layer:layer + 1], self.gq[layer], self.gk[layer],
-                                self.gv[layer], self.galpha[layer], self.gbeta[layer],
-                                tape=self.tapes[layer], out=self.gout[layer])
-            for _ in range(3):  # gate, up, down
-                self.run_qmv(self.proj[i])
-                i += 1
-        self.run_qmv(self.lm)
         sv.spec_accept(self.target, self.draft, self.draft_tokens, self.ua, self.us,
                        0.6, 20, 0.95, workspace=self.ws, out_tokens=self.out_tokens,
                        n_accepted=self.n_acc, err_flags=self.flags)
         sv.gdn_tape_replay(self.state, self.tape, self.n_acc, self.M, n_replay_bias=1)
 
     def run_qmv_only(self):
-        for c in self.qmv_calls:
-            self.run_qmv(c)
+        self._forward(with_gdn=False)
+
+    def run_plans_only(self):
+        for pl in self.plans:
+            pl.run()
+
+    def _gdn(self, layer):
+        self.sv.gdn_tape_capture(self.state[layer:layer + 1], self.gq[layer], self.gk[layer],
+                                 self.gv[layer], self.galpha[layer], self.gbeta[layer],
+                                 tape=self.tapes[layer], out=self.gout[layer])
+
+    def _forward(self, with_gdn):
+        n = len(wl.LAYER_PROJECTIONS)
+        for layer in range(self.layers):
+            if self.layout == "plans":
+                by = dict(zip([m for m, _, _ in wl.LAYER_PROJECTIONS],
+                              self.proj[layer * n:(layer + 1) * n]))
+                self.plans[2 * layer].run()           # q, k, v
+                if with_gdn:
+                    self._gdn(layer)
+                self.run_qmv(by["o"])
+                self.plans[2 * layer + 1].run()       # gate, up
+                self.run_qmv(by["down"])
+            else:
+                c = self.proj[layer * n:(layer + 1) * n]
+                for i in range(3):  # q, k, v
+                    self.run_qmv(c[i])
+                if with_gdn:
+                    self._gdn(layer)
+                for i in range(3, n):  # o, gate, up, down
+                    self.run_qmv(c[i])
+        if self.layout == "plans":
+            self.plans[-1].run()
+        else:
+            self.run_qmv(self.lm)
 
 
 def capture(torch, fn, stream):
@@ -397,7 +460,7 @@ def run_cycle(args):
         log(f"cpu oracle: {t:.2f} s per cycle (extrapolated) on {threads} threads")
 
     sv.set_pdl(True)
-    cyc = Cycle(sv, torch, device, depth=args.depth, seed=rank)
+    cyc = Cycle(sv, torch, device, depth=args.depth, seed=rank, layout=args.layout)
     cyc.prepare_drafts()
     stream = torch.cuda.Stream(device)
     graph = capture(torch, cyc.run, stream)
@@ -417,13 +480,31 @@ def run_cycle(args):
     total_cycles = args.steps * world
     value = total_cycles / (ms / 1e3)
 
-    # the dominant kernel: the cycle's 449 qmv_smallm launches as their own graph
-    qms = time_graph(torch, qgraph, stream, args.steps, 1)
-    n_q = len(cyc.qmv_calls)
-    per_launch_s = qms / 1e3 / (args.steps * n_q)
-    bytes_per_launch = cyc.qmv_bytes / n_q
+    # the dominant kernel: the cycle's qmv launches (plans or single
+    # projections) as their own graph
+    qms = time_graph(torch, qgraph, stream, args.steps, 3)
+    qmv_all_gbs = cyc.qmv_bytes / (qms / 1e3 / args.steps) / 1e9
+    if args.layout == "plans":
+        # qmv_plan launches (q,k,v and gate,up of every layer, the LM head) in
+        # cycle order as their own graph
+        pgraph = capture(torch, cyc.run_plans_only, stream)
+        pms = time_graph(torch, pgraph, stream, args.steps, 3)
+        del pgraph
+        n_q, q_bytes, q_ms = len(cyc.plans), cyc.plan_bytes, pms
+    else:
+        n_q, q_bytes, q_ms = cyc.qmv_launches, cyc.qmv_bytes, qms
+    per_launch_s = q_ms / 1e3 / (args.steps * n_q)
+    bytes_per_launch = q_bytes / n_q
     achieved = bytes_per_launch / per_launch_s / 1e9
     peaks = measured_peaks()
+    # the whole weight stream of the cycle (every projection and the LM head,
+    # M rows each) as one plan without waits: the qmv kernel's streaming rate
+    stream_plan = sv.QmvPlan([tuple(c[:5]) + (False,) for c in cyc.qmv_calls])
+    sgraph = capture(torch, stream_plan.run, stream)
+    sms = time_graph(torch, sgraph, stream, args.steps, 3) / args.steps
+    stream_gbs = cyc.qmv_bytes / (sms / 1e3) / 1e9
+    del sgraph
+    stream_plan.close()
 
     # end to end through the API: drafts/uniforms in from pinned host memory,
     # tokens and accepted length back, every step
@@ -479,18 +560,29 @@ def run_cycle(args):
                    "cycle_gb_per_s": cycle_bytes / (per_step_ms / 1e3) / 1e9,
                    "l2": "inputs larger than L2 (13.8 GB weight stream per step)",
                    "graph": "one CUDA graph per cycle, PDL between qmv launches",
+                   "layout": args.layout,
                    "arithmetic": "4-bit weights x bf16 rows on bf16 MMA, fp32 accumulate; "
                                  "accept and GDN in fp32",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "qmv_smallm", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "qmv_plan" if args.layout == "plans" else "qmv_smallm",
+                     "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                      "peak_source": peaks["source"],
                      "bytes_per_launch": bytes_per_launch,
                      "launch_us": per_launch_s * 1e6,
-                     "how": f"the cycle's {n_q} qmv_smallm launches (M={args.depth + 1}) "
-                            f"captured as their own graph, CUDA events over {args.steps} "
-                            f"replays on the launching stream"},
+                     "how": f"the cycle's {n_q} launches of this kernel (M={args.depth + 1}) "
+                            f"in cycle order captured as their own graph, CUDA events over "
+                            f"{args.steps} replays on the launching stream"},
+        "qmv_all": {"value": qmv_all_gbs, "unit": "GB/s", "frac": qmv_all_gbs / peaks["hbm_gbs"],
+                    "launches": cyc.qmv_launches,
+                    "how": "every qmv launch of the cycle (plans and single projections) in "
+                           "cycle order as one graph"},
+        "qmv_stream": {"value": stream_gbs, "unit": "GB/s", "frac": stream_gbs / peaks["hbm_gbs"],
+                       "ms": sms, "bytes": cyc.qmv_bytes,
+                       "how": f"all {len(cyc.qmv_calls)} projections of the cycle (27B-class "
+                              f"weight stream, M={args.depth + 1}) as one qmv plan without "
+                              f"waits, CUDA events over {args.steps} graph replays"},
         "cpu_baseline": cpu,
         "e2e": {"value": total_cycles / t_e2e, "unit": "cycles/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -612,6 +704,51 @@ def run_qmv(args):
     return 0
 
 
+def run_stream(args):
+    """The 27B-class verify weight stream (--layers decoder layers of q, k,
+    v, o 5120x5120, gate, up 5120->17408, down 17408->5120, plus the LM head
+    5120->151936) at M = depth + 1 as ONE qmv plan without dependency waits:
+    the qmv kernel's streaming rate.  Also the case the ncu captures of the
+    plan kernel run (a few layers)."""
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    M = args.depth + 1
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.MASTER_SEED + 41)
+    shapes = [(N, K) for _ in range(args.layers) for _, N, K in wl.LAYER_PROJECTIONS]
+    shapes.append((wl.VOCAB, wl.HIDDEN))
+    probs = []
+    for N, K in shapes:
+        w = torch.randint(-(2 ** 31), 2 ** 31 - 1, (N, K // 8), generator=g, device=dev,
+                          dtype=torch.int32)
+        s_ = (torch.randn((N, K // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        b_ = (torch.randn((N, K // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        probs.append((w, s_, b_, x, torch.empty((M, N), device=dev), False))
+    plan = sv.QmvPlan(probs)
+    nbytes = sum(qmv_bytes(M, N, K) for N, K in shapes)
+    stream = torch.cuda.Stream(dev)
+    graph = capture(torch, plan.run, stream)
+    ms = time_graph(torch, graph, stream, args.steps, args.warmup) / args.steps
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"27B-class weight stream: {args.layers} layers x {{q,k,v,o "
+                                   f"5120x5120; gate,up 5120->17408; down 17408->5120}} + LM "
+                                   f"head 5120->151936, 4-bit g64, M={M}, one qmv plan",
+                       "bytes": nbytes, "grid": plan.grid,
+                       "l2": "inputs larger than L2" if nbytes > 3e8 else "small case"},
+            "ms_per_step": ms, "frac": gbs / peaks["hbm_gbs"], "peak": peaks}
+    print(json.dumps(line), flush=True)
+    sv.device_status()
+    return 0
+
+
 def run_lmhead(args):
     """LM-head verify + accept: 32 sequences x (M=4 LM-head qmv 5120->151936)
     then one spec_accept over the batch (draft = target + N(0, 0.5))."""
@@ -727,8 +864,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--depth", type=int, default=3, help="draft depth K (M = K+1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn", "qmv"],
+    ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn", "qmv", "stream"],
                     default="cycle")
+    ap.add_argument("--layers", type=int, default=wl.N_LAYERS,
+                    help="decoder layers of the --workload stream plan")
+    ap.add_argument("--layout", choices=["plans", "launches"], default="plans",
+                    help="cycle: qmv plans per layer (persistent launches with dependency "
+                         "waits) or one qmv_smallm launch per projection")
     ap.add_argument("--shape", type=int, nargs=2, metavar=("N", "K"),
                     default=[wl.INTERMEDIATE, wl.HIDDEN],
                     help="output and input size of the --workload qmv projection")
@@ -738,7 +880,7 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     return {"cycle": run_cycle, "mlp": run_mlp, "lmhead": run_lmhead, "gdn": run_gdn,
-            "qmv": run_qmv}[
+            "qmv": run_qmv, "stream": run_stream}[
         args.workload](args)
 
 
