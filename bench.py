@@ -54,6 +54,13 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+# DRAM bytes (read + written) per algorithmic byte of one qmv_plan launch,
+# from the ncu capture of the 4-layer weight-stream plan (bench.py --workload
+# stream --layers 4): 1.2926 GB of traffic for 1.2830 GB of algorithmic bytes.
+# Re-take it whenever the plan kernel changes.
+PLAN_TRAFFIC_RATIO = 1.2926 / 1.2830
+
+
 def qmv_bytes(M: int, N: int, K: int) -> int:
     """Algorithmic bytes of one qmv_smallm call: packed nibbles, bf16 scales
     and biases, bf16 rows in, fp32 rows out."""
@@ -567,7 +574,13 @@ def run_cycle(args):
         "roofline": {"kernel": "qmv_plan" if args.layout == "plans" else "qmv_smallm",
                      "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": (bytes_per_launch * PLAN_TRAFFIC_RATIO
+                                 if args.layout == "plans" else None),
+                     "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of "
+                                        "one 4-layer weight-stream plan launch, scaled to this "
+                                        "launch size by algorithmic bytes"
+                                        if args.layout == "plans" else None),
                      "peak_source": peaks["source"],
                      "bytes_per_launch": bytes_per_launch,
                      "launch_us": per_launch_s * 1e6,

@@ -97,6 +97,21 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
   const int i = r0 + tid / kLanesPerRow;  // state row (value dim)
   const int j = tid % kLanesPerRow;
   const bool row_ok = i < a.dv;
+  pdl_launch_dependents();
+  // the committed state does not depend on the preceding kernel: its load
+  // overlaps that kernel's tail under programmatic dependent launch
+  float S[kChunks * 4];
+  const float *src = a.state0 + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk;
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row_ok && chunk_col(j, c) < a.dk) f = *reinterpret_cast<const float4 *>(src + chunk_col(j, c));
+    S[4 * c] = f.x;
+    S[4 * c + 1] = f.y;
+    S[4 * c + 2] = f.z;
+    S[4 * c + 3] = f.w;
+  }
+  pdl_wait();  // the verify tokens' q, k, v and gates are the preceding kernels' outputs
   // the tokens' keys, queries, gates and this CTA's values, once
   for (int t = 0; t < a.T; ++t) {
     const size_t bth = ((size_t)b * a.T + t) * a.H + h;
@@ -111,17 +126,6 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
     }
   }
 
-  float S[kChunks * 4];
-  const float *src = a.state0 + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk;
-#pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row_ok && chunk_col(j, c) < a.dk) f = *reinterpret_cast<const float4 *>(src + chunk_col(j, c));
-    S[4 * c] = f.x;
-    S[4 * c + 1] = f.y;
-    S[4 * c + 2] = f.z;
-    S[4 * c + 3] = f.w;
-  }
   __syncthreads();
 
   for (int t = 0; t < a.T; ++t) {
@@ -188,6 +192,8 @@ __global__ void __launch_bounds__(kThreads) gdn_replay_kernel(const GdnArgs a) {
   __shared__ float als[kMaxT];
   const int tid = threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
+  pdl_launch_dependents();
+  pdl_wait();  // the accepted counts are the preceding kernel's output
   int L = a.n_replay[b % a.n_replay_count] + a.n_replay_bias;
   const bool clamped = L < 0 || L > a.T;
   L = min(max(L, 0), a.T);
@@ -303,7 +309,17 @@ extern "C" sv_status gdn_tape_capture(const float *state0, const float *q, const
   args.dk = dk;
   args.dv = dv;
   dim3 grid((unsigned)((dv + kRowsPerCta - 1) / kRowsPerCta), (unsigned)H, (unsigned)B);
-  gdn_capture_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, gdn_capture_kernel, args) != cudaSuccess)
+    return fail(SV_ERR_CUDA, "gdn_capture: launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return check_launch("gdn_tape_capture");
 }
 
@@ -339,6 +355,16 @@ extern "C" sv_status gdn_tape_replay(float *state, const float *tape, const int3
   args.dk = dk;
   args.dv = dv;
   dim3 grid((unsigned)((dv + kRowsPerCta - 1) / kRowsPerCta), (unsigned)H, (unsigned)B);
-  gdn_replay_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, gdn_replay_kernel, args) != cudaSuccess)
+    return fail(SV_ERR_CUDA, "gdn_replay: launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return check_launch("gdn_tape_replay");
 }
