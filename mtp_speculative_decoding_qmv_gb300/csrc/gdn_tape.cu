@@ -112,17 +112,27 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
     S[4 * c + 3] = f.w;
   }
   pdl_wait();  // the verify tokens' q, k, v and gates are the preceding kernels' outputs
-  // the tokens' keys, queries, gates and this CTA's values, once
-  for (int t = 0; t < a.T; ++t) {
-    const size_t bth = ((size_t)b * a.T + t) * a.H + h;
-    for (int c = tid; c < a.dk; c += kThreads) {
-      ks[t][c] = a.k[bth * a.dk + c];
-      qs[t][c] = a.q[bth * a.dk + c];
+  // the tokens' keys, queries, gates and this CTA's values, once; one flat
+  // unrolled loop so that the loads of all tokens are in flight together
+  {
+    const int nk = a.T * a.dk;
+#pragma unroll 4
+    for (int e = tid; e < nk; e += kThreads) {
+      const int t = e / a.dk, c = e - t * a.dk;
+      const size_t off = (((size_t)b * a.T + t) * a.H + h) * a.dk + c;
+      ks[t][c] = a.k[off];
+      qs[t][c] = a.q[off];
     }
-    if (tid < kRowsPerCta) vs[t][tid] = r0 + tid < a.dv ? a.v[bth * a.dv + r0 + tid] : 0.f;
-    if (tid == 0) {
-      als[t] = a.alpha[bth];
-      bes[t] = a.beta[bth];
+    const int nv = a.T * kRowsPerCta;
+    for (int e = tid; e < nv; e += kThreads) {
+      const int t = e / kRowsPerCta, r = e - t * kRowsPerCta;
+      const size_t bth = ((size_t)b * a.T + t) * a.H + h;
+      vs[t][r] = r0 + r < a.dv ? a.v[bth * a.dv + r0 + r] : 0.f;
+    }
+    if (tid < a.T) {
+      const size_t bth = ((size_t)b * a.T + tid) * a.H + h;
+      als[tid] = a.alpha[bth];
+      bes[tid] = a.beta[bth];
     }
   }
 
@@ -204,10 +214,19 @@ __global__ void __launch_bounds__(kThreads) gdn_replay_kernel(const GdnArgs a) {
   const int i = r0 + tid / kLanesPerRow;
   const int j = tid % kLanesPerRow;
   const bool row_ok = i < a.dv;
-  for (int t = 0; t < L; ++t) {
-    for (int c = tid; c < a.dk; c += kThreads) ks[t][c] = a.tape.k(b, t, h)[c];
-    if (tid < kRowsPerCta) es[t][tid] = r0 + tid < a.dv ? a.tape.e(b, t, h)[r0 + tid] : 0.f;
-    if (tid == 0) als[t] = *a.tape.alpha(b, t, h);
+  {  // the accepted records, all loads in flight together
+    const int nk = L * a.dk;
+#pragma unroll 4
+    for (int e = tid; e < nk; e += kThreads) {
+      const int t = e / a.dk, c = e - t * a.dk;
+      ks[t][c] = a.tape.k(b, t, h)[c];
+    }
+    const int ne = L * kRowsPerCta;
+    for (int e = tid; e < ne; e += kThreads) {
+      const int t = e / kRowsPerCta, r = e - t * kRowsPerCta;
+      es[t][r] = r0 + r < a.dv ? a.tape.e(b, t, h)[r0 + r] : 0.f;
+    }
+    if (tid < L) als[tid] = *a.tape.alpha(b, tid, h);
   }
   float S[kChunks * 4];
   float *dst = a.state + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk;

@@ -370,6 +370,19 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
   const int any_nonfinite = __syncthreads_or(nonfinite);
   const int nc = S.nc;
 
+  u64 *dst = a.cand + ((size_t)b * a.rows_max + rloc) * (size_t)a.C * kMaxTopK +
+             (size_t)cx * kMaxTopK;
+  if (nc <= kThreads) {
+    // ---- usual case: one candidate per thread; its rank among the (distinct)
+    // candidates is its place in the descending top-ksel list
+    if (tid < nc) {
+      const u64 mine = S.buf[tid];
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) rank += S.buf[j] > mine ? 1 : 0;
+      if (rank < ksel) dst[rank] = mine;
+    }
+    if (tid >= nc && tid < ksel) dst[tid] = 0;  // empty slots
+  } else {
   // ---- exact top-ksel of the chunk -----------------------------------------
   u64 thr;
   if (nc <= kCap) {
@@ -407,19 +420,25 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
     mine = S.top[tid];
     for (int j = 0; j < ntop; ++j) rank += S.top[j] > mine ? 1 : 0;
   }
-  u64 *dst = a.cand + ((size_t)b * a.rows_max + rloc) * (size_t)a.C * kMaxTopK +
-             (size_t)cx * kMaxTopK;
   if (tid < ntop) dst[rank] = mine;
   else if (tid < ksel) dst[tid] = 0;  // empty slots
+  }
   if (tid == 0 && any_nonfinite) atomicOr(&a.rowflags[b * a.rows_max + rloc], SV_FLAG_NONFINITE_LOGIT);
 
   // ---- the last CTA of this sequence finishes it ---------------------------
-  __threadfence();
+  // every thread's candidate stores precede thread 0's release (CTA barrier,
+  // then a cumulative acq_rel add); the last CTA acquires the others' lists
   __syncthreads();
-  if (tid == 0) S.last = atomicAdd(&a.counters[b], 1) == a.rows * a.C - 1;
+  if (tid == 0) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(&a.counters[b])
+                 : "memory");
+    S.last = old == a.rows * a.C - 1;
+  }
   __syncthreads();
   if (!S.last) return;
-  __threadfence();
 
   // merge: one warp per row, rows in waves.  The chunk-phase buffers are dead
   // from here on; this region aliases them.
