@@ -91,8 +91,8 @@ struct PlanSeg {
 struct PlanParams {
   const PlanProblem *problems;
   const PlanPhase *phases;
-  const PlanSeg *segs;  // [seg_off[G]]
-  const int *seg_off;   // [G + 1]: CTA c runs segs[seg_off[c] .. seg_off[c+1])
+  const PlanSeg *segs;  // [G] first run of each CTA (c0 == c1: none), then the rest
+  const int *seg_off;   // [G + 1]: CTA c's later runs are segs[seg_off[c] .. seg_off[c+1])
   float *partials;      // [tiles of a phase][max_splits][kPartial]
   int *tile_count;      // [tiles of a phase] arrivals
   int *done_tiles;      // tiles written (all phases so far)
@@ -163,6 +163,23 @@ __device__ __forceinline__ XRaw<kXF32> load_x_l2(const void *xrow, int g, int t)
   return r;
 }
 
+// This CTA's runs: the first at segs[cta] (loaded without waiting for the
+// offsets), the later ones from seg_off.
+struct RunList {
+  const PlanSeg *segs;
+  int head, rest, n;
+  __device__ RunList(const PlanParams &P, int cta) : segs(P.segs) {
+    const PlanSeg &h = P.segs[cta];
+    const int first = P.seg_off[cta], last = P.seg_off[cta + 1];
+    head = cta;
+    rest = first;
+    n = (h.c1 > h.c0 ? 1 : 0) + (last - first);
+  }
+  __device__ const PlanSeg &operator[](int i) const {
+    return i == 0 ? segs[head] : segs[rest + i - 1];
+  }
+};
+
 __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
 }
@@ -203,9 +220,9 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
       int st = 0, ph = 0;
       long long issued = 0;
       bool ok = true;
-      const int i_end = P.seg_off[cta + 1];
-      for (int i = P.seg_off[cta]; ok && i < i_end; ++i) {
-        const PlanSeg s = P.segs[i];
+      const RunList runs(P, cta);
+      for (int i = 0; ok && i < runs.n; ++i) {
+        const PlanSeg s = runs[i];
         {
           const PlanProblem &q = P.problems[s.p];
           const int n0 = s.tile * kRows;
@@ -246,9 +263,9 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     const float4 *red4 = reinterpret_cast<const float4 *>(red);
     pdl_wait();  // y and the plan's counters belong to the preceding kernel until here
     int cur_phase = -1, max_splits = 1, signal = 0;
-    const int i_end = P.seg_off[cta + 1];
-    for (int i = P.seg_off[cta]; i < i_end; ++i) {
-      const PlanSeg s = P.segs[i];
+    const RunList runs(P, cta);
+    for (int i = 0; i < runs.n; ++i) {
+      const PlanSeg s = runs[i];
       if (s.phase != cur_phase) {
         cur_phase = s.phase;
         max_splits = P.phases[cur_phase].max_splits;
@@ -360,13 +377,14 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     float acc[kTiles][4];
 #pragma unroll
     for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    const int i_end = P.seg_off[cta + 1];
-    int i = P.seg_off[cta];
+    const RunList runs(P, cta);
+    const int i_end = runs.n;
+    int i = 0;
     int cur_phase = -1;
     bool have_x = false;  // xnext holds the first stage of segment i
     XRaw<kXF32> xnext;
     PlanSeg s;
-    if (i < i_end) s = P.segs[i];
+    if (i < i_end) s = runs[0];
     while (i < i_end) {
       if (s.phase != cur_phase) {
         cur_phase = s.phase;
@@ -384,7 +402,7 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
       // the next run, for the activation prefetch (same phase only)
       const bool have2 = i + 1 < i_end;
       PlanSeg s2 = s;
-      if (have2) s2 = P.segs[i + 1];
+      if (have2) s2 = runs[i + 1];
       const bool same = have2 && s2.phase == s.phase;
       int g = s.c0 * kConsumerWarps + gl;
       for (int c = s.c0; c < s.c1; ++c, g += kConsumerWarps) {
@@ -431,11 +449,11 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     }
   }
 
-  // the last CTA to finish leaves the counters at zero for the next launch
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(P.done_ctas, 1) == G - 1) {
+  // the last CTA to finish leaves the tile count at zero for the next launch
+  // (a single-phase plan never counts tiles)
+  if (P.n_phases > 1) {
+    __syncthreads();
+    if (threadIdx.x == 0 && atom_add_acq_rel(P.done_ctas, 1) == G - 1) {
       *P.done_tiles = 0;
       *P.done_ctas = 0;
       __threadfence();
@@ -535,10 +553,10 @@ sv_status plan_shape(const sv_qmv_problem *pr, int n, int G, PlanShape &S) {
     const int big = r * (q + 1);
     return j < big ? j / (q + 1) : r + (j - big) / q;
   };
-  S.seg_off.assign(G + 1, 0);
-  S.segs.clear();
+  // per CTA, in order; then split into the first run of each CTA (at index
+  // c) and the later runs
+  std::vector<std::vector<PlanSeg>> per(G);
   for (int c = 0; c < G; ++c) {
-    S.seg_off[c] = (int)S.segs.size();
     for (int f = 0; f < (int)S.phases.size(); ++f) {
       const PlanPhase &ph = S.phases[f];
       int j = run_begin(c, ph.run_q, ph.run_r);
@@ -565,10 +583,17 @@ sv_status plan_shape(const sv_qmv_problem *pr, int n, int G, PlanShape &S) {
           return fail(SV_ERR_CUDA, "qmv_plan_create: internal split count error");
         g.tile_in_phase = q.tile_off + g.tile;
         g.phase = f;
-        S.segs.push_back(g);
+        per[c].push_back(g);
         j = seg_end;
       }
     }
+  }
+  S.segs.assign(G, PlanSeg{});  // c0 == c1 == 0: no run
+  S.seg_off.assign(G + 1, 0);
+  for (int c = 0; c < G; ++c) {
+    if (!per[c].empty()) S.segs[c] = per[c][0];
+    S.seg_off[c] = (int)S.segs.size();
+    for (size_t k = 1; k < per[c].size(); ++k) S.segs.push_back(per[c][k]);
   }
   S.seg_off[G] = (int)S.segs.size();
   if (tiles_before >= (1 << 30))
