@@ -140,28 +140,31 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
 
   for (int t = 0; t < a.T; ++t) {
     const float al = als[t], be = bes[t];
-    // S' = alpha S ; u = S' k   (chunks past dk hold zeros and contribute 0)
-    float u = 0.f;
+    // S' = alpha S ; u = S' k   (chunks past dk hold zeros and contribute 0;
+    // one partial sum per chunk keeps four independent FMA chains)
+    float uc[kChunks];
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
       S[4 * c] = __fmul_rn(al, S[4 * c]);
       S[4 * c + 1] = __fmul_rn(al, S[4 * c + 1]);
       S[4 * c + 2] = __fmul_rn(al, S[4 * c + 2]);
       S[4 * c + 3] = __fmul_rn(al, S[4 * c + 3]);
+      uc[c] = 0.f;
       if (chunk_col(j, c) < a.dk) {
         const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
-        u = fmaf(S[4 * c], kk.x, u);
-        u = fmaf(S[4 * c + 1], kk.y, u);
-        u = fmaf(S[4 * c + 2], kk.z, u);
-        u = fmaf(S[4 * c + 3], kk.w, u);
+        uc[c] = fmaf(S[4 * c], kk.x, uc[c]);
+        uc[c] = fmaf(S[4 * c + 1], kk.y, uc[c]);
+        uc[c] = fmaf(S[4 * c + 2], kk.z, uc[c]);
+        uc[c] = fmaf(S[4 * c + 3], kk.w, uc[c]);
       }
     }
-    u = row_sum(u);
+    float u = row_sum((uc[0] + uc[1]) + (uc[2] + uc[3]));
     const float e = be * (vs[t][tid / kLanesPerRow] - u);
     // S_t = S' + e k^T ; o = S_t q
-    float o = 0.f;
+    float oc[kChunks];
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
+      oc[c] = 0.f;
       if (chunk_col(j, c) < a.dk) {
         const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
         const float4 qq = *reinterpret_cast<const float4 *>(&qs[t][chunk_col(j, c)]);
@@ -169,13 +172,13 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
         S[4 * c + 1] = __fadd_rn(S[4 * c + 1], __fmul_rn(e, kk.y));
         S[4 * c + 2] = __fadd_rn(S[4 * c + 2], __fmul_rn(e, kk.z));
         S[4 * c + 3] = __fadd_rn(S[4 * c + 3], __fmul_rn(e, kk.w));
-        o = fmaf(S[4 * c], qq.x, o);
-        o = fmaf(S[4 * c + 1], qq.y, o);
-        o = fmaf(S[4 * c + 2], qq.z, o);
-        o = fmaf(S[4 * c + 3], qq.w, o);
+        oc[c] = fmaf(S[4 * c], qq.x, oc[c]);
+        oc[c] = fmaf(S[4 * c + 1], qq.y, oc[c]);
+        oc[c] = fmaf(S[4 * c + 2], qq.z, oc[c]);
+        oc[c] = fmaf(S[4 * c + 3], qq.w, oc[c]);
       }
     }
-    o = row_sum(o);
+    const float o = row_sum((oc[0] + oc[1]) + (oc[2] + oc[3]));
     const size_t bth = ((size_t)b * a.T + t) * a.H + h;
     if (row_ok && j == 0) {
       a.tape.e(b, t, h)[i] = e;
@@ -332,11 +335,8 @@ extern "C" sv_status gdn_tape_capture(const float *state0, const float *q, const
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  // launched in stream order (starting early measured slower); the kernel
+  // triggers its dependents at entry so the following kernel may start early
   if (cudaLaunchKernelEx(&cfg, gdn_capture_kernel, args) != cudaSuccess)
     return fail(SV_ERR_CUDA, "gdn_capture: launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return check_launch("gdn_tape_capture");
@@ -378,11 +378,8 @@ extern "C" sv_status gdn_tape_replay(float *state, const float *tape, const int3
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  // launched in stream order (starting early measured slower); the kernel
+  // triggers its dependents at entry so the following kernel may start early
   if (cudaLaunchKernelEx(&cfg, gdn_replay_kernel, args) != cudaSuccess)
     return fail(SV_ERR_CUDA, "gdn_replay: launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return check_launch("gdn_tape_replay");
