@@ -2,11 +2,12 @@
 """Benchmark of the verify-and-accept hot path on GB300.
 
 Default workload (one step = one verify+accept cycle at draft depth K=3,
-M=K+1=4 verify rows, batch 1, 27B-class stack):
-  per layer (64): q, k, v, o (5120x5120), gate, up (5120->17408), down
-      (17408->5120) -- all 4-bit affine g64 qmv_smallm -- and
-      gdn_tape_capture over the 4 verify tokens (48 heads, 128 x 128 fp32)
-  then the LM head (5120->151936) qmv_smallm whose output is the target
+M=K+1=4 verify rows, batch 1, 27B-class stack, 4-bit affine g64 weights):
+  per layer (64): q, k, v (5120x5120) as one qmv plan, gdn_tape_capture over
+      the 4 verify tokens (48 heads, 128 x 128 fp32), o (5120x5120)
+      qmv_smallm, gate, up (5120->17408) as one qmv plan, down (17408->5120)
+      qmv_smallm
+  then the LM head (5120->151936, a qmv plan) whose output is the target
   logits, spec_accept (temperature 0.6, top_k 20, top_p 0.95), and one
   gdn_tape_replay launch committing n_accepted + 1 tape records in all 64
   layers (n_accepted read on the device).
@@ -16,8 +17,9 @@ larger than L2, so every step streams from HBM.
 
 Prints one JSON line.  --impl reference times the CPU oracle instead
 (bounded sample of the same cycle, extrapolated).  --workload mlp | lmhead |
-gdn measure the MLP projections, the LM head + accept batch and the GDN tape
-on their own.
+gdn | stream | qmv measure the MLP projections, the LM head + accept batch,
+the GDN tape, the weight stream as one plan and one projection shape on
+their own.
 """
 from __future__ import annotations
 
@@ -40,6 +42,14 @@ import workloads as wl  # noqa: E402
 METRIC = "qmv_smallm HBM GB/s (% of peak) at M=4; verify+accept cycles/s at K=3"
 GROUP = 64
 WEIGHT_BYTES = 0.5625  # 4-bit nibble + bf16 scale and bias per 64 weights
+
+
+def roofline_rate(bandwidth_bytes_per_s: float, bytes_per_step: float) -> float:
+    """Upper bound on steps per second when every step streams `bytes_per_step`
+    from memory at `bandwidth_bytes_per_s` ("MTP in llama.cpp", section
+    "Theoretical maximum tg t/s": decode speed <= bandwidth / active-weight
+    bytes)."""
+    return bandwidth_bytes_per_s / bytes_per_step
 
 
 def log(*a):
@@ -596,6 +606,11 @@ def run_cycle(args):
                        "how": f"all {len(cyc.qmv_calls)} projections of the cycle (27B-class "
                               f"weight stream, M={args.depth + 1}) as one qmv plan without "
                               f"waits, CUDA events over {args.steps} graph replays"},
+        "cycle_roofline": {
+            "bound_cycles_per_s": roofline_rate(peaks["hbm_gbs"] * 1e9, cycle_bytes),
+            "frac": value / world / roofline_rate(peaks["hbm_gbs"] * 1e9, cycle_bytes),
+            "how": "measured HBM bandwidth / algorithmic bytes of one cycle (weights, "
+                   "activations, GDN state and tape)"},
         "cpu_baseline": cpu,
         "e2e": {"value": total_cycles / t_e2e, "unit": "cycles/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
