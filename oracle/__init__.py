@@ -65,6 +65,10 @@ def lib() -> ctypes.CDLL:
         L.oracle_gdn_capture.restype = None
         L.oracle_gdn_replay.argtypes = [P, P, P, P, P, I, I, I, I, I]
         L.oracle_gdn_replay.restype = None
+        L.oracle_conv_capture.argtypes = [P, P, P, I, I, I, I, P]
+        L.oracle_conv_capture.restype = None
+        L.oracle_conv_replay.argtypes = [P, P, P, I, I, I, I]
+        L.oracle_conv_replay.restype = None
         L.oracle_set_threads.argtypes = [I]
         L.oracle_has_openmp.restype = I
         _lib = L
@@ -191,3 +195,31 @@ def gdn_replay(state, tape, n_replay):
     assert nr.shape == (B,) and (nr >= 0).all() and (nr <= T).all()
     lib().oracle_gdn_replay(_ptr(S), _ptr(ta), _ptr(te), _ptr(tk), _ptr(nr), B, T, H, dk, dv)
     return S
+
+
+def conv_capture(window, x, weight):
+    """Causal depthwise convolution outputs y [B, T, C] (float64) of the T
+    verify inputs x [B, T, C] from the committed window [B, W-1, C], with
+    weight [W, C]."""
+    win = _c(window, np.float64)
+    xx = _c(x, np.float64)
+    w = _c(weight, np.float64)
+    B, T, C = xx.shape
+    W = w.shape[0]
+    assert win.shape == (B, W - 1, C) and w.shape == (W, C)
+    y = np.zeros((B, T, C), np.float64)
+    lib().oracle_conv_capture(_ptr(win), _ptr(xx), _ptr(w), B, T, C, W, _ptr(y))
+    return y
+
+
+def conv_replay(window, x, n_replay):
+    """The committed window [B, W-1, C] (float64 copy) after the first
+    n_replay[b] verify inputs of x [B, T, C]."""
+    win = np.array(window, dtype=np.float64, order="C", copy=True)
+    xx = _c(x, np.float64)
+    B, T, C = xx.shape
+    W = win.shape[1] + 1
+    nr = _c(n_replay, np.int32)
+    assert nr.shape == (B,) and (nr >= 0).all() and (nr <= T).all()
+    lib().oracle_conv_replay(_ptr(win), _ptr(xx), _ptr(nr), B, T, C, W)
+    return win

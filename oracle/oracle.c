@@ -478,3 +478,56 @@ void oracle_gdn_replay(double *state, const double *tape_alpha, const double *ta
             }
         }
 }
+
+/* ------------------------------------------------------------------------
+ * Short causal convolution windows of a GatedDeltaNet layer.
+ * [MLXCEL] "MTP와 DFlash", section "Qwen3.8-Flash-Next (qwen4_exp) MTP": the
+ * rollback replays the GatedDeltaNet recurrence and two convolution windows
+ * over the accepted tokens; the batched DFlash paragraph of the same page:
+ * linear-attention layers replay the convolution and recurrent state over
+ * each row's accepted prefix.  The pages give no formula; the reading
+ * adopted is the depthwise causal convolution of width W over a channel
+ * stream, whose state is the W-1 most recent inputs of every channel:
+ *   h(tau) = x[tau][c] for tau >= 0, window[W-1+tau][c] for -(W-1) <= tau < 0
+ *   y[t][c] = sum_{j=0}^{W-1} weight[j][c] * h(t - (W-1) + j)
+ * Layouts (time-major): window [B][W-1][C], x and y [B][T][C], weight [W][C].
+ * ------------------------------------------------------------------------ */
+static double conv_h(const double *win, const double *x, int W, int C, int c, int tau) {
+    return tau >= 0 ? x[(size_t)tau * C + c] : win[(size_t)(W - 1 + tau) * C + c];
+}
+
+/* Capture: outputs of the T verify tokens from the committed window, which is
+ * left unchanged.  Sum in ascending j. */
+void oracle_conv_capture(const double *window, const double *x, const double *weight, int B,
+                         int T, int C, int W, double *y) {
+    for (int b = 0; b < B; ++b) {
+        const double *win = window + (size_t)b * (W - 1) * C;
+        const double *xb = x + (size_t)b * T * C;
+        for (int t = 0; t < T; ++t)
+            for (int c = 0; c < C; ++c) {
+                double s = 0.0;
+                for (int j = 0; j < W; ++j)
+                    s += weight[(size_t)j * C + c] * conv_h(win, xb, W, C, c, t - (W - 1) + j);
+                y[((size_t)b * T + t) * C + c] = s;
+            }
+    }
+}
+
+/* Replay (commit): the window after the first L_b = n_replay[b] verify tokens
+ * is the last W-1 entries of (old window, x[0..L_b)); L_b = 0 leaves it as it
+ * is.  Written as W-1 positions of h, not as a shift, so that a test can
+ * compare it with shifting the window one token at a time. */
+void oracle_conv_replay(double *window, const double *x, const int32_t *n_replay, int B, int T,
+                        int C, int W) {
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)(W > 1 ? W - 1 : 1) * C);
+    for (int b = 0; b < B; ++b) {
+        double *win = window + (size_t)b * (W - 1) * C;
+        const double *xb = x + (size_t)b * T * C;
+        const int L = n_replay[b];
+        for (int i = 0; i < W - 1; ++i)
+            for (int c = 0; c < C; ++c)
+                tmp[(size_t)i * C + c] = conv_h(win, xb, W, C, c, L - (W - 1) + i);
+        memcpy(win, tmp, sizeof(double) * (size_t)(W - 1) * C);
+    }
+    free(tmp);
+}

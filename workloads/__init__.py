@@ -131,3 +131,21 @@ def gdn_inputs(stream: int, B: int, T: int, H: int, dk: int, dv: int, state_std:
     n_replay = g.integers(0, T + 1, size=B).astype(np.int32)
     return {"state0": np.ascontiguousarray(s0), "q": q, "k": k, "v": v,
             "alpha": alpha, "beta": beta, "n_replay": n_replay}
+
+
+# ----------------------------------------------------------------------------
+# short causal convolution windows of a GatedDeltaNet layer
+# ----------------------------------------------------------------------------
+CONV_WIDTH = 4
+CONV_CHANNELS = 3 * GDN_HEADS * GDN_DIM  # q, k, v streams of the 48 heads
+
+
+def conv_inputs(stream: int, B: int, T: int, C: int, W: int = CONV_WIDTH):
+    """Committed window [B, W-1, C] and verify inputs x [B, T, C] ~ N(0, 1),
+    weight [W, C] ~ N(0, 1/W) (float32); n_replay [B] ~ U{0..T}."""
+    g = rng(7, stream)
+    window = g.standard_normal((B, W - 1, C), dtype=np.float32)
+    x = g.standard_normal((B, T, C), dtype=np.float32)
+    weight = (g.standard_normal((W, C), dtype=np.float32) / np.float32(np.sqrt(W)))
+    n_replay = g.integers(0, T + 1, size=B).astype(np.int32)
+    return {"window": window, "x": x, "weight": weight, "n_replay": n_replay}
