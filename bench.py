@@ -932,6 +932,51 @@ def run_gdn(args):
     return 0
 
 
+def run_conv(args):
+    """Short convolution windows of a GatedDeltaNet layer: batch 16, T = 5
+    verify tokens, C = 3 x 48 x 128 channels (q, k, v streams), W = 4; the
+    capture's outputs and the commit of an accepted prefix ~ U{0..5}."""
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    B, T, C, W = 16, 5, wl.CONV_CHANNELS, wl.CONV_WIDTH
+    d = wl.conv_inputs(70, B, T, C, W)
+    copies = 24  # distinct buffers so that timing streams from HBM
+    t = {k: torch.from_numpy(v).to(dev) for k, v in d.items()}
+    wins = [t["window"].clone() for _ in range(copies)]
+    xs = [t["x"].clone() for _ in range(copies)]
+    ys = [torch.empty_like(t["x"]) for _ in range(copies)]
+
+    def cap():
+        for i in range(copies):
+            sv.conv_window_capture(wins[i], xs[i], t["weight"], y=ys[i])
+
+    def rep():
+        for i in range(copies):
+            sv.conv_window_replay(wins[i], xs[i], t["n_replay"])
+
+    stream = torch.cuda.Stream(dev)
+    gc, gr = capture(torch, cap, stream), capture(torch, rep, stream)
+    mc = time_graph(torch, gc, stream, args.steps, args.warmup) / args.steps / copies
+    mr = time_graph(torch, gr, stream, args.steps, args.warmup) / args.steps / copies
+    cap_bytes = 4 * (B * (W - 1) * C + 2 * B * T * C + W * C)
+    n_live = int((d["n_replay"] > 0).sum())
+    rep_bytes = 4 * n_live * (2 * (W - 1) * C)  # reads at most W-1 entries, writes W-1
+    peaks = measured_peaks()
+    line = {"metric": "conv window capture/commit GB/s", "value": cap_bytes / (mc / 1e3) / 1e9,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"conv windows: B={B}, T={T}, C={C}, W={W}, prefix ~ U{{0..{T}}}"},
+            "capture_us": mc * 1e3, "replay_us": mr * 1e3,
+            "capture_frac": cap_bytes / (mc / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "replay_gbs": rep_bytes / (mr / 1e3) / 1e9}
+    print(json.dumps(line), flush=True)
+    sv.device_status()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -940,7 +985,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--depth", type=int, default=3, help="draft depth K (M = K+1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn", "qmv", "stream"],
+    ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn", "qmv", "stream",
+                                           "conv"],
                     default="cycle")
     ap.add_argument("--layers", type=int, default=wl.N_LAYERS,
                     help="decoder layers of the --workload stream plan")
@@ -956,7 +1002,7 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     return {"cycle": run_cycle, "mlp": run_mlp, "lmhead": run_lmhead, "gdn": run_gdn,
-            "qmv": run_qmv, "stream": run_stream}[
+            "qmv": run_qmv, "stream": run_stream, "conv": run_conv}[
         args.workload](args)
 
 

@@ -18,6 +18,7 @@
  *   gdn_tape_capture  GatedDeltaNet recurrence over the verify tokens, with a
  *                     (gate, innovation, key) tape per token and head
  *   gdn_tape_replay   rebuild the recurrent state over an accepted prefix
+ *   conv_window_*     short convolution windows: outputs, commit of a prefix
  *
  * Conventions (all entry points):
  *  - Every tensor argument is a DEVICE pointer owned by the caller, to
@@ -298,6 +299,37 @@ sv_status gdn_tape_capture(const float *state0, const float *q, const float *k, 
 sv_status gdn_tape_replay(float *state, const float *tape, const int32_t *n_replay,
                           int n_replay_count, int n_replay_bias, int B, int T, int H, int dk,
                           int dv, int32_t *err_flags, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Short causal convolution windows of a GatedDeltaNet layer.                */
+/* ------------------------------------------------------------------------ */
+/* Source: "MTP와 DFlash" (mlxcel manual), section "Qwen3.8-Flash-Next
+ * (qwen4_exp) MTP": the rollback replays the GatedDeltaNet recurrence and two
+ * convolution windows over the accepted tokens; the batched DFlash paragraph
+ * of the same page: linear-attention layers replay the convolution and
+ * recurrent state over each row's accepted prefix.  The pages give no
+ * formula; implemented is the depthwise causal convolution of width W whose
+ * state is the W-1 most recent inputs of each channel:
+ *   h(tau) = x[tau][c] for tau >= 0, window[W-1+tau][c] for -(W-1) <= tau < 0
+ *   y[t][c] = sum_{j=0}^{W-1} weight[j][c] * h(t - (W-1) + j)   (fp32, j ascending)
+ * Layouts (fp32, time-major): window [B][W-1][C], x and y [B][T][C], weight
+ * [W][C].  Requires B >= 0 (0: no-op), 1 <= T <= 64, C >= 1, 2 <= W <= 8,
+ * 4-byte aligned pointers, no output overlapping an input.
+ *
+ * conv_window_capture: y for the T verify tokens; the committed window is
+ * read only (a rejection needs nothing restored).
+ * conv_window_replay: commit: window <- the last W-1 entries of (window,
+ * x[0..L_b)) with L_b = n_replay[b % n_replay_count] + n_replay_bias clamped
+ * to [0, T] (a clamp sets SV_FLAG_REPLAY_RANGE in err_flags[b] if given);
+ * L_b = 0 leaves the window unchanged.  An exact copy: bit for bit.  The
+ * verify inputs x are the tape of the convolution.  n_replay is read on the
+ * device (spec_accept's n_accepted, bias 1 when the last committed token is
+ * among the verify rows). */
+sv_status conv_window_capture(const float *window, const float *x, const float *weight, int B,
+                              int T, int C, int W, float *y, sv_stream_t stream);
+sv_status conv_window_replay(float *window, const float *x, const int32_t *n_replay,
+                             int n_replay_count, int n_replay_bias, int B, int T, int C, int W,
+                             int32_t *err_flags, sv_stream_t stream);
 
 #ifdef __cplusplus
 }

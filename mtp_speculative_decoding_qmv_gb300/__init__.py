@@ -22,7 +22,7 @@ __all__ = [
     "SvError", "lib", "abi_version", "qmv_smallm", "spec_accept", "spec_accept_workspace_bytes",
     "make_accept_workspace", "gdn_tape_bytes", "gdn_tape_capture", "gdn_tape_replay",
     "set_pdl", "get_pdl", "device_status", "FLAGS", "QmvPlan", "spec_accept_noalloc",
-    "spec_accept_noalloc_scratch_bytes",
+    "spec_accept_noalloc_scratch_bytes", "conv_window_capture", "conv_window_replay",
 ]
 
 _LIB_PATH = Path(__file__).resolve().parent / "libspecverify.so"
@@ -91,6 +91,10 @@ def lib() -> ctypes.CDLL:
         L.qmv_plan_destroy.restype = None
         L.qmv_plan_grid.argtypes = [P]
         L.qmv_plan_grid.restype = I
+        L.conv_window_capture.argtypes = [P, P, P, I, I, I, I, P, P]
+        L.conv_window_capture.restype = I
+        L.conv_window_replay.argtypes = [P, P, P, I, I, I, I, I, I, P, P]
+        L.conv_window_replay.restype = I
         L.gdn_tape_bytes.argtypes = [I, I, I, I, I]
         L.gdn_tape_bytes.restype = Z
         L.gdn_tape_capture.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P]
@@ -375,3 +379,38 @@ def gdn_tape_replay(state: torch.Tensor, tape: torch.Tensor, n_replay: torch.Ten
                                int(n_replay_bias), B, T, H, dk, dv, _ptr(err_flags), _stream(dev))
     _check(st, "gdn_tape_replay")
     return state
+
+
+def conv_window_capture(window: torch.Tensor, x: torch.Tensor, weight: torch.Tensor,
+                        y: torch.Tensor | None = None) -> torch.Tensor:
+    """Causal depthwise convolution outputs y [B, T, C] (fp32) of x [B, T, C]
+    from the committed window [B, W-1, C] (read only), weight [W, C]."""
+    dev = x.device
+    B, T, C = x.shape
+    W = weight.shape[0]
+    _need(window, "window", torch.float32, (B, W - 1, C), dev)
+    _need(x, "x", torch.float32, (B, T, C), dev)
+    _need(weight, "weight", torch.float32, (W, C), dev)
+    if y is None:
+        y = torch.empty((B, T, C), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, (B, T, C), dev)
+    _check(lib().conv_window_capture(_ptr(window), _ptr(x), _ptr(weight), B, T, C, W, _ptr(y),
+                                     _stream(dev)), "conv_window_capture")
+    return y
+
+
+def conv_window_replay(window: torch.Tensor, x: torch.Tensor, n_replay: torch.Tensor,
+                       n_replay_bias: int = 0, err_flags: torch.Tensor | None = None) -> None:
+    """Commits the first n_replay[b % len] + bias verify inputs of x [B, T, C]
+    into window [B, W-1, C] in place."""
+    dev = x.device
+    B, T, C = x.shape
+    W = window.shape[1] + 1
+    _need(window, "window", torch.float32, (B, W - 1, C), dev)
+    _need(x, "x", torch.float32, (B, T, C), dev)
+    _need(n_replay, "n_replay", torch.int32, None, dev)
+    if err_flags is not None:
+        _need(err_flags, "err_flags", torch.int32, (B,), dev)
+    _check(lib().conv_window_replay(_ptr(window), _ptr(x), _ptr(n_replay), n_replay.numel(),
+                                    int(n_replay_bias), B, T, C, W, _ptr(err_flags),
+                                    _stream(dev)), "conv_window_replay")

@@ -150,3 +150,20 @@ def test_replay_rejects(L):
                              None) == 1  # count < 1
     assert L.gdn_tape_replay(A, A + 0x1000000, A + 0x2000000, 1, 0, 0, 5, 4, 128, 128, None,
                              None) == 0
+
+
+def test_conv_window_rejects(L):
+    win, x, w, y = A, A + 0x1000000, A + 0x2000000, A + 0x3000000
+    assert L.conv_window_capture(win, x, w, 2, 5, 64, 1, y, None) == 2   # W < 2
+    assert L.conv_window_capture(win, x, w, 2, 5, 64, 9, y, None) == 2   # W > 8
+    assert L.conv_window_capture(win, x, w, 2, 65, 64, 4, y, None) == 2  # T > 64
+    assert L.conv_window_capture(win, x, w, 2, 0, 64, 4, y, None) == 1   # T < 1
+    assert L.conv_window_capture(None, x, w, 2, 5, 64, 4, y, None) == 1
+    assert L.conv_window_capture(win, x, w, 2, 5, 64, 4, x, None) == 1   # y overlaps x
+    assert L.conv_window_capture(win, x, w, 0, 5, 64, 4, y, None) == 0   # empty batch
+    n = A + 0x4000000
+    assert L.conv_window_replay(win, x, n, 3, 1, 2, 5, 64, 4, None, None) == 1  # count > B
+    assert L.conv_window_replay(win, x, None, 1, 1, 2, 5, 64, 4, None, None) == 1
+    assert L.conv_window_replay(win, win, n, 1, 1, 2, 5, 64, 4, None, None) == 1  # window = x
+    assert L.conv_window_replay(win + 2, x, n, 1, 1, 2, 5, 64, 4, None, None) == 1
+    assert L.conv_window_replay(win, x, n, 1, 1, 0, 5, 64, 4, None, None) == 0
