@@ -411,6 +411,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(torch, seconds: float, world: int, device) -> float:
+    """The slowest rank's time (replicas: the job ends when the last one does);
+    `seconds` itself on one rank.  All ranks call it."""
+    if world <= 1:
+        return seconds
+    import torch.distributed as dist
+
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, slowest_seconds: float) -> float:
+    """Whole-job throughput of `world` replicas, each doing `units_per_rank`
+    units: every rank's units over the slowest rank's time (weak scaling)."""
+    return units_per_rank * world / slowest_seconds
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -488,14 +506,9 @@ def run_cycle(args):
         ms = time_graph(torch, graph, stream, args.steps, args.warmup, barrier)
     clocks = clk.summary()
     per_step_ms = ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(torch, ms / 1e3, world, device) * 1e3
     total_cycles = args.steps * world
-    value = total_cycles / (ms / 1e3)
+    value = job_rate(args.steps, world, ms / 1e3)
 
     # the dominant kernel: the cycle's qmv launches (plans or single
     # projections) as their own graph
@@ -554,12 +567,7 @@ def run_cycle(args):
         e2e_step()
     t_e2e = time.perf_counter() - t0
     barrier()
-    if world > 1:
-        import torch.distributed as dist
-
-        tt = torch.tensor([t_e2e], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = max_over_ranks(torch, t_e2e, world, device)
     sv.device_status()
 
     if rank != 0:
