@@ -14,11 +14,13 @@
 //  * chunk phase: CTA (chunk, row) reads 16384 logits (coalesced 16-byte
 //    streaming loads), bounds the k-th largest from below by the minimum of
 //    64 (or 32, 16) group maxima, keeps only elements at or above that bound
-//    (typically ~1 % of them), finds the exact top-k among those with a block
-//    radix select on 64-bit keys (ordered float bits, then lower token id),
-//    sorts them and writes them to the workspace;
-//  * the last CTA of a sequence to finish (threadfence + atomic counter, no
-//    spinning) merges the per-chunk lists of each row (one warp per row,
+//    (typically ~1 % of them) as 64-bit keys (ordered float bits, then lower
+//    token id), and writes the chunk's exact top-k sorted to the workspace:
+//    with at most 512 candidates each thread ranks its own by counting the
+//    larger keys; otherwise a block radix select finds the k-th key first;
+//  * the last CTA of a sequence to finish (CTA barrier, then one acq_rel
+//    atomic add by thread 0; no spinning) merges the per-chunk lists of each
+//    row (one warp per row,
 //    k-way merge) and runs the acceptance for that sequence in one warp:
 //    softmax over the kept logits, top-p cut on the descending order,
 //    u < p/q test, residual (p - q)+ sampled by inverse CDF in ascending
