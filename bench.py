@@ -66,9 +66,10 @@ def measured_peaks():
 
 # DRAM bytes (read + written) per algorithmic byte of one qmv_plan launch,
 # from the ncu capture of the 4-layer weight-stream plan (bench.py --workload
-# stream --layers 4): 1.2926 GB of traffic for 1.2830 GB of algorithmic bytes.
+# stream --layers 4): 1.2921 GB of traffic for 1.2830 GB of algorithmic bytes.
 # Re-take it whenever the plan kernel changes.
-PLAN_TRAFFIC_RATIO = 1.2926 / 1.2830
+PLAN_TRAFFIC_RATIO = 1.292094 / 1.283004
+E_DRAWS = 16  # seeded draft/uniform draws the end-to-end steps rotate through
 
 
 def qmv_bytes(M: int, N: int, K: int) -> int:
@@ -205,26 +206,28 @@ class Cycle:
         self.n_acc = torch.empty((1,), device=device, dtype=torch.int32)
         self.flags = torch.empty((1,), device=device, dtype=torch.int32)
         self.plans = []
-        if layout == "plans":
+        if layout in ("plans", "allplans"):
             self._make_plans()
-        self.qmv_launches = (len(self.plans) + 2 * layers if layout == "plans"
-                             else len(self.qmv_calls))
+        self.qmv_launches = (len(self.plans) + (2 * layers if layout == "plans" else 0)
+                             if self.plans else len(self.qmv_calls))
         self.launches_per_step = self.qmv_launches + layers + 2
 
     def _make_plans(self):
         """Per layer: one plan for q, k, v and one for gate, up (projections
-        that read the same input), o and down as single launches; the LM head
-        as a plan.  Between them sit the dependency points of a decoder layer
-        (the GatedDeltaNet capture, then o, then down), so each is its own
-        launch, overlapped with its predecessor by programmatic dependent
-        launch."""
+        that read the same input); o and down as single launches ("plans") or
+        as one-problem plans ("allplans"); the LM head as a plan.  Between them
+        sit the dependency points of a decoder layer (the GatedDeltaNet
+        capture, then o, then down), so each is its own launch, overlapped
+        with its predecessor by programmatic dependent launch."""
         QmvPlan = self.sv.QmvPlan
         names = [n for n, _, _ in wl.LAYER_PROJECTIONS]
         n = len(names)
+        groups = ((("q", "k", "v"), ("gate", "up")) if self.layout == "plans" else
+                  (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)))
         for layer in range(self.layers):
             by = dict(zip(names, self.proj[layer * n:(layer + 1) * n]))
-            self.plans.append(QmvPlan([tuple(by[k][:5]) + (False,) for k in ("q", "k", "v")]))
-            self.plans.append(QmvPlan([tuple(by[k][:5]) + (False,) for k in ("gate", "up")]))
+            for grp in groups:
+                self.plans.append(QmvPlan([tuple(by[k][:5]) + (False,) for k in grp]))
         self.plans.append(QmvPlan([tuple(self.lm[:5]) + (False,)]))
         self.plan_bytes = sum(qmv_bytes(self.M, w.shape[0], w.shape[1] * 8)
                               for pl in self.plans for (w, *_rest) in pl.problems)
@@ -254,14 +257,20 @@ class Cycle:
         z = self.target[:, : self.K].clone()
         z += t.randn(z.shape, generator=self.g, device=self.dev) * noise
         self.draft.copy_(z)
-        # drafts drawn from the filtered draft distributions q (T 0.6, top-k
-        # 20, top-p 0.95), as the ratio test assumes
-        top, idx = (z[0] / 0.6).topk(20, dim=-1)
+        self.draft_tokens.copy_(self.sample_draft_tokens(1)[0])
+
+    def sample_draft_tokens(self, n: int):
+        """n independent draft-token sets [n, 1, K] (int32), each drawn from the
+        filtered draft distributions q (T 0.6, top-k 20, top-p 0.95), as the
+        ratio test assumes."""
+        t = self.torch
+        top, idx = (self.draft[0] / 0.6).topk(20, dim=-1)
         q = t.softmax(top, dim=-1)
         keep = (q.cumsum(-1) - q) < 0.95
         q = t.where(keep, q, t.zeros_like(q))
-        pick = t.multinomial(q / q.sum(-1, keepdim=True), 1, generator=self.g)
-        self.draft_tokens.copy_(idx.gather(-1, pick).view(1, self.K).to(t.int32))
+        pick = t.multinomial(q / q.sum(-1, keepdim=True), n, replacement=True,
+                             generator=self.g)                      # [K, n]
+        return idx.gather(-1, pick).t().reshape(n, 1, self.K).to(t.int32).contiguous()
 
     def run_qmv(self, c):
         w, s, b, x, y = c
@@ -302,6 +311,12 @@ class Cycle:
                 self.run_qmv(by["o"])
                 self.plans[2 * layer + 1].run()       # gate, up
                 self.run_qmv(by["down"])
+            elif self.layout == "allplans":
+                self.plans[4 * layer].run()           # q, k, v
+                if with_gdn:
+                    self._gdn(layer)
+                for i in range(1, 4):                 # o; gate, up; down
+                    self.plans[4 * layer + i].run()
             else:
                 c = self.proj[layer * n:(layer + 1) * n]
                 for i in range(3):  # q, k, v
@@ -310,7 +325,7 @@ class Cycle:
                     self._gdn(layer)
                 for i in range(3, n):  # o, gate, up, down
                     self.run_qmv(c[i])
-        if self.layout == "plans":
+        if self.plans:
             self.plans[-1].run()
         else:
             self.run_qmv(self.lm)
@@ -514,9 +529,10 @@ def run_cycle(args):
     # projections) as their own graph
     qms = time_graph(torch, qgraph, stream, args.steps, 3)
     qmv_all_gbs = cyc.qmv_bytes / (qms / 1e3 / args.steps) / 1e9
-    if args.layout == "plans":
-        # qmv_plan launches (q,k,v and gate,up of every layer, the LM head) in
-        # cycle order as their own graph
+    if cyc.plans:
+        # qmv_plan launches (q,k,v and gate,up of every layer -- with o and
+        # down for "allplans" -- and the LM head) in cycle order as their own
+        # graph
         pgraph = capture(torch, cyc.run_plans_only, stream)
         pms = time_graph(torch, pgraph, stream, args.steps, 3)
         del pgraph
@@ -537,22 +553,29 @@ def run_cycle(args):
     stream_plan.close()
 
     # end to end through the API: drafts/uniforms in from pinned host memory,
-    # tokens and accepted length back, every step
+    # tokens and accepted length back, every step.  Each step takes the next
+    # of E_DRAWS seeded draws of draft tokens and uniforms (a decode loop
+    # draws both afresh every cycle), so the accepted lengths reported are a
+    # sample mean, not one fixed draw.
     h_draft = cyc.draft.cpu().pin_memory()
-    h_tokens = cyc.draft_tokens.cpu().pin_memory()
-    h_ua, h_us = cyc.ua.cpu().pin_memory(), cyc.us.cpu().pin_memory()
+    h_tokens = cyc.sample_draft_tokens(E_DRAWS).cpu().pin_memory()
+    uni = [wl.accept_uniforms(1000 + 97 * rank + i, 1, cyc.K) for i in range(E_DRAWS)]
+    h_ua = torch.stack([torch.from_numpy(u[0]) for u in uni]).pin_memory()
+    h_us = torch.stack([torch.from_numpy(u[1]) for u in uni]).pin_memory()
     h_out = torch.empty_like(cyc.out_tokens, device="cpu").pin_memory()
     h_n = torch.empty_like(cyc.n_acc, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_draft, h_tokens, h_ua, h_us))
+    h2d = sum(t[0].numel() * t.element_size() for t in (h_tokens, h_ua, h_us))
+    h2d += h_draft.numel() * h_draft.element_size()
     d2h = h_out.numel() * 4 + h_n.numel() * 4
     accepted = []
 
     def e2e_step():
+        i = len(accepted) % E_DRAWS
         with torch.cuda.stream(stream):
             cyc.draft.copy_(h_draft, non_blocking=True)
-            cyc.draft_tokens.copy_(h_tokens, non_blocking=True)
-            cyc.ua.copy_(h_ua, non_blocking=True)
-            cyc.us.copy_(h_us, non_blocking=True)
+            cyc.draft_tokens.copy_(h_tokens[i], non_blocking=True)
+            cyc.ua.copy_(h_ua[i], non_blocking=True)
+            cyc.us.copy_(h_us[i], non_blocking=True)
             graph.replay()
             h_out.copy_(cyc.out_tokens, non_blocking=True)
             h_n.copy_(cyc.n_acc, non_blocking=True)
@@ -589,16 +612,16 @@ def run_cycle(args):
                    "arithmetic": "4-bit weights x bf16 rows on bf16 MMA, fp32 accumulate; "
                                  "accept and GDN in fp32",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "qmv_plan" if args.layout == "plans" else "qmv_smallm",
+        "roofline": {"kernel": "qmv_plan" if cyc.plans else "qmv_smallm",
                      "bound": "hbm", "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": (bytes_per_launch * PLAN_TRAFFIC_RATIO
-                                 if args.layout == "plans" else None),
+                                 if cyc.plans else None),
                      "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of "
                                         "one 4-layer weight-stream plan launch, scaled to this "
                                         "launch size by algorithmic bytes"
-                                        if args.layout == "plans" else None),
+                                        if cyc.plans else None),
                      "peak_source": peaks["source"],
                      "bytes_per_launch": bytes_per_launch,
                      "launch_us": per_launch_s * 1e6,
@@ -625,7 +648,10 @@ def run_cycle(args):
         "gpu_launches": cyc.launches_per_step * args.steps,
         "clocks": clocks,
         "acceptance": {"mean_accepted": statistics.mean(accepted) if accepted else None,
-                       "depth": args.depth},
+                       "depth": args.depth, "draws": min(len(accepted), E_DRAWS),
+                       "how": "accepted drafts per cycle over the e2e steps (warm-up "
+                              "included), each step a fresh seeded draw of draft "
+                              "tokens and uniforms"},
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -998,9 +1024,10 @@ def main(argv=None):
                     default="cycle")
     ap.add_argument("--layers", type=int, default=wl.N_LAYERS,
                     help="decoder layers of the --workload stream plan")
-    ap.add_argument("--layout", choices=["plans", "launches"], default="plans",
-                    help="cycle: qmv plans per layer (persistent launches with dependency "
-                         "waits) or one qmv_smallm launch per projection")
+    ap.add_argument("--layout", choices=["plans", "allplans", "launches"], default="plans",
+                    help="cycle: qmv plans for the projections that share an input and "
+                         "qmv_smallm for o and down (plans), plans for every projection "
+                         "(allplans), or one qmv_smallm launch per projection (launches)")
     ap.add_argument("--shape", type=int, nargs=2, metavar=("N", "K"),
                     default=[wl.INTERMEDIATE, wl.HIDDEN],
                     help="output and input size of the --workload qmv projection")
