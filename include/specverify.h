@@ -19,6 +19,7 @@
  *                     (gate, innovation, key) tape per token and head
  *   gdn_tape_replay   rebuild the recurrent state over an accepted prefix
  *   conv_window_*     short convolution windows: outputs, commit of a prefix
+ *   qmv_identity_probe  start-up check: block verify rows == single-row calls
  *
  * Conventions (all entry points):
  *  - Every tensor argument is a DEVICE pointer owned by the caller, to
@@ -26,9 +27,12 @@
  *    keeps no pointer after a call returns, except a qmv plan (below), which
  *    holds the pointers it was created with.
  *  - Calls are asynchronous on `stream` (NULL = the legacy default stream) and
- *    never synchronise with the host.
+ *    never synchronise with the host -- except qmv_plan_create and the
+ *    start-up probe qmv_identity_probe, which say so.
  *  - Arguments are validated on the host before any launch.  A nonzero status
- *    means nothing was launched (SV_ERR_CUDA: the launch itself failed).
+ *    means nothing was launched (SV_ERR_CUDA: the launch itself failed), except
+ *    for qmv_identity_probe, a sequence of launches that stops at the first
+ *    failing one.
  *    sv_last_error() returns a thread-local message for the last failure.
  *  - Data-dependent problems found on the device (a draft token out of range,
  *    a NaN logit, ...) never trap: they are reported in per-sequence flag
@@ -140,8 +144,11 @@ sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales, const uin
  * 256-byte aligned, at least qmv_plan_device_bytes; synchronous; the device
  * current at creation runs the plan); *plan_out is a host object freed by
  * qmv_plan_destroy.  The buffer and every problem's tensors must stay valid
- * while the plan is used.  qmv_plan_run: one cooperative launch on `stream`
- * (capturable in a CUDA graph); runs of one plan must not overlap in time.
+ * while the plan is used.  qmv_plan_run: one launch on `stream` of exactly
+ * as many CTAs as fit on the device at once (capturable in a CUDA graph);
+ * runs of one plan must not overlap in time.  Its CTAs wait on one another,
+ * so the plan assumes that no other work holds SMs indefinitely while it
+ * runs (kernels of other streams that themselves wait on this plan would).
  * With sv_set_pdl(1) the launch may start while the preceding kernel runs:
  * weights are streamed at once, while x, y and the plan's counters are
  * touched only after that kernel has finished.
@@ -169,6 +176,37 @@ sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream);
 void qmv_plan_destroy(sv_qmv_plan *plan);
 /* CTAs of the plan's launch (the co-resident count), 0 for NULL. */
 int qmv_plan_grid(const sv_qmv_plan *plan);
+
+/* ------------------------------------------------------------------------ */
+/* qmv_identity_probe: start-up check that block verification is exact.      */
+/* ------------------------------------------------------------------------ */
+/* Source: "MTP와 DFlash" (mlxcel manual), section "MTP 정확성 검사": when a
+ * worker starts, three independent synthetic inputs go through a verify block
+ * and through the equivalent single-token steps; block verification is used
+ * only if both agree byte for byte, and the verdict is kept per (model,
+ * block width).
+ *
+ * For the given weights (layout of qmv_smallm), three synthetic activation
+ * blocks x_s [M][K] (values in [-2, 2) from a hash of the element index,
+ * fp32 or bf16 per x_dtype) are generated on the device; each is multiplied
+ * with qmv_smallm as one M-row block and as M one-row calls, and the fp32
+ * outputs are compared as bit patterns.  *mismatches = the number of outputs
+ * (over the three blocks) whose bits differ; 0 means block verification of
+ * this projection at width M is exact.  Keeping the verdict per (weights, M)
+ * is the caller's part.
+ *
+ * Requires 1 <= M <= 8, N >= 1, K >= 64, K % 64 == 0; w_packed, scales and
+ * biases as qmv_smallm requires.  scratch: caller-owned device memory,
+ * 256-byte aligned, at least qmv_identity_probe_bytes(M, N, K, x_dtype)
+ * bytes (0 on invalid input), not overlapping the weights; its contents are
+ * overwritten.  Runs on `stream` and waits for it (synchronous: call it at
+ * start-up, outside stream capture).  On error *mismatches is -1 (or left
+ * unchanged when the arguments are rejected before any work). */
+size_t qmv_identity_probe_bytes(int M, int N, int K, sv_dtype x_dtype);
+sv_status qmv_identity_probe(const uint32_t *w_packed, const uint16_t *scales,
+                             const uint16_t *biases, sv_dtype x_dtype, int M, int N, int K,
+                             void *scratch, size_t scratch_bytes, int *mismatches,
+                             sv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* spec_accept: probability-ratio verification of K drafts per sequence.     */

@@ -91,6 +91,10 @@ def lib() -> ctypes.CDLL:
         L.qmv_plan_destroy.restype = None
         L.qmv_plan_grid.argtypes = [P]
         L.qmv_plan_grid.restype = I
+        L.qmv_identity_probe_bytes.argtypes = [I, I, I, I]
+        L.qmv_identity_probe_bytes.restype = Z
+        L.qmv_identity_probe.argtypes = [P, P, P, I, I, I, I, P, Z, ctypes.POINTER(I), P]
+        L.qmv_identity_probe.restype = I
         L.conv_window_capture.argtypes = [P, P, P, I, I, I, I, P, P]
         L.conv_window_capture.restype = I
         L.conv_window_replay.argtypes = [P, P, P, I, I, I, I, I, I, P, P]
@@ -184,6 +188,40 @@ def qmv_smallm(w_packed: torch.Tensor, scales: torch.Tensor, biases: torch.Tenso
                           M, N, K, 64, 4, _stream(dev))
     _check(st, "qmv_smallm")
     return y
+
+
+def qmv_identity_probe(w_packed: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+                       M: int, x_dtype: torch.dtype = torch.bfloat16) -> int:
+    """Start-up check of block verification for one projection: the number
+    of outputs, over three synthetic M-row activation blocks, where the M-row
+    qmv_smallm product differs in any bit from the same rows multiplied one at
+    a time (0: exact).  Synchronous."""
+    dev = w_packed.device
+    N, K8 = w_packed.shape
+    K = K8 * 8
+    if w_packed.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("w_packed must be int32 or uint32")
+    _need(w_packed, "w_packed", w_packed.dtype, (N, K8), dev)
+    if scales.dtype not in (torch.bfloat16, torch.int16):
+        raise TypeError("scales must be bfloat16 (or int16 bit patterns)")
+    _need(scales, "scales", scales.dtype, (N, K // 64), dev)
+    _need(biases, "biases", scales.dtype, (N, K // 64), dev)
+    if x_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x_dtype must be float32 or bfloat16")
+    dt = SV_BF16 if x_dtype == torch.bfloat16 else SV_F32
+    nbytes = int(lib().qmv_identity_probe_bytes(M, N, K, dt))
+    out = ctypes.c_int(-1)
+    if nbytes == 0:  # invalid: the probe itself reports why, before any work
+        _check(lib().qmv_identity_probe(_ptr(w_packed), _ptr(scales), _ptr(biases), dt, M, N, K,
+                                        None, 0, ctypes.byref(out), _stream(dev)),
+               "qmv_identity_probe")
+    scratch = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+    off = (-scratch.data_ptr()) % 256
+    st = lib().qmv_identity_probe(_ptr(w_packed), _ptr(scales), _ptr(biases), dt, M, N, K,
+                                  scratch.data_ptr() + off, nbytes, ctypes.byref(out),
+                                  _stream(dev))
+    _check(st, "qmv_identity_probe")
+    return int(out.value)
 
 
 class QmvPlan:

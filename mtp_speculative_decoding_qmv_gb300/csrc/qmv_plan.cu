@@ -11,7 +11,9 @@
 // by one, each pays the launch and the latency of its first weight stage
 // (several microseconds on this part, as much as streaming a 50 MB
 // projection takes), so the weight stream stops at every boundary.  Here the
-// whole list is one cooperative launch of exactly the co-resident CTAs:
+// whole list is one launch of exactly as many CTAs as fit on the GPU at once
+// (not a cooperative launch, which measured ~1.5 us slower per launch; see
+// qmv_plan_run for why every CTA still becomes resident):
 //  * the list is cut into phases at every problem flagged `after` (its
 //    activations are an earlier problem's output); inside a phase the
 //    problems are independent;
@@ -778,10 +780,15 @@ extern "C" sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream) {
   cfg.blockDim = dim3(kPlanThreads);
   cfg.dynamicSmemBytes = plan->smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the phase waits need it
-  attr[0].val.cooperative = 1;
-  int na = 1;
+  // The grid is the co-resident count, so every CTA becomes resident as soon
+  // as the kernels ahead of it on the device release their SMs, which they do
+  // without waiting on this plan; dependents launched early (PDL) start only
+  // after every CTA of the plan has started.  The waits between CTAs (phase
+  // counts, split tiles) therefore end; each is bounded all the same.  A
+  // cooperative launch would guarantee residency outright but measured ~1.5 us
+  // slower per launch.
+  cudaLaunchAttribute attr[1];
+  int na = 0;
   if (pdl_enabled()) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;

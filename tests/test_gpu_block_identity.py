@@ -54,3 +54,33 @@ def test_plan_rows_equal_single_row_plans(sv):
         for i, (a, r) in enumerate(zip(ys, y1)):
             np.testing.assert_array_equal(a.cpu().numpy()[m], r.cpu().numpy()[0],
                                           err_msg=f"problem {i} row {m}")
+
+
+@pytest.mark.parametrize("N,K", [(5120, 5120), (100, 640), (64, 17408), (17408, 5120)])
+@pytest.mark.parametrize("M", [2, 4, 8])
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float32])
+def test_identity_probe_reports_exact(sv, N, K, M, xdt):
+    """the start-up probe (three synthetic blocks, compared on the device)
+    finds no differing output bit"""
+    w, s, b = wl.qmv_weights(500 + N % 89, N, K)
+    wt, st, bt, _ = qmv_to_device(w, s, b, np.zeros((1, K), np.float32))
+    assert sv.qmv_identity_probe(wt, st, bt, M, xdt) == 0
+    sv.device_status()
+
+
+def test_identity_probe_counts_what_a_host_comparison_counts(sv):
+    """the probe's verdict agrees with comparing the same products on the
+    host: here both are zero for M = 5 on a ragged shape, and the probe leaves
+    the weights untouched"""
+    N, K = 1000, 1536
+    w, s, b = wl.qmv_weights(601, N, K)
+    wt, st, bt, _ = qmv_to_device(w, s, b, np.zeros((1, K), np.float32))
+    before = wt.clone()
+    assert sv.qmv_identity_probe(wt, st, bt, 5) == 0
+    assert torch.equal(wt, before)
+    x = wl.qmv_activations(601, 5, K, "bf16")
+    _, _, _, xt = qmv_to_device(w, s, b, x)
+    block = sv.qmv_smallm(wt, st, bt, xt).cpu().numpy()
+    rows = np.concatenate([sv.qmv_smallm(wt, st, bt, xt[m:m + 1].contiguous()).cpu().numpy()
+                           for m in range(5)])
+    assert int((block.view(np.uint32) != rows.view(np.uint32)).sum()) == 0
