@@ -38,6 +38,9 @@ constexpr int kMaxDim = kLanesPerRow * kChunks * 4;  // 128
 constexpr int kRowsPerCta = 16;
 constexpr int kThreads = kRowsPerCta * kLanesPerRow;  // 128
 constexpr int kMaxT = 16;
+// float4 loads per thread to stage kMaxT tokens of one kMaxDim-wide vector
+constexpr int kStage4 = kMaxT * kMaxDim / 4 / kThreads;  // 4
+static_assert(kMaxT * (kRowsPerCta / 4) <= kThreads, "one float4 of values per thread");
 
 // Tape: one block per sequence b of tape_block_floats(T,H,dk,dv) floats, each
 // block holding e [T][H][dv], then k [T][H][dk], then alpha [T][H] (padded to
@@ -89,7 +92,7 @@ __device__ __forceinline__ float row_sum(float v) {
 __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) {
   __shared__ __align__(16) float ks[kMaxT][kMaxDim];
   __shared__ __align__(16) float qs[kMaxT][kMaxDim];
-  __shared__ float vs[kMaxT][kRowsPerCta];
+  __shared__ __align__(16) float vs[kMaxT][kRowsPerCta];
   __shared__ float als[kMaxT], bes[kMaxT];
   const int tid = threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
@@ -105,34 +108,58 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
 #pragma unroll
   for (int c = 0; c < kChunks; ++c) {
     float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row_ok && chunk_col(j, c) < a.dk) f = *reinterpret_cast<const float4 *>(src + chunk_col(j, c));
+    if (row_ok && chunk_col(j, c) < a.dk)
+      f = __ldcg(reinterpret_cast<const float4 *>(src + chunk_col(j, c)));
     S[4 * c] = f.x;
     S[4 * c + 1] = f.y;
     S[4 * c + 2] = f.z;
     S[4 * c + 3] = f.w;
   }
   pdl_wait();  // the verify tokens' q, k, v and gates are the preceding kernels' outputs
-  // the tokens' keys, queries, gates and this CTA's values, once; one flat
-  // unrolled loop so that the loads of all tokens are in flight together
+  // The tokens' keys, queries, gates and this CTA's values, once.  Every load
+  // names the global space and all of them are issued before the first
+  // shared-memory store: a generic load might alias those stores and would
+  // wait behind each one, one round trip per load.
   {
-    const int nk = a.T * a.dk;
-#pragma unroll 4
-    for (int e = tid; e < nk; e += kThreads) {
-      const int t = e / a.dk, c = e - t * a.dk;
-      const size_t off = (((size_t)b * a.T + t) * a.H + h) * a.dk + c;
-      ks[t][c] = a.k[off];
-      qs[t][c] = a.q[off];
+    const int dk4 = a.dk / 4, nk4 = a.T * dk4;
+    float4 kr[kStage4], qr[kStage4];
+#pragma unroll
+    for (int u = 0; u < kStage4; ++u) {
+      const int e = tid + u * kThreads;
+      if (e < nk4) {
+        const int t = e / dk4, c4 = e - t * dk4;
+        const size_t off = (((size_t)b * a.T + t) * a.H + h) * a.dk + 4 * c4;
+        kr[u] = __ldcg(reinterpret_cast<const float4 *>(a.k + off));
+        qr[u] = __ldcg(reinterpret_cast<const float4 *>(a.q + off));
+      }
     }
-    const int nv = a.T * kRowsPerCta;
-    for (int e = tid; e < nv; e += kThreads) {
-      const int t = e / kRowsPerCta, r = e - t * kRowsPerCta;
-      const size_t bth = ((size_t)b * a.T + t) * a.H + h;
-      vs[t][r] = r0 + r < a.dv ? a.v[bth * a.dv + r0 + r] : 0.f;
-    }
+    // this CTA's 16 value rows per token: 4 float4 (dv % 4 == 0, so a float4
+    // is either wholly inside the rows or wholly past them)
+    const int t_v = tid / (kRowsPerCta / 4), r_v = 4 * (tid % (kRowsPerCta / 4));
+    const bool has_v = tid < a.T * (kRowsPerCta / 4);
+    float4 vr = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (has_v && r0 + r_v < a.dv)
+      vr = __ldcg(reinterpret_cast<const float4 *>(
+          a.v + (((size_t)b * a.T + t_v) * a.H + h) * a.dv + r0 + r_v));
+    float al_r = 0.f, be_r = 0.f;
     if (tid < a.T) {
       const size_t bth = ((size_t)b * a.T + tid) * a.H + h;
-      als[tid] = a.alpha[bth];
-      bes[tid] = a.beta[bth];
+      al_r = __ldcg(a.alpha + bth);
+      be_r = __ldcg(a.beta + bth);
+    }
+#pragma unroll
+    for (int u = 0; u < kStage4; ++u) {
+      const int e = tid + u * kThreads;
+      if (e < nk4) {
+        const int t = e / dk4, c4 = e - t * dk4;
+        *reinterpret_cast<float4 *>(&ks[t][4 * c4]) = kr[u];
+        *reinterpret_cast<float4 *>(&qs[t][4 * c4]) = qr[u];
+      }
+    }
+    if (has_v) *reinterpret_cast<float4 *>(&vs[t_v][r_v]) = vr;
+    if (tid < a.T) {
+      als[tid] = al_r;
+      bes[tid] = be_r;
     }
   }
 
@@ -201,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
 
 __global__ void __launch_bounds__(kThreads) gdn_replay_kernel(const GdnArgs a) {
   __shared__ __align__(16) float ks[kMaxT][kMaxDim];
-  __shared__ float es[kMaxT][kRowsPerCta];
+  __shared__ __align__(16) float es[kMaxT][kRowsPerCta];
   __shared__ float als[kMaxT];
   const int tid = threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
@@ -217,30 +244,48 @@ __global__ void __launch_bounds__(kThreads) gdn_replay_kernel(const GdnArgs a) {
   const int i = r0 + tid / kLanesPerRow;
   const int j = tid % kLanesPerRow;
   const bool row_ok = i < a.dv;
-  {  // the accepted records, all loads in flight together
-    const int nk = L * a.dk;
-#pragma unroll 4
-    for (int e = tid; e < nk; e += kThreads) {
-      const int t = e / a.dk, c = e - t * a.dk;
-      ks[t][c] = a.tape.k(b, t, h)[c];
-    }
-    const int ne = L * kRowsPerCta;
-    for (int e = tid; e < ne; e += kThreads) {
-      const int t = e / kRowsPerCta, r = e - t * kRowsPerCta;
-      es[t][r] = r0 + r < a.dv ? a.tape.e(b, t, h)[r0 + r] : 0.f;
-    }
-    if (tid < L) als[tid] = *a.tape.alpha(b, tid, h);
-  }
+  // The accepted records and this row's state: every load names the global
+  // space and all are issued before the first shared-memory store (a
+  // generic load might alias those stores and would wait behind each one).
   float S[kChunks * 4];
   float *dst = a.state + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk;
 #pragma unroll
   for (int c = 0; c < kChunks; ++c) {
     float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row_ok && chunk_col(j, c) < a.dk) f = *reinterpret_cast<const float4 *>(dst + chunk_col(j, c));
+    if (row_ok && chunk_col(j, c) < a.dk)
+      f = __ldcg(reinterpret_cast<const float4 *>(dst + chunk_col(j, c)));
     S[4 * c] = f.x;
     S[4 * c + 1] = f.y;
     S[4 * c + 2] = f.z;
     S[4 * c + 3] = f.w;
+  }
+  {
+    const int dk4 = a.dk / 4, nk4 = L * dk4;
+    float4 kr[kStage4];
+#pragma unroll
+    for (int u = 0; u < kStage4; ++u) {
+      const int e = tid + u * kThreads;
+      if (e < nk4) {
+        const int t = e / dk4, c4 = e - t * dk4;
+        kr[u] = __ldcg(reinterpret_cast<const float4 *>(a.tape.k(b, t, h) + 4 * c4));
+      }
+    }
+    const int t_e = tid / (kRowsPerCta / 4), r_e = 4 * (tid % (kRowsPerCta / 4));
+    const bool has_e = tid < L * (kRowsPerCta / 4);
+    float4 er = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (has_e && r0 + r_e < a.dv)
+      er = __ldcg(reinterpret_cast<const float4 *>(a.tape.e(b, t_e, h) + r0 + r_e));
+    const float al_r = tid < L ? __ldcg(a.tape.alpha(b, tid, h)) : 0.f;
+#pragma unroll
+    for (int u = 0; u < kStage4; ++u) {
+      const int e = tid + u * kThreads;
+      if (e < nk4) {
+        const int t = e / dk4, c4 = e - t * dk4;
+        *reinterpret_cast<float4 *>(&ks[t][4 * c4]) = kr[u];
+      }
+    }
+    if (has_e) *reinterpret_cast<float4 *>(&es[t_e][r_e]) = er;
+    if (tid < L) als[tid] = al_r;
   }
   __syncthreads();
   if (!row_ok) return;
