@@ -12,7 +12,7 @@
  * committed by replaying the innovation tape over the accepted prefix.
  *
  * This library provides the data-parallel steps of that cycle:
- *   qmv_smallm        the target's 4-bit small-M quantised mat-vec (M = 1..8)
+ *   qmv_smallm        the target's 4-bit small-M quantised mat-vec (M = 1..16)
  *   qmv_plan_*        an ordered list of those mat-vecs in one persistent launch
  *   spec_accept       fp32 acceptance, residual resampling and bonus token
  *   gdn_tape_capture  GatedDeltaNet recurrence over the verify tokens, with a
@@ -108,10 +108,14 @@ sv_status sv_device_status(void);
  *
  * w_packed  uint32 [N][K/8];  scales, biases: bf16 bit patterns [N][K/64];
  * x         [M][K], fp32 (SV_F32) or bf16 (SV_BF16);   y: fp32 [M][N].
- * Requires 1 <= M <= 8 (M == 0 or N == 0: no-op), K > 0, K % 64 == 0,
+ * Requires 1 <= M <= 16 (M == 0 or N == 0: no-op), K > 0, K % 64 == 0,
  * group_size == 64, bits == 4; w_packed, scales, biases and x 16-byte
  * aligned; y 4-byte aligned and not overlapping any input.  Each output is a
- * fixed-order sum (deterministic run to run).  Accuracy: fp32 accumulation
+ * fixed-order sum (deterministic run to run) whose order does not depend on
+ * M: row m of an M-row call equals the same row computed alone, bit for
+ * bit.  M = 9..16 (a DFlash-width block, "MTPLX 2.24x faster TPS", section
+ * "Layer 0: MLX Runtime") uses two 8-row MMA tiles per weight fragment and
+ * one CTA per SM.  Accuracy: fp32 accumulation
  * of exact products; fp32 x is split into two bf16 terms (|x - hi - lo| <=
  * 2^-16 |x|). */
 sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales, const uint16_t *biases,
@@ -195,7 +199,7 @@ int qmv_plan_grid(const sv_qmv_plan *plan);
  * this projection at width M is exact.  Keeping the verdict per (weights, M)
  * is the caller's part.
  *
- * Requires 1 <= M <= 8, N >= 1, K >= 64, K % 64 == 0; w_packed, scales and
+ * Requires 1 <= M <= 16, N >= 1, K >= 64, K % 64 == 0; w_packed, scales and
  * biases as qmv_smallm requires.  scratch: caller-owned device memory,
  * 256-byte aligned, at least qmv_identity_probe_bytes(M, N, K, x_dtype)
  * bytes (0 on invalid input), not overlapping the weights; its contents are

@@ -6,7 +6,7 @@ tensors (device, dtype, shape, contiguity) and calls the C function on the
 current CUDA stream.  All arithmetic runs in the library's CUDA kernels; if
 the library is missing, every call raises -- there is no fallback.
 
-  qmv_smallm        4-bit affine group-64 mat-vec over M = 1..8 verify rows
+  qmv_smallm        4-bit affine group-64 mat-vec over M = 1..16 verify rows
   spec_accept       fp32 probability-ratio acceptance, residual, bonus token
   gdn_tape_capture  GatedDeltaNet recurrence + innovation tape
   gdn_tape_replay   rebuild the recurrent state over an accepted prefix

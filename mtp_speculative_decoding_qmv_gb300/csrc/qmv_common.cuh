@@ -207,6 +207,72 @@ __device__ __forceinline__ void group_math(float (&acc)[kTiles][4], uint32_t wba
   }
 }
 
+// Sixteen activation rows (M = 9..16): the same per-group math with two
+// 8-column MMA n-tiles, rows 0-7 and 8-15.  Each widened weight fragment
+// feeds both n-tiles, so the unpack is paid once per weight whatever M is.
+template <bool kXF32>
+__device__ __forceinline__ void group_math_x2(float (&acc)[2][kTiles][4], uint32_t wbase,
+                                              const XRaw<kXF32> (&xcur)[2], uint32_t sb,
+                                              uint32_t sb_rt, uint32_t sb_r8, uint32_t sb_b) {
+  uint32_t hi[2][8], lo[2][8];
+  b_fragments<kXF32>(xcur[0], hi[0], lo[0]);
+  b_fragments<kXF32>(xcur[1], hi[1], lo[1]);
+  uint32_t w[kTiles][4];
+#pragma unroll
+  for (int rt = 0; rt < kTiles; ++rt) ldmatrix_x4(w[rt], wbase + rt * 16 * 128);
+  float xs[2][4];  // sum of x over the group per n-tile, columns 2t, 2t+1
+  float d[2][kTiles][4];
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    const int wi = (ks >> 1) * 2;
+    const int sh = (ks & 1) * 8;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      if (ks == 0)
+        mma_bf16_zero(xs[nt], kBf16One2, kBf16One2, kBf16One2, kBf16One2, hi[nt][2 * ks],
+                      hi[nt][2 * ks + 1]);
+      else
+        mma_bf16_m16n8k16(xs[nt], kBf16One2, kBf16One2, kBf16One2, kBf16One2, hi[nt][2 * ks],
+                          hi[nt][2 * ks + 1]);
+      if constexpr (kXF32)
+        mma_bf16_m16n8k16(xs[nt], kBf16One2, kBf16One2, kBf16One2, kBf16One2, lo[nt][2 * ks],
+                          lo[nt][2 * ks + 1]);
+    }
+#pragma unroll
+    for (int rt = 0; rt < kTiles; ++rt) {
+      const uint32_t wr = w[rt][wi] >> sh, wr8 = w[rt][wi + 1] >> sh;
+      const uint32_t p0 = and_or(wr, kNibbleMask, kBf16Base);
+      const uint32_t p0r8 = and_or(wr8, kNibbleMask, kBf16Base);
+      const uint32_t p1 = and_or(wr >> 4, kNibbleMask, kBf16Base);
+      const uint32_t p1r8 = and_or(wr8 >> 4, kNibbleMask, kBf16Base);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        if (ks == 0)
+          mma_bf16_zero(d[nt][rt], p0, p0r8, p1, p1r8, hi[nt][2 * ks], hi[nt][2 * ks + 1]);
+        else
+          mma_bf16_m16n8k16(d[nt][rt], p0, p0r8, p1, p1r8, hi[nt][2 * ks], hi[nt][2 * ks + 1]);
+        if constexpr (kXF32)
+          mma_bf16_m16n8k16(d[nt][rt], p0, p0r8, p1, p1r8, lo[nt][2 * ks], lo[nt][2 * ks + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int rt = 0; rt < kTiles; ++rt) {
+    const uint32_t p = sb + rt * sb_rt;
+    const float s0 = bf16_bits_to_float(lds_u16(p));
+    const float s1 = bf16_bits_to_float(lds_u16(p + sb_r8));
+    const float c0 = fmaf(-128.f, s0, bf16_bits_to_float(lds_u16(p + sb_b)));
+    const float c1 = fmaf(-128.f, s1, bf16_bits_to_float(lds_u16(p + sb_b + sb_r8)));
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      acc[nt][rt][0] = fmaf(s0, d[nt][rt][0], fmaf(c0, xs[nt][0], acc[nt][rt][0]));
+      acc[nt][rt][1] = fmaf(s0, d[nt][rt][1], fmaf(c0, xs[nt][1], acc[nt][rt][1]));
+      acc[nt][rt][2] = fmaf(s1, d[nt][rt][2], fmaf(c1, xs[nt][0], acc[nt][rt][2]));
+      acc[nt][rt][3] = fmaf(s1, d[nt][rt][3], fmaf(c1, xs[nt][1], acc[nt][rt][3]));
+    }
+  }
+}
+
 // ldmatrix.x4 address offset of `lane` of the warp reducing group gl of a
 // stage: lane L reads row ((L >> 3) & 1) * 8 + (L & 7) of an MMA tile, 16-byte
 // chunk 2 * (gl % 4) + (L >> 4) of the 128-byte box row, at its swizzled

@@ -82,7 +82,8 @@ ProbeLayout probe_layout(int M, int N, int K, sv_dtype x_dtype) {
 }
 
 sv_status probe_validate(int M, int N, int K, sv_dtype x_dtype) {
-  if (M < 1 || M > 8) return fail(SV_ERR_UNSUPPORTED, "qmv_identity_probe: M=%d outside [1, 8]", M);
+  if (M < 1 || M > 16)
+    return fail(SV_ERR_UNSUPPORTED, "qmv_identity_probe: M=%d outside [1, 16]", M);
   if (N < 1 || K < 64 || K % 64 != 0)
     return fail(SV_ERR_INVALID_ARG,
                 "qmv_identity_probe: need N >= 1, K >= 64, K %% 64 == 0 (N=%d K=%d)", N, K);

@@ -1,4 +1,4 @@
-// qmv_smallm.cu -- small-M (1..8 rows) 4-bit affine group-64 quantised mat-vec
+// qmv_smallm.cu -- small-M (1..16 rows) 4-bit affine group-64 quantised mat-vec
 // for the target model's verify forward, sm_103a.
 //
 // Source: "MTPLX 2.24x faster TPS", section "Layer 0: MLX Runtime" (the verify
@@ -57,7 +57,11 @@ namespace {
 using namespace qmv;
 
 constexpr int kMaxSplits = 8;                      // portable cluster size
-constexpr int kMinCtasPerSm = 2;                   // register budget: 113 per thread
+// CTAs per SM the register budget is set for: 2 (113 registers a thread) for
+// up to 8 activation rows; 1 for 9..16 rows, whose accumulators are twice as
+// many
+template <int kNT>
+constexpr int kMinCtasPerSm = kNT == 1 ? 2 : 1;
 __device__ unsigned int g_qmv_device_error;
 
 struct QmvArgs {
@@ -81,12 +85,14 @@ __host__ __device__ inline uint32_t round_up_u32(uint32_t v, uint32_t a) {
 
 // [stages] then, if not streamed, the tile's scale/bias block, then the
 // mbarriers.  The end-of-kernel reductions reuse the drained ring (at least
-// kRedBytes long).  `total` includes 1 KB of alignment slack.
-__host__ __device__ inline Layout qmv_layout(int groups, int stages, bool sb_stream) {
+// kRedBytes long per 8 activation rows).  `total` includes 1 KB of
+// alignment slack.
+__host__ __device__ inline Layout qmv_layout(int groups, int stages, bool sb_stream, int nt) {
   Layout L;
   L.stage = sb_stream ? kStageBytesStream : kStageBytesBlock;
   const uint32_t ring = (uint32_t)stages * L.stage;
-  L.sb = (ring > kRedBytes ? ring : kRedBytes);
+  const uint32_t red = kRedBytes * (uint32_t)nt;
+  L.sb = (ring > red ? ring : red);
   const uint32_t after = L.sb + (sb_stream ? 0u : round_up_u32(2u * kRows * groups * 2u, 16));
   L.bar = round_up_u32(after, 16);
   L.total = L.bar + (uint32_t)(2 * stages + 1) * 8u + 1024u;
@@ -135,8 +141,10 @@ __device__ __forceinline__ void issue_stage(const QmvArgs &a, const CUtensorMap 
 // kStream: K % 512 == 0, scales and biases stream with the stages and every
 // group of every stage is real; otherwise the tile's whole scale block is
 // loaded once and groups past K/64 are skipped.
-template <bool kXF32, bool kStream>
-__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
+//
+// kNT: 8-row MMA n-tiles of activation rows (1: M <= 8, 2: M <= 16).
+template <bool kXF32, bool kStream, int kNT>
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm<kNT>)
     qmv_smallm_kernel(const __grid_constant__ CUtensorMap wmap,
                       const __grid_constant__ CUtensorMap smap,
                       const __grid_constant__ CUtensorMap bmap, const QmvArgs a) {
@@ -155,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   const int c_begin = (int)((long long)split * n_chunks / splits);
   const int c_end = (int)((long long)(split + 1) * n_chunks / splits);
   const int stages = a.stages;
-  const Layout L = qmv_layout(groups, stages, kStream);
+  const Layout L = qmv_layout(groups, stages, kStream, kNT);
+  constexpr int kCols = 8 * kNT;          // activation rows a CTA's sums cover
+  constexpr int kParts = 2 * kNT;         // output elements per consumer thread
   const uint32_t full0 = base + L.bar;          // full[i]  = full0 + 8 i
   const uint32_t empty0 = full0 + 8u * stages;  // empty[i] = empty0 + 8 i
   const uint32_t sb_bar = empty0 + 8u * stages;
@@ -172,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   __syncthreads();
   pdl_launch_dependents();
 
-  float part[2] = {0.f, 0.f};  // this thread's two sums of the tile (consumers)
+  float part[kParts] = {};  // this thread's sums of the tile (consumers)
   bool ok = true;
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
@@ -229,36 +239,55 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     // scale / bias of rows g8 and g8+8 of tile 0, group gl (streamed layout)
     const uint32_t sb_off = kSbOff + (uint32_t)(g8 * 16 + gl * 2);
     const uint32_t blk = base + L.sb;  // whole-tile block (not streamed)
-    // lanes of padding columns (m >= M) read row 0; their sums are never stored
-    const void *xrow = static_cast<const uint8_t *>(a.x) +
-                       (size_t)(g8 < a.M ? g8 : 0) * a.K * (kXF32 ? 4 : 2);
-    float acc[kTiles][4];
+    // lanes of padding columns (m >= M) read row 0; their sums are never
+    // stored.  n-tile nt covers activation rows 8 nt .. 8 nt + 7.
+    const void *xrow[kNT];
 #pragma unroll
-    for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int nt = 0; nt < kNT; ++nt)
+      xrow[nt] = static_cast<const uint8_t *>(a.x) +
+                 (size_t)(8 * nt + g8 < a.M ? 8 * nt + g8 : 0) * a.K * (kXF32 ? 4 : 2);
+    float acc[kNT][kTiles][4];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int i = 0; i < kTiles; ++i)
+        acc[nt][i][0] = acc[nt][i][1] = acc[nt][i][2] = acc[nt][i][3] = 0.f;
     // every lane waits (each needs the acquire); the outcome is made warp-uniform
     ok = __all_sync(0xffffffffu, mbar_wait_u32(sb_bar, 0));
     pdl_wait();  // x and y belong to the preceding kernel until here
     int g = c_begin * kConsumerWarps + gl;
     // groups past K/64 (last stage of a ragged K) read a real group's
     // activations; their weights are skipped
-    XRaw<kXF32> xnext = load_x<kXF32>(xrow, true, kStream ? g : min(g, groups - 1), t);
+    XRaw<kXF32> xnext[kNT];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+      xnext[nt] = load_x<kXF32>(xrow[nt], true, kStream ? g : min(g, groups - 1), t);
     int st = 0, ph = 0;  // stage of chunk c and the parity of its fill
     for (int c = c_begin; ok && c < c_end; ++c, g += kConsumerWarps) {
-      const XRaw<kXF32> xcur = xnext;
+      XRaw<kXF32> xcur[kNT];
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) xcur[nt] = xnext[nt];
       // next stage's activations: the loads fly during this stage's work
       const int gn = min(g + kConsumerWarps, groups - 1);
-      xnext = load_x<kXF32>(xrow, true, gn, t);
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) xnext[nt] = load_x<kXF32>(xrow[nt], true, gn, t);
       if (!warp_wait_stage(full0 + 8u * st, ph)) {
         ok = false;
         break;
       }
       const uint32_t stage = base + st * L.stage;
-      if constexpr (kStream) {  // [64][8] scales then [64][8] biases of this stage
-        group_math<kXF32>(acc, stage + ldm_off, xcur, stage + sb_off, 16 * 16, 8 * 16, kRows * 16);
-      } else if (g < groups) {  // the tile's whole [64][groups] block
-        const uint32_t gb = (uint32_t)groups * 2;
-        group_math<kXF32>(acc, stage + ldm_off, xcur, blk + (uint32_t)(g8 * groups + g) * 2,
-                          16 * gb, 8 * gb, kRows * gb);
+      // scales/biases: [64][8] scales then [64][8] biases of this stage when
+      // streamed, else the tile's whole [64][groups] block
+      const uint32_t gb = (uint32_t)groups * 2;
+      const bool real = kStream || g < groups;
+      const uint32_t sbp = kStream ? stage + sb_off : blk + (uint32_t)(g8 * groups + g) * 2;
+      const uint32_t srt = kStream ? 16 * 16 : 16 * gb, sr8 = kStream ? 8 * 16 : 8 * gb;
+      const uint32_t sbb = kStream ? kRows * 16 : kRows * gb;
+      if (real) {
+        if constexpr (kNT == 1)
+          group_math<kXF32>(acc[0], stage + ldm_off, xcur[0], sbp, srt, sr8, sbb);
+        else
+          group_math_x2<kXF32>(acc, stage + ldm_off, xcur, sbp, srt, sr8, sbb);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
@@ -273,28 +302,31 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     float *red = reinterpret_cast<float *>(smem);
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
 #pragma unroll
-    for (int rt = 0; rt < kTiles; ++rt) {
-      float *p = red + ((size_t)warp * kRows + rt * 16) * 8;
-      p[g8 * 8 + 2 * t] = acc[rt][0];
-      p[g8 * 8 + 2 * t + 1] = acc[rt][1];
-      p[(g8 + 8) * 8 + 2 * t] = acc[rt][2];
-      p[(g8 + 8) * 8 + 2 * t + 1] = acc[rt][3];
+    for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+      for (int rt = 0; rt < kTiles; ++rt) {
+        float *p = red + ((size_t)warp * kRows + rt * 16) * kCols + 8 * nt;
+        p[g8 * kCols + 2 * t] = acc[nt][rt][0];
+        p[g8 * kCols + 2 * t + 1] = acc[nt][rt][1];
+        p[(g8 + 8) * kCols + 2 * t] = acc[nt][rt][2];
+        p[(g8 + 8) * kCols + 2 * t + 1] = acc[nt][rt][3];
+      }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-    // element e = col * 64 + row; thread handles e = tid and tid + 256
+    // element e = col * 64 + row; thread handles e = tid + 256 h
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kParts; ++h) {
       const int e = threadIdx.x + h * kConsumerWarps * 32;
       const int col = e / kRows, row = e % kRows;
       float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v += red[((size_t)w * kRows + row) * 8 + col];
+      for (int w = 0; w < kConsumerWarps; ++w) v += red[((size_t)w * kRows + row) * kCols + col];
       part[h] = v;
     }
     if (splits == 1) {
       if (!ok) return;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kParts; ++h) {
         const int e = threadIdx.x + h * kConsumerWarps * 32;
         const int col = e / kRows, row = e % kRows;  // row fastest: coalesced stores
         if (col < a.M && row < rows) a.y[(size_t)col * a.N + n0 + row] = part[h];
@@ -308,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   cluster_sync_all();  // all rings drained: the first CTA's ring may be overwritten
   const uint32_t rank = cluster_rank();
   if (warp < kConsumerWarps) {
-    const uint32_t slot = map_shared_to_rank(base, 0) + rank * (kRows * 8 * 4);
+    const uint32_t slot = map_shared_to_rank(base, 0) + rank * (kRows * kCols * 4);
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < kParts; ++h)
       st_cluster_f32(slot + 4u * (threadIdx.x + h * kConsumerWarps * 32), part[h]);
   }
   cluster_sync_all();  // every partial has landed
@@ -318,23 +350,23 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   if (__any_sync(0xffffffffu, !ok)) return;
   const float *slots = reinterpret_cast<const float *>(smem);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < kParts; ++h) {
     const int e = threadIdx.x + h * kConsumerWarps * 32;
     const int col = e / kRows, row = e % kRows;
     float v = 0.f;
-    for (int r = 0; r < splits; ++r) v += slots[r * kRows * 8 + e];
+    for (int r = 0; r < splits; ++r) v += slots[r * kRows * kCols + e];
     if (col < a.M && row < rows) a.y[(size_t)col * a.N + n0 + row] = v;
   }
 }
 
 // Co-resident CTAs per SM allowed by registers and threads (cached per device).
-template <bool kXF32, bool kStream>
+template <bool kXF32, bool kStream, int kNT>
 int occupancy_without_smem(int dev) {
   static int cached[64] = {};
   if (dev < 0 || dev >= 64) return 1;
   if (cached[dev] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmv_smallm_kernel<kXF32, kStream>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmv_smallm_kernel<kXF32, kStream, kNT>,
                                                       kThreads, 0) != cudaSuccess || n < 1)
       n = 1;
     cached[dev] = n;
@@ -342,11 +374,11 @@ int occupancy_without_smem(int dev) {
   return cached[dev];
 }
 
-template <bool kXF32, bool kStream>
+template <bool kXF32, bool kStream, int kNT>
 sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   static bool configured[64] = {};
   const int dev = current_device();
-  auto kern = qmv_smallm_kernel<kXF32, kStream>;
+  auto kern = qmv_smallm_kernel<kXF32, kStream, kNT>;
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
@@ -359,12 +391,17 @@ sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   const int tiles = (args.N + kRows - 1) / kRows;
   const int n_chunks = (args.K + kStageInputs - 1) / kStageInputs;
   const int sms = device_sm_count();
-  const int occ = occupancy_without_smem<kXF32, kStream>(dev);
+  const int occ = occupancy_without_smem<kXF32, kStream, kNT>(dev);
   // split K over a cluster when the row tiles alone would leave CTA slots
-  // idle, as far as the grid still fits in one wave of resident CTAs
+  // idle, as far as the grid still fits in one wave of resident CTAs.  The
+  // split decides the fp32 summation order, so it is chosen from the
+  // occupancy of the <= 8-row kernel for every M: a row of a 9..16-row call
+  // then equals the same row computed alone, bit for bit (at one CTA per SM
+  // such a grid may take two waves).
+  const int occ_split = occupancy_without_smem<kXF32, kStream, 1>(dev);
   int splits = 1;
   if (kStream) {
-    const int fit = (occ * sms) / tiles;
+    const int fit = (occ_split * sms) / tiles;
     splits = std::max(1, std::min({fit, kMaxSplits, n_chunks}));
   }
   args.splits = splits;
@@ -379,9 +416,9 @@ sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   const int per_cta_chunks = (n_chunks + splits - 1) / splits;
   const int max_stages = std::min(32, std::max(2, per_cta_chunks));
   int stages = 2;
-  while (stages < max_stages && qmv_layout(groups, stages + 1, sbs).total <= budget) ++stages;
-  Layout L = qmv_layout(groups, stages, sbs);
-  while (L.total > (uint32_t)optin && stages > 2) L = qmv_layout(groups, --stages, sbs);
+  while (stages < max_stages && qmv_layout(groups, stages + 1, sbs, kNT).total <= budget) ++stages;
+  Layout L = qmv_layout(groups, stages, sbs, kNT);
+  while (L.total > (uint32_t)optin && stages > 2) L = qmv_layout(groups, --stages, sbs, kNT);
   if (L.total > (uint32_t)optin)
     return fail(SV_ERR_UNSUPPORTED, "qmv_smallm: K=%d needs %u bytes of shared memory",
                 args.K, L.total);
@@ -456,7 +493,7 @@ extern "C" sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales
     return fail(SV_ERR_UNSUPPORTED, "qmv_smallm: only bits=4, group_size=64 (got %d, %d)", bits,
                 group_size);
   if (K % 64 != 0) return fail(SV_ERR_INVALID_ARG, "qmv_smallm: K=%d is not a multiple of 64", K);
-  if (M > 8) return fail(SV_ERR_UNSUPPORTED, "qmv_smallm: M=%d > 8", M);
+  if (M > 16) return fail(SV_ERR_UNSUPPORTED, "qmv_smallm: M=%d > 16", M);
   if (x_dtype != SV_F32 && x_dtype != SV_BF16)
     return fail(SV_ERR_INVALID_ARG, "qmv_smallm: unknown x_dtype %d", (int)x_dtype);
   if (M == 0 || N == 0) return SV_OK;
@@ -477,9 +514,13 @@ extern "C" sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales
   // scale/bias rows are 16-byte aligned for the copy engine when K % 512 == 0
   QmvArgs args{scales, biases, x, y, M, N, K, 0, 1, K % 512 == 0 ? 1 : 0};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf = x_dtype == SV_BF16;
+  if (M <= 8) {
+    if (args.sb_stream)
+      return bf ? launch<false, true, 1>(w_packed, args, s) : launch<true, true, 1>(w_packed, args, s);
+    return bf ? launch<false, false, 1>(w_packed, args, s) : launch<true, false, 1>(w_packed, args, s);
+  }
   if (args.sb_stream)
-    return x_dtype == SV_BF16 ? launch<false, true>(w_packed, args, s)
-                              : launch<true, true>(w_packed, args, s);
-  return x_dtype == SV_BF16 ? launch<false, false>(w_packed, args, s)
-                            : launch<true, false>(w_packed, args, s);
+    return bf ? launch<false, true, 2>(w_packed, args, s) : launch<true, true, 2>(w_packed, args, s);
+  return bf ? launch<false, false, 2>(w_packed, args, s) : launch<true, false, 2>(w_packed, args, s);
 }

@@ -173,13 +173,13 @@ def test_identity_probe_sizes_and_rejects(L):
     # x: 3 blocks of 4 x 512 bf16, y block and y rows 4 x 512 fp32, a counter
     assert L.qmv_identity_probe_bytes(4, 512, 512, 1) == 12288 + 8192 + 8192 + 256
     assert L.qmv_identity_probe_bytes(4, 512, 512, 0) == 24576 + 8192 + 8192 + 256
-    assert L.qmv_identity_probe_bytes(9, 512, 512, 1) == 0
+    assert L.qmv_identity_probe_bytes(17, 512, 512, 1) == 0
     assert L.qmv_identity_probe_bytes(4, 512, 100, 1) == 0
     w, s, b, scr = A, A + 0x1000000, A + 0x2000000, A + 0x3000000
     n = L.qmv_identity_probe_bytes(4, 512, 512, 1)
     out = ctypes.c_int(7)
     assert L.qmv_identity_probe(w, s, b, 1, 0, 512, 512, scr, n, ctypes.byref(out), None) == 2
-    assert L.qmv_identity_probe(w, s, b, 1, 9, 512, 512, scr, n, ctypes.byref(out), None) == 2
+    assert L.qmv_identity_probe(w, s, b, 1, 17, 512, 512, scr, n, ctypes.byref(out), None) == 2
     assert L.qmv_identity_probe(w, s, b, 1, 4, 512, 96, scr, n, ctypes.byref(out), None) == 1
     assert L.qmv_identity_probe(w, s, b, 7, 4, 512, 512, scr, n, ctypes.byref(out), None) == 1
     assert L.qmv_identity_probe(None, s, b, 1, 4, 512, 512, scr, n, ctypes.byref(out), None) == 1

@@ -111,6 +111,46 @@ def test_empty_and_invalid(sv):
     wt, st, bt, _ = qmv_to_device(w, s, b, wl.qmv_activations(600, 1, 64, "bf16"))
     x0 = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda:0")
     assert sv.qmv_smallm(wt, st, bt, x0).shape == (0, 32)
-    x9 = torch.zeros((9, 64), dtype=torch.bfloat16, device="cuda:0")
+    x17 = torch.zeros((17, 64), dtype=torch.bfloat16, device="cuda:0")
     with pytest.raises(sv.SvError):
-        sv.qmv_smallm(wt, st, bt, x9)
+        sv.qmv_smallm(wt, st, bt, x17)
+
+
+# ---- 9..16 rows (a DFlash-width verify block): two 8-row MMA n-tiles ------
+
+@pytest.mark.parametrize("M", [9, 10, 12, 15, 16])
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_wide_m_ragged_tiles(sv, oracle, M, xdt):
+    N, K = 100, 640  # ragged row tile, K not a multiple of 512 (scale block path)
+    w, s, b = wl.qmv_weights(700 + M, N, K)
+    x = wl.qmv_activations(700 + M, M, K, xdt)
+    assert_qmv_close(_run(sv, w, s, b, x), oracle.qmv(w, s, b, x))
+
+
+@pytest.mark.parametrize("N,K", [(1, 64), (33, 576), (130, 2048), (7, 1536)])
+def test_wide_m_edge_shapes(sv, oracle, N, K):
+    w, s, b = wl.qmv_weights(800 + N, N, K)
+    x = wl.qmv_activations(800 + N, 16, K, "bf16")
+    assert_qmv_close(_run(sv, w, s, b, x), oracle.qmv(w, s, b, x))
+
+
+@pytest.mark.parametrize("N,K,M", [(5120, 5120, 16), (17408, 5120, 12), (5120, 17408, 16)])
+def test_wide_m_full_shapes(sv, oracle, N, K, M):
+    """split-K clusters (5120 rows: 80 tiles) and many tiles (17408 rows)"""
+    _sampled(sv, oracle, N, K, M, 900 + M)
+
+
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_wide_m_rows_equal_single_rows(sv, xdt):
+    """row m of a 16-row product is bitwise the product of row m alone (the
+    block-vs-sequential identity holds across the two n-tiles too)"""
+    N, K = 5120, 5120
+    w, s, b = wl.qmv_weights(950, N, K)
+    x = wl.qmv_activations(950, 16, K, xdt)
+    wt, st, bt, xt = qmv_to_device(w, s, b, x)
+    block = sv.qmv_smallm(wt, st, bt, xt)
+    rows = [sv.qmv_smallm(wt, st, bt, xt[m:m + 1].contiguous()) for m in (0, 7, 8, 9, 15)]
+    torch.cuda.synchronize()
+    block = block.cpu().numpy()
+    for m, r in zip((0, 7, 8, 9, 15), rows):
+        np.testing.assert_array_equal(block[m], r.cpu().numpy()[0], err_msg=f"row {m}")
