@@ -312,9 +312,9 @@ sv_status spec_accept_noalloc(const float *target_logits, const float *draft_log
  * so the tapes of consecutive batches, stacked, form the tape of the
  * concatenated batch (one replay launch can commit several layers).
  * Replaying records t = 0..L-1 applies S[i][j] <- alpha_t*S[i][j] + e_t[i]*k_t[j]
- * (multiply, multiply, add: the same roundings as the capture), so the state
- * after replaying L records equals, bit for bit, the capture's state after
- * its first L tokens.
+ * (a rounded multiply, then one fused multiply-add: the same roundings as the
+ * capture), so the state after replaying L records equals, bit for bit, the
+ * capture's state after its first L tokens.
  * Shapes: state [B][H][dv][dk]; q, k [B][T][H][dk]; v [B][T][H][dv];
  * alpha, beta [B][T][H]; out [B][T][H][dv].
  * Requires B >= 0 (0: no-op), 1 <= T <= 16, H >= 1, dk and dv in [4, 128]

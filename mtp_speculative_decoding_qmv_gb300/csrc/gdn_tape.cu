@@ -19,9 +19,10 @@
 // is a run of 128 contiguous bytes per row and a warp covers four rows; the
 // row's dot products are finished with three shuffles.  Small batches still
 // give (dv / 16) x H CTAs (384 at H = 48, dv = 128).  The state element
-// update is written as separate round-to-nearest multiply, multiply, add (no
-// contraction) in both kernels, so replaying the tape reproduces the
-// capture's states bit for bit.
+// update is written as the same explicit roundings in both kernels -- a
+// round-to-nearest multiply by the gate, then one fused multiply-add of the
+// rank-1 term -- so replaying the tape reproduces the capture's states bit
+// for bit.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -195,10 +196,10 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
       if (chunk_col(j, c) < a.dk) {
         const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
         const float4 qq = *reinterpret_cast<const float4 *>(&qs[t][chunk_col(j, c)]);
-        S[4 * c] = __fadd_rn(S[4 * c], __fmul_rn(e, kk.x));
-        S[4 * c + 1] = __fadd_rn(S[4 * c + 1], __fmul_rn(e, kk.y));
-        S[4 * c + 2] = __fadd_rn(S[4 * c + 2], __fmul_rn(e, kk.z));
-        S[4 * c + 3] = __fadd_rn(S[4 * c + 3], __fmul_rn(e, kk.w));
+        S[4 * c] = __fmaf_rn(e, kk.x, S[4 * c]);
+        S[4 * c + 1] = __fmaf_rn(e, kk.y, S[4 * c + 1]);
+        S[4 * c + 2] = __fmaf_rn(e, kk.z, S[4 * c + 2]);
+        S[4 * c + 3] = __fmaf_rn(e, kk.w, S[4 * c + 3]);
         oc[c] = fmaf(S[4 * c], qq.x, oc[c]);
         oc[c] = fmaf(S[4 * c + 1], qq.y, oc[c]);
         oc[c] = fmaf(S[4 * c + 2], qq.z, oc[c]);
@@ -295,10 +296,10 @@ __global__ void __launch_bounds__(kThreads) gdn_replay_kernel(const GdnArgs a) {
     for (int c = 0; c < kChunks; ++c) {
       if (chunk_col(j, c) < a.dk) {
         const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
-        S[4 * c] = __fadd_rn(__fmul_rn(al, S[4 * c]), __fmul_rn(et, kk.x));
-        S[4 * c + 1] = __fadd_rn(__fmul_rn(al, S[4 * c + 1]), __fmul_rn(et, kk.y));
-        S[4 * c + 2] = __fadd_rn(__fmul_rn(al, S[4 * c + 2]), __fmul_rn(et, kk.z));
-        S[4 * c + 3] = __fadd_rn(__fmul_rn(al, S[4 * c + 3]), __fmul_rn(et, kk.w));
+        S[4 * c] = __fmaf_rn(et, kk.x, __fmul_rn(al, S[4 * c]));
+        S[4 * c + 1] = __fmaf_rn(et, kk.y, __fmul_rn(al, S[4 * c + 1]));
+        S[4 * c + 2] = __fmaf_rn(et, kk.z, __fmul_rn(al, S[4 * c + 2]));
+        S[4 * c + 3] = __fmaf_rn(et, kk.w, __fmul_rn(al, S[4 * c + 3]));
       }
     }
   }
