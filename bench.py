@@ -148,7 +148,7 @@ class Cycle:
 
     def __init__(self, sv, torch, device, depth: int = 3, layers: int = wl.N_LAYERS,
                  heads: int = wl.GDN_HEADS, dim: int = wl.GDN_DIM, seed: int = 0,
-                 layout: str = "plans"):
+                 layout: str = "plans", weights_from=None):
         self.sv, self.torch, self.dev = sv, torch, device
         self.layout = layout
         self.K = depth
@@ -160,10 +160,14 @@ class Cycle:
         g.manual_seed(wl.MASTER_SEED + 17 + seed)
         self.g = g
         self.proj = []  # (w, s, b, x, y)
-        for _ in range(layers):
-            for _, N, Kin in wl.LAYER_PROJECTIONS:
-                self.proj.append(self._qmv_buffers(N, Kin))
-        self.lm = self._qmv_buffers(self.V, wl.HIDDEN)
+        if weights_from is None:
+            for _ in range(layers):
+                for _, N, Kin in wl.LAYER_PROJECTIONS:
+                    self.proj.append(self._qmv_buffers(N, Kin))
+            self.lm = self._qmv_buffers(self.V, wl.HIDDEN)
+        else:  # the same weights at another depth: new activation rows only
+            self.proj = [self._rows_for(c) for c in weights_from.proj]
+            self.lm = self._rows_for(weights_from.lm)
         self.qmv_calls = self.proj + [self.lm]
         self.qmv_bytes = sum(qmv_bytes(self.M, w.shape[0], w.shape[1] * 8)
                              for (w, _, _, _, _) in self.qmv_calls)
@@ -241,6 +245,13 @@ class Cycle:
         x = t.randn((self.M, Kin), generator=g, device=d).to(t.bfloat16)
         y = t.empty((self.M, N), device=d, dtype=t.float32)
         return (w, s, b, x, y)
+
+    def _rows_for(self, c):
+        t = self.torch
+        w, s, b = c[:3]
+        Kin = w.shape[1] * 8
+        x = t.randn((self.M, Kin), generator=self.g, device=self.dev).to(t.bfloat16)
+        return (w, s, b, x, t.empty((self.M, w.shape[0]), device=self.dev, dtype=t.float32))
 
     def prepare_drafts(self, noise: float = 0.5, logit_std: float = 3.0):
         """Once, outside timing: the LM-head input is scaled so that the target
@@ -593,6 +604,23 @@ def run_cycle(args):
     t_e2e = max_over_ranks(torch, t_e2e, world, device)
     sv.device_status()
 
+    # the same cycle at the configuration's other draft depths (same weights,
+    # M = K + 1 rows), each its own graph, timed the same way
+    depths = {str(args.depth): value}
+    if not args.no_depth_sweep:
+        for k in (2, 3, 4, 5):
+            if k == args.depth:
+                continue
+            other = Cycle(sv, torch, device, depth=k, seed=rank, layout=args.layout,
+                          weights_from=cyc)
+            other.prepare_drafts()
+            og = capture(torch, other.run, stream)
+            oms = time_graph(torch, og, stream, args.steps, args.warmup, barrier)
+            oms = max_over_ranks(torch, oms / 1e3, world, device) * 1e3
+            depths[str(k)] = job_rate(args.steps, world, oms / 1e3)
+            del og, other
+        sv.device_status()
+
     if rank != 0:
         return 0
     cycle_bytes = cyc.qmv_bytes + cyc.gdn_bytes
@@ -647,6 +675,7 @@ def run_cycle(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": cyc.launches_per_step * args.steps,
         "clocks": clocks,
+        "cycles_per_s_by_depth": {k: depths[k] for k in sorted(depths)},
         "acceptance": {"mean_accepted": statistics.mean(accepted) if accepted else None,
                        "depth": args.depth, "draws": min(len(accepted), E_DRAWS),
                        "how": "accepted drafts per cycle over the e2e steps (warm-up "
@@ -1019,6 +1048,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--depth", type=int, default=3, help="draft depth K (M = K+1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-depth-sweep", action="store_true",
+                    help="cycle: skip the draft depths K = 2..5 other than --depth")
     ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn", "qmv", "stream",
                                            "conv"],
                     default="cycle")
