@@ -109,6 +109,11 @@ def uniforms(stream: int, shape) -> np.ndarray:
     return rng(5, stream).random(shape, dtype=np.float32)
 
 
+def noise(stream: int, shape, std: float) -> np.ndarray:
+    """float32 draws of N(0, std) (e.g. draft logits = target logits + noise)."""
+    return (rng(8, stream).standard_normal(shape, dtype=np.float32) * np.float32(std))
+
+
 # ----------------------------------------------------------------------------
 # GatedDeltaNet tape
 # ----------------------------------------------------------------------------
