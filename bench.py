@@ -212,21 +212,23 @@ class Cycle:
         self.plans = []
         if layout in ("plans", "allplans"):
             self._make_plans()
-        self.qmv_launches = (len(self.plans) + (2 * layers if layout == "plans" else 0)
+        self.qmv_launches = (len(self.plans) + (layers if layout == "plans" else 0)
                              if self.plans else len(self.qmv_calls))
         self.launches_per_step = self.qmv_launches + layers + 2
 
     def _make_plans(self):
         """Per layer: one plan for q, k, v and one for gate, up (projections
-        that read the same input); o and down as single launches ("plans") or
-        as one-problem plans ("allplans"); the LM head as a plan.  Between them
-        sit the dependency points of a decoder layer (the GatedDeltaNet
-        capture, then o, then down), so each is its own launch, overlapped
-        with its predecessor by programmatic dependent launch."""
+        that read the same input), down as a one-problem plan and o as a
+        qmv_smallm launch ("plans"; o follows the GatedDeltaNet capture, whose
+        small CTAs leave room for qmv_smallm's to start early), or o as a plan
+        too ("allplans"); the LM head as a plan.  Between them sit the
+        dependency points of a decoder layer (the GatedDeltaNet capture, then
+        o, then down), so each is its own launch, overlapped with its
+        predecessor by programmatic dependent launch."""
         QmvPlan = self.sv.QmvPlan
         names = [n for n, _, _ in wl.LAYER_PROJECTIONS]
         n = len(names)
-        groups = ((("q", "k", "v"), ("gate", "up")) if self.layout == "plans" else
+        groups = ((("q", "k", "v"), ("gate", "up"), ("down",)) if self.layout == "plans" else
                   (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)))
         for layer in range(self.layers):
             by = dict(zip(names, self.proj[layer * n:(layer + 1) * n]))
@@ -316,12 +318,12 @@ class Cycle:
             if self.layout == "plans":
                 by = dict(zip([m for m, _, _ in wl.LAYER_PROJECTIONS],
                               self.proj[layer * n:(layer + 1) * n]))
-                self.plans[2 * layer].run()           # q, k, v
+                self.plans[3 * layer].run()           # q, k, v
                 if with_gdn:
                     self._gdn(layer)
                 self.run_qmv(by["o"])
-                self.plans[2 * layer + 1].run()       # gate, up
-                self.run_qmv(by["down"])
+                self.plans[3 * layer + 1].run()       # gate, up
+                self.plans[3 * layer + 2].run()       # down
             elif self.layout == "allplans":
                 self.plans[4 * layer].run()           # q, k, v
                 if with_gdn:
@@ -541,8 +543,8 @@ def run_cycle(args):
     qms = time_graph(torch, qgraph, stream, args.steps, 3)
     qmv_all_gbs = cyc.qmv_bytes / (qms / 1e3 / args.steps) / 1e9
     if cyc.plans:
-        # qmv_plan launches (q,k,v and gate,up of every layer -- with o and
-        # down for "allplans" -- and the LM head) in cycle order as their own
+        # qmv_plan launches (q,k,v, gate,up and down of every layer -- with o
+        # too for "allplans" -- and the LM head) in cycle order as their own
         # graph
         pgraph = capture(torch, cyc.run_plans_only, stream)
         pms = time_graph(torch, pgraph, stream, args.steps, 3)
@@ -1056,9 +1058,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=wl.N_LAYERS,
                     help="decoder layers of the --workload stream plan")
     ap.add_argument("--layout", choices=["plans", "allplans", "launches"], default="plans",
-                    help="cycle: qmv plans for the projections that share an input and "
-                         "qmv_smallm for o and down (plans), plans for every projection "
-                         "(allplans), or one qmv_smallm launch per projection (launches)")
+                    help="cycle: qmv plans for q,k,v / gate,up / down and qmv_smallm for o "
+                         "(plans), plans for every projection (allplans), or one "
+                         "qmv_smallm launch per projection (launches)")
     ap.add_argument("--shape", type=int, nargs=2, metavar=("N", "K"),
                     default=[wl.INTERMEDIATE, wl.HIDDEN],
                     help="output and input size of the --workload qmv projection")
