@@ -48,6 +48,7 @@ constexpr int kCap = 2048;                     // candidate buffer entries
 constexpr int kMaxChunks = 64;                 // V <= 64 * 16384
 constexpr int kMaxK = 8;
 constexpr int kMaxRows = 2 * kMaxK + 1;
+constexpr int kStageBatch = 8;                 // candidate loads per lane in flight
 
 typedef unsigned long long u64;
 
@@ -454,7 +455,22 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
     if (active) {
       u64 *st = stage + (size_t)warp * per_row;
       const u64 *src = a.cand + ((size_t)b * a.rows_max + r) * (size_t)a.C * kMaxTopK;
-      for (int i = lane; i < per_row; i += 32) st[i] = __ldcg(src + (i / ksel) * kMaxTopK + i % ksel);
+      // the row's lists, kStageBatch loads per lane in flight before their
+      // shared-memory stores (a load issued after a store to a possibly
+      // aliasing address would wait for it: one round trip per element)
+      for (int i0 = 0; i0 < per_row; i0 += 32 * kStageBatch) {
+        u64 v[kStageBatch];
+#pragma unroll
+        for (int u = 0; u < kStageBatch; ++u) {
+          const int i = i0 + 32 * u + lane;
+          v[u] = i < per_row ? __ldcg(src + (i / ksel) * kMaxTopK + i % ksel) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kStageBatch; ++u) {
+          const int i = i0 + 32 * u + lane;
+          if (i < per_row) st[i] = v[u];
+        }
+      }
       __syncwarp();
       int h0 = 0, h1 = 0;  // heads of lists lane and lane+32
       int j = 0;
@@ -482,12 +498,26 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
   const bool greedy = a.temperature == 0.f;
   int32_t *out = a.out + (size_t)b * (K + 1);
   for (int j = lane; j <= K; j += 32) out[j] = -1;
+  // every position's inputs at once, lane j holding position j (K <= 8):
+  // draft token, uniform, and the flags of rows j (target) and K+1+j (draft);
+  // lane K the bonus row's flags
+  int d_l = 0, f_t = 0, f_d = 0;
+  float ua_l = 0.f;
+  if (lane < K) {
+    d_l = a.dt[(size_t)b * K + lane];
+    ua_l = a.ua[(size_t)b * K + lane];
+    f_t = __ldcg(&a.rowflags[b * a.rows_max + lane]);
+    if (!greedy) f_d = __ldcg(&a.rowflags[b * a.rows_max + K + 1 + lane]);
+  } else if (lane == K) {
+    f_t = __ldcg(&a.rowflags[b * a.rows_max + K]);
+  }
+  const float us_b = a.us[b];
   __syncwarp();
   int k = 0;
   for (; k < K; ++k) {
-    const int d = a.dt[(size_t)b * K + k];
+    const int d = __shfl_sync(0xffffffffu, d_l, k);
     const bool d_ok = d >= 0 && d < V;
-    flags |= __ldcg(&a.rowflags[b * a.rows_max + k]);
+    flags |= __shfl_sync(0xffffffffu, f_t, k);
     if (greedy) {
       const int am = mcount[k] > 0 ? composite_id(merged[k * kMaxTopK]) : -1;
       if (!d_ok) flags |= SV_FLAG_DRAFT_OUT_OF_RANGE;
@@ -499,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
       emitted = am;
       break;
     }
-    flags |= __ldcg(&a.rowflags[b * a.rows_max + K + 1 + k]);
+    flags |= __shfl_sync(0xffffffffu, f_d, k);
     const RowDist P = row_dist(merged + k * kMaxTopK, mcount[k], a.temperature, a.top_p);
     const RowDist Q =
         row_dist(merged + (K + 1 + k) * kMaxTopK, mcount[K + 1 + k], a.temperature, a.top_p);
@@ -512,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
         flags |= SV_FLAG_DRAFT_ZERO_Q;
       } else {
         const float pd = dist_lookup(P, d);
-        accept = a.ua[(size_t)b * K + k] < pd / qd;
+        accept = __shfl_sync(0xffffffffu, ua_l, k) < pd / qd;
       }
     }
     if (accept) {
@@ -538,17 +568,17 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
       R[0] = P.p[0];
       R[1] = P.p[1];
     }
-    emitted = inverse_cdf_by_id(P.id, R, a.us[b], sR, sId);
+    emitted = inverse_cdf_by_id(P.id, R, us_b, sR, sId);
     break;
   }
   if (emitted == -2) {  // all K accepted: bonus from position K+1
-    flags |= __ldcg(&a.rowflags[b * a.rows_max + K]);
+    flags |= __shfl_sync(0xffffffffu, f_t, K);
     if (greedy) {
       emitted = mcount[K] > 0 ? composite_id(merged[K * kMaxTopK]) : -1;
     } else {
       const RowDist P = row_dist(merged + K * kMaxTopK, mcount[K], a.temperature, a.top_p);
       float R[2] = {P.p[0], P.p[1]};
-      emitted = inverse_cdf_by_id(P.id, R, a.us[b], sR, sId);
+      emitted = inverse_cdf_by_id(P.id, R, us_b, sR, sId);
     }
   }
   if (emitted < 0) flags |= SV_FLAG_EMPTY_DIST;
