@@ -380,19 +380,21 @@ def time_graph(torch, graph, stream, steps: int, warmup: int, barrier=None):
 # CPU oracle on a bounded sample of the cycle
 # ----------------------------------------------------------------------------
 def oracle_cycle_sample(depth: int = 3, layer_fraction: float = 1.0, repeats: int = 8,
-                        lm_fraction: float = 1.0 / 8, head_fraction: float = 1.0):
+                        lm_fraction: float = 1.0 / 8, head_fraction: float = 1.0,
+                        threads: int | None = None):
     """Times the oracle on a sample of one cycle and extrapolates to a full
     cycle: `layer_fraction` of the rows of one layer's seven projections, run
     `repeats` times (x64/repeats layers), `lm_fraction` of the LM-head rows,
     spec_accept at batch 1 on the full vocabulary, and GDN capture + replay on
-    `head_fraction` of one layer's heads (x64 layers).  Returns (seconds per
+    `head_fraction` of one layer's heads (x64 layers), on `threads` host
+    threads (default: every core this process may use).  Returns (seconds per
     cycle, sample text, threads)."""
     import numpy as np
 
     import oracle
 
     oracle.build()
-    threads = oracle.set_threads(len(os.sched_getaffinity(0)))
+    threads = oracle.set_threads(threads or len(os.sched_getaffinity(0)))
     M = depth + 1
     t_qmv = 0.0
     for j, (_, N, Kin) in enumerate(wl.LAYER_PROJECTIONS):
@@ -515,12 +517,20 @@ def run_cycle(args):
 
             dist.barrier()
 
-    cpu = None
+    cpu = cpu1 = None
     if rank == 0 and not args.no_cpu_baseline:
         t, sample, threads = oracle_cycle_sample(args.depth)
         cpu = {"value": 1.0 / t, "unit": "cycles/s", "cores": threads, "kind": "oracle",
                "sample": sample}
         log(f"cpu oracle: {t:.2f} s per cycle (extrapolated) on {threads} threads")
+        # the same oracle on one thread, on a smaller sample (about the same
+        # wall time)
+        t1, sample1, _ = oracle_cycle_sample(args.depth, layer_fraction=1.0 / 4, repeats=1,
+                                             lm_fraction=1.0 / 32, head_fraction=0.25,
+                                             threads=1)
+        cpu1 = {"value": 1.0 / t1, "unit": "cycles/s", "cores": 1, "kind": "oracle",
+                "sample": sample1}
+        log(f"cpu oracle: {t1:.2f} s per cycle (extrapolated) on 1 thread")
 
     sv.set_pdl(True)
     cyc = Cycle(sv, torch, device, depth=args.depth, seed=rank, layout=args.layout)
@@ -673,6 +683,7 @@ def run_cycle(args):
             "how": "measured HBM bandwidth / algorithmic bytes of one cycle (weights, "
                    "activations, GDN state and tape)"},
         "cpu_baseline": cpu,
+        "cpu_baseline_1thread": cpu1,
         "e2e": {"value": total_cycles / t_e2e, "unit": "cycles/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": cyc.launches_per_step * args.steps,
@@ -753,6 +764,7 @@ def run_mlp(args):
                        "l2": "inputs larger than L2"},
             "per_M_gbs": per_m,
             "per_M_frac": {m: v / peaks["hbm_gbs"] for m, v in per_m.items()},
+            "per_M_frac_of_8tbs_nominal": {m: v / 8000.0 for m, v in per_m.items()},
             "per_M_gbs_separate_launches": per_m_launch,
             "peak": peaks}
     print(json.dumps(line), flush=True)
@@ -944,6 +956,7 @@ def run_lmhead(args):
             "spec_accept_greedy_gbs": B * (K + 1) * V * 4 / (gms / 1e3 / args.steps) / 1e9,
             "mean_accepted": float(n.mean()),
             "acceptance_rate_per_position": int(n.sum()) / max(tested, 1),
+            "logit_scale_c": c,
             "mean_accepted_greedy": float(n_greedy.float().mean().item())}
     print(json.dumps(line), flush=True)
     plan.close()
