@@ -150,9 +150,13 @@ sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales, const uin
  * qmv_plan_destroy.  The buffer and every problem's tensors must stay valid
  * while the plan is used.  qmv_plan_run: one launch on `stream` of exactly
  * as many CTAs as fit on the device at once (capturable in a CUDA graph);
- * runs of one plan must not overlap in time.  Its CTAs wait on one another,
- * so the plan assumes that no other work holds SMs indefinitely while it
- * runs (kernels of other streams that themselves wait on this plan would).
+ * runs of one plan must not overlap in time.  Its CTAs wait on one another
+ * (phase counts, split tiles) and it is not a cooperative launch, so every
+ * CTA must become resident: on one device, run plans one at a time (not
+ * concurrently on several streams) and beside no other kernel whose CTAs
+ * wait for one another.  Otherwise two such grids can each hold the SMs the
+ * other needs; the plan's waits then give up after ~1 s, set the device
+ * error word and leave invalid results (no hang).
  * With sv_set_pdl(1) the launch may start while the preceding kernel runs:
  * weights are streamed at once, while x, y and the plan's counters are
  * touched only after that kernel has finished.
