@@ -265,6 +265,7 @@ class QmvPlan:
                                          ctypes.c_void_p(self.buffer.data_ptr() + off),
                                          n, ctypes.byref(h)), "qmv_plan_create")
         self._h = h
+        self._off, self._nbytes = off, n  # the plan's bytes: buffer[off : off + n]
         self.device = dev
         self.problems = list(problems)  # keep the tensors alive
         self.grid = int(lib().qmv_plan_grid(h))

@@ -6,6 +6,8 @@ Chained problems (`after`) read an earlier problem's fp32 output as their
 activations; the oracle chains its own outputs (rounded to fp32), never the
 GPU's.
 """
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -178,3 +180,32 @@ def test_plan_rejects(sv):
     with pytest.raises(sv.SvError):  # reads problem 0's output without `after`
         sv.QmvPlan([(w1, s1, b1, x, y0, False), (wt, st, bt, y0, y, False)])
     sv.QmvPlan([(w1, s1, b1, x, y0, False), (wt, st, bt, y0, y, True)]).close()
+
+
+def test_phase_wait_gives_up_and_reports(sv, oracle):
+    """Failure detection without a fault: the finished-tile count of a
+    two-phase plan (the last 256 bytes of its buffer hold the counters) is
+    preset so that the second phase's wait can never be met.  Every CTA gives
+    up after its bounded wait (about a second), sets the device error word
+    and finishes; sv_device_status reports it, the plan's last CTA has put
+    the count back to zero and the context and the plan work again."""
+    specs = [(1024, 512, None), (512, 1024, 0)]
+    plan, probs, refs = _plan_case(sv, oracle, specs, 4, "f32", 21)
+    end = plan._off + plan._nbytes
+    done = plan.buffer[end - 256:end - 252].view(torch.int32)
+    done.fill_(-(1 << 30))
+    torch.cuda.synchronize()
+    t0 = time.time()
+    plan.run()
+    torch.cuda.synchronize()
+    took = time.time() - t0
+    with pytest.raises(sv.SvError) as e:
+        sv.device_status()
+    assert e.value.status == 4
+    assert 0.5 < took < 60
+    assert int(done.item()) == 0
+    for p in probs:
+        p[4].fill_(float("nan"))
+    plan.run()
+    _check(probs, refs)
+    sv.device_status()
