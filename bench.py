@@ -300,6 +300,15 @@ class Cycle:
                        n_accepted=self.n_acc, err_flags=self.flags)
         sv.gdn_tape_replay(self.state, self.tape, self.n_acc, self.M, n_replay_bias=1)
 
+    def run_stream_accept(self):
+        """The cycle as the weight-stream configuration lists it: every
+        projection of every layer, the LM head and spec_accept (no
+        GatedDeltaNet tape capture or replay)."""
+        self._forward(with_gdn=False)
+        self.sv.spec_accept(self.target, self.draft, self.draft_tokens, self.ua, self.us,
+                            0.6, 20, 0.95, workspace=self.ws, out_tokens=self.out_tokens,
+                            n_accepted=self.n_acc, err_flags=self.flags)
+
     def run_qmv_only(self):
         self._forward(with_gdn=False)
 
@@ -616,6 +625,14 @@ def run_cycle(args):
     t_e2e = max_over_ranks(torch, t_e2e, world, device)
     sv.device_status()
 
+    # the cycle as the weight-stream configuration lists it (projections, LM
+    # head, spec_accept; no GatedDeltaNet tape), for comparison
+    ngraph = capture(torch, cyc.run_stream_accept, stream)
+    nms = time_graph(torch, ngraph, stream, args.steps, args.warmup, barrier)
+    nms = max_over_ranks(torch, nms / 1e3, world, device) * 1e3
+    no_tape = job_rate(args.steps, world, nms / 1e3)
+    del ngraph
+
     # the same cycle at the configuration's other draft depths (same weights,
     # M = K + 1 rows), each its own graph, timed the same way
     depths = {str(args.depth): value}
@@ -689,6 +706,7 @@ def run_cycle(args):
         "gpu_launches": cyc.launches_per_step * args.steps,
         "clocks": clocks,
         "cycles_per_s_by_depth": {k: depths[k] for k in sorted(depths)},
+        "cycles_per_s_without_gdn_tape": no_tape,
         "acceptance": {"mean_accepted": statistics.mean(accepted) if accepted else None,
                        "depth": args.depth, "draws": min(len(accepted), E_DRAWS),
                        "how": "accepted drafts per cycle over the e2e steps (warm-up "
