@@ -15,7 +15,10 @@
 //    streaming loads), bounds the k-th largest from below by the minimum of
 //    64 (or 32, 16) group maxima, keeps only elements at or above that bound
 //    (typically ~1 % of them) as 64-bit keys (ordered float bits, then lower
-//    token id), and writes the chunk's exact top-k sorted to the workspace:
+//    token id), and writes the chunk's exact top-k sorted to the workspace;
+//    chunks of finite logits do the maxima and the bound test in float and
+//    build keys only for the kept elements (placed by warp ballots), chunks
+//    holding a NaN or an infinity take the same steps on keys throughout:
 //    with at most 512 candidates each thread ranks its own by counting the
 //    larger keys; otherwise a block radix select finds the k-th key first;
 //  * the last CTA of a sequence to finish (CTA barrier, then one acq_rel
@@ -30,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cfloat>
 #include <cstdint>
 #include <mutex>
 
@@ -111,7 +115,9 @@ struct ChunkSmem {
   u64 top[kMaxTopK];
   unsigned hist[256];
   uint32_t gmax[64];
+  float gmaxf[64];
   uint32_t tau;
+  float tauf;
   int nc, ntop, done, rem;
   u64 prefix;
   int last;
@@ -299,75 +305,130 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
   const int base = cx * kChunk;
   const int ksel = a.ksel;
 
-  // ---- load the chunk and map it to ordered keys ---------------------------
-  uint32_t key[kPerThread];
-  int nonfinite = 0;
+  // ---- load the chunk (values past V read as -inf: key 0, never kept) ------
+  float v[kPerThread];
+  float vsum = 0.f;  // finite iff every value of this thread's share is
   if (a.vec) {
 #pragma unroll
     for (int i = 0; i < kPerThread / 4; ++i) {
       const int e = base + 4 * (tid + kThreads * i);
-      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-      const bool in = e < V;  // V % 4 == 0 on this path
-      if (in) f = __ldcs(reinterpret_cast<const float4 *>(row + e));
-      key[4 * i + 0] = in ? logit_key(f.x, nonfinite) : 0u;
-      key[4 * i + 1] = in ? logit_key(f.y, nonfinite) : 0u;
-      key[4 * i + 2] = in ? logit_key(f.z, nonfinite) : 0u;
-      key[4 * i + 3] = in ? logit_key(f.w, nonfinite) : 0u;
+      float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      if (e < V) {  // V % 4 == 0 on this path
+        f = __ldcs(reinterpret_cast<const float4 *>(row + e));
+        vsum += (f.x + f.y) + (f.z + f.w);
+      }
+      v[4 * i + 0] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
     }
   } else {
 #pragma unroll
     for (int i = 0; i < kPerThread; ++i) {
       const int e = base + tid + kThreads * i;
-      key[i] = e < V ? logit_key(__ldcs(row + e), nonfinite) : 0u;
+      v[i] = -INFINITY;
+      if (e < V) {
+        v[i] = __ldcs(row + e);
+        vsum += v[i];
+      }
     }
   }
   auto index_of = [&](int i) -> uint32_t {
     return a.vec ? (uint32_t)(base + 4 * (tid + kThreads * (i >> 2)) + (i & 3))
                  : (uint32_t)(base + tid + kThreads * i);
   };
+  // Rows whose chunk holds a NaN or an infinity (a -inf mask included) take
+  // the exact key path below; the others the float path, which keeps the same
+  // candidates (the key map is monotone on finite values and maps -0 and +0
+  // to one key) and computes keys only for them.
+  int nonfinite = 0, dummy = 0;
 
   // ---- lower bound on the ksel-th largest: min over >= ksel group maxima --
-  uint32_t tmax = 0;
-#pragma unroll
-  for (int i = 0; i < kPerThread; ++i) tmax = max(tmax, key[i]);
+  // (group maxima in float; the same barrier tells whether the chunk is
+  // exotic, and only then are key maxima taken, behind one more barrier)
   const int n_groups = ksel <= 16 ? 16 : (ksel <= 32 ? 32 : 64);
   const int tpg = kThreads / n_groups;  // 32, 16 or 8 threads per group
-  for (int o = 1; o < tpg; o <<= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-  if ((tid % tpg) == 0) S.gmax[tid / tpg] = tmax;
+  {
+    float fmx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) fmx = fmaxf(fmx, v[i]);
+    for (int o = 1; o < tpg; o <<= 1) fmx = fmaxf(fmx, __shfl_xor_sync(0xffffffffu, fmx, o));
+    if ((tid % tpg) == 0) S.gmaxf[tid / tpg] = fmx;
+  }
   if (tid == 0) S.nc = 0;
-  __syncthreads();
+  const int exotic = __syncthreads_or(!(fabsf(vsum) <= FLT_MAX));
+  if (exotic) {
+    uint32_t tmax = 0;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) tmax = max(tmax, logit_key(v[i], nonfinite));
+    for (int o = 1; o < tpg; o <<= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    if ((tid % tpg) == 0) S.gmax[tid / tpg] = tmax;
+    __syncthreads();
+  }
   if (warp == 0) {
-    const uint32_t g0 = lane < n_groups ? S.gmax[lane] : 0u;
-    const uint32_t g1 = lane + 32 < n_groups ? S.gmax[lane + 32] : 0u;
-    const int nz = __popc(__ballot_sync(0xffffffffu, g0 != 0)) +
-                   __popc(__ballot_sync(0xffffffffu, g1 != 0));
-    uint32_t mn = 0xFFFFFFFFu;
-    if (g0) mn = min(mn, g0);
-    if (g1) mn = min(mn, g1);
-    for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    if (lane == 0) S.tau = nz >= ksel ? mn : 1u;
+    if (!exotic) {  // a group of padding only has maximum -inf
+      const float g0 = lane < n_groups ? S.gmaxf[lane] : -INFINITY;
+      const float g1 = lane + 32 < n_groups ? S.gmaxf[lane + 32] : -INFINITY;
+      const int nz = __popc(__ballot_sync(0xffffffffu, g0 > -INFINITY)) +
+                     __popc(__ballot_sync(0xffffffffu, g1 > -INFINITY));
+      float mn = INFINITY;
+      if (g0 > -INFINITY) mn = fminf(mn, g0);
+      if (g1 > -INFINITY) mn = fminf(mn, g1);
+      for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      if (lane == 0) S.tauf = nz >= ksel ? mn : -FLT_MAX;  // else every finite value
+    } else {
+      const uint32_t g0 = lane < n_groups ? S.gmax[lane] : 0u;
+      const uint32_t g1 = lane + 32 < n_groups ? S.gmax[lane + 32] : 0u;
+      const int nz = __popc(__ballot_sync(0xffffffffu, g0 != 0)) +
+                     __popc(__ballot_sync(0xffffffffu, g1 != 0));
+      uint32_t mn = 0xFFFFFFFFu;
+      if (g0) mn = min(mn, g0);
+      if (g1) mn = min(mn, g1);
+      for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      if (lane == 0) S.tau = nz >= ksel ? mn : 1u;
+    }
   }
   __syncthreads();
-  const uint32_t tau = S.tau;
 
   // ---- keep the candidates at or above the bound ---------------------------
-  int cnt = 0;
+  if (!exotic) {
+    // candidates are rare (~1 %): one ballot per value slot, and only a warp
+    // that has some reserves places for them
+    const float tauf = S.tauf;
+    const unsigned below = (1u << lane) - 1u;
 #pragma unroll
-  for (int i = 0; i < kPerThread; ++i) cnt += key[i] >= tau ? 1 : 0;
-  int incl = cnt;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  int wbase = 0;
-  if (lane == 31) wbase = atomicAdd(&S.nc, incl);
-  wbase = __shfl_sync(0xffffffffu, wbase, 31);
-  int pos = wbase + incl - cnt;
+    for (int i = 0; i < kPerThread; ++i) {
+      const bool keep = v[i] >= tauf;
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      if (m) {
+        int wb = 0;
+        if (lane == 0) wb = atomicAdd(&S.nc, __popc(m));
+        wb = __shfl_sync(0xffffffffu, wb, 0);
+        const int pos = wb + __popc(m & below);
+        if (keep && pos < kCap) S.buf[pos] = composite(logit_key(v[i], dummy), index_of(i));
+      }
+    }
+  } else {
+    const uint32_t tau = S.tau;
+    int cnt = 0;
 #pragma unroll
-  for (int i = 0; i < kPerThread; ++i) {
-    if (key[i] >= tau) {
-      if (pos < kCap) S.buf[pos] = composite(key[i], index_of(i));
-      ++pos;
+    for (int i = 0; i < kPerThread; ++i) cnt += logit_key(v[i], dummy) >= tau ? 1 : 0;
+    int incl = cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int wbase = 0;
+    if (lane == 31) wbase = atomicAdd(&S.nc, incl);
+    wbase = __shfl_sync(0xffffffffu, wbase, 31);
+    int pos = wbase + incl - cnt;
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      const uint32_t k = logit_key(v[i], dummy);
+      if (k >= tau) {
+        if (pos < kCap) S.buf[pos] = composite(k, index_of(i));
+        ++pos;
+      }
     }
   }
   const int any_nonfinite = __syncthreads_or(nonfinite);
@@ -399,17 +460,26 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
       if (c >= thr) S.top[atomicAdd(&S.ntop, 1)] = c;
     }
   } else {  // many ties / a flat row: select over the whole chunk
+    // (rare) the logits are read again from L2, so that the values need not
+    // stay in registers through the selection
+    auto key_again = [&](int i) -> uint32_t {
+      const int e = (int)index_of(i);
+      return e < V ? logit_key(__ldcg(row + e), dummy) : 0u;
+    };
     thr = block_select_threshold(S, ksel, [&](auto f) {
-#pragma unroll
-      for (int i = 0; i < kPerThread; ++i)
-        if (key[i]) f(composite(key[i], index_of(i)));
+#pragma unroll 4
+      for (int i = 0; i < kPerThread; ++i) {
+        const uint32_t k = key_again(i);
+        if (k) f(composite(k, index_of(i)));
+      }
     });
     if (tid == 0) S.ntop = 0;
     __syncthreads();
-#pragma unroll
+#pragma unroll 4
     for (int i = 0; i < kPerThread; ++i) {
-      if (key[i]) {
-        const u64 c = composite(key[i], index_of(i));
+      const uint32_t k = key_again(i);
+      if (k) {
+        const u64 c = composite(k, index_of(i));
         if (c >= thr) S.top[atomicAdd(&S.ntop, 1)] = c;
       }
     }
