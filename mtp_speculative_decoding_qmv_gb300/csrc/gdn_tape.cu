@@ -90,6 +90,8 @@ __device__ __forceinline__ float row_sum(float v) {
   return v;
 }
 
+// kFull: dk == kMaxDim, so every lane's chunks are real columns (no checks).
+template <bool kFull>
 __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) {
   __shared__ __align__(16) float ks[kMaxT][kMaxDim];
   __shared__ __align__(16) float qs[kMaxT][kMaxDim];
@@ -166,10 +168,24 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
 
   __syncthreads();
 
+  // the token's records and outputs advance by fixed strides
+  float *e_out = a.tape.e(b, 0, h) + i;
+  float *o_out = a.out ? a.out + ((size_t)b * a.T * a.H + h) * a.dv + i : nullptr;
+  float *k_out = a.tape.k(b, 0, h);
+  float *al_out = a.tape.alpha(b, 0, h);
+  const size_t e_step = (size_t)a.H * a.dv, k_step = (size_t)a.H * a.dk;
   for (int t = 0; t < a.T; ++t) {
     const float al = als[t], be = bes[t];
-    // S' = alpha S ; u = S' k   (chunks past dk hold zeros and contribute 0;
-    // one partial sum per chunk keeps four independent FMA chains)
+    // this lane's key chunks, read once for both passes (chunks past dk hold
+    // zeros and contribute 0)
+    float4 kr[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c)
+      kr[c] = (kFull || chunk_col(j, c) < a.dk)
+                  ? *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)])
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    // S' = alpha S ; u = S' k   (one partial sum per chunk keeps four
+    // independent FMA chains)
     float uc[kChunks];
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
@@ -178,8 +194,8 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
       S[4 * c + 2] = __fmul_rn(al, S[4 * c + 2]);
       S[4 * c + 3] = __fmul_rn(al, S[4 * c + 3]);
       uc[c] = 0.f;
-      if (chunk_col(j, c) < a.dk) {
-        const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
+      if (kFull || chunk_col(j, c) < a.dk) {
+        const float4 kk = kr[c];
         uc[c] = fmaf(S[4 * c], kk.x, uc[c]);
         uc[c] = fmaf(S[4 * c + 1], kk.y, uc[c]);
         uc[c] = fmaf(S[4 * c + 2], kk.z, uc[c]);
@@ -193,8 +209,8 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
       oc[c] = 0.f;
-      if (chunk_col(j, c) < a.dk) {
-        const float4 kk = *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)]);
+      if (kFull || chunk_col(j, c) < a.dk) {
+        const float4 kk = kr[c];
         const float4 qq = *reinterpret_cast<const float4 *>(&qs[t][chunk_col(j, c)]);
         S[4 * c] = __fmaf_rn(e, kk.x, S[4 * c]);
         S[4 * c + 1] = __fmaf_rn(e, kk.y, S[4 * c + 1]);
@@ -207,15 +223,18 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
       }
     }
     const float o = row_sum((oc[0] + oc[1]) + (oc[2] + oc[3]));
-    const size_t bth = ((size_t)b * a.T + t) * a.H + h;
     if (row_ok && j == 0) {
-      a.tape.e(b, t, h)[i] = e;
-      if (a.out) a.out[bth * a.dv + i] = o;
+      *e_out = e;
+      if (o_out) *o_out = o;
     }
     if (blockIdx.x == 0) {
-      for (int c = tid; c < a.dk; c += kThreads) a.tape.k(b, t, h)[c] = ks[t][c];
-      if (tid == 0) *a.tape.alpha(b, t, h) = al;
+      for (int c = tid; c < a.dk; c += kThreads) k_out[c] = ks[t][c];
+      if (tid == 0) *al_out = al;
     }
+    e_out += e_step;
+    if (o_out) o_out += e_step;
+    k_out += k_step;
+    al_out += a.H;
   }
   if (a.state_out && row_ok) {
     float *dst = a.state_out + (((size_t)b * a.H + h) * a.dv + i) * a.dk;
@@ -383,7 +402,8 @@ extern "C" sv_status gdn_tape_capture(const float *state0, const float *q, const
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   // launched in stream order (starting early measured slower); the kernel
   // triggers its dependents at entry so the following kernel may start early
-  if (cudaLaunchKernelEx(&cfg, gdn_capture_kernel, args) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, dk == kMaxDim ? gdn_capture_kernel<true> : gdn_capture_kernel<false>,
+                         args) != cudaSuccess)
     return fail(SV_ERR_CUDA, "gdn_capture: launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return check_launch("gdn_tape_capture");
 }
