@@ -236,6 +236,20 @@ __device__ RowDist row_dist(const u64 *top, int n, float temperature, float top_
   return D;
 }
 
+// A distribution stored by row_dist's warp (see the finish phase).
+__device__ __forceinline__ RowDist stored_dist(const float *dist_p, const int *dist_id,
+                                               const int *dist_n, int row) {
+  const int lane = threadIdx.x & 31;
+  RowDist D;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    D.p[h] = dist_p[row * 64 + lane + 32 * h];
+    D.id[h] = dist_id[row * 64 + lane + 32 * h];
+  }
+  D.n = dist_n[row];
+  return D;
+}
+
 __device__ float dist_lookup(const RowDist &D, int token) {
   const unsigned hit0 = __ballot_sync(0xffffffffu, D.id[0] == token && D.p[0] > 0.f);
   const unsigned hit1 = __ballot_sync(0xffffffffu, D.id[1] == token && D.p[1] > 0.f);
@@ -247,17 +261,19 @@ __device__ float dist_lookup(const RowDist &D, int token) {
 
 // Smallest token id whose running sum of R (ascending id) exceeds u * sum(R);
 // the last token with R > 0 if rounding never crosses; -1 if sum(R) <= 0.
-// ids[h], R[h] as in RowDist; scratch: 64 floats + 64 ints of warp smem.
+// ids[h], R[h] as in RowDist, the same 64 ids also in shared memory (row_ids,
+// read by every lane at once); scratch: 64 floats + 64 ints of warp smem.
 __device__ int inverse_cdf_by_id(const int (&ids)[2], const float (&R)[2], float u, float *sR,
-                                 int *sId) {
+                                 int *sId, const int *row_ids) {
   const int lane = threadIdx.x & 31;
   // rank of each of the 64 slots by (token id, slot); id -1 (unused) sorts last
   int rank[2] = {0, 0};
   u64 mykey[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) mykey[h] = ((u64)(uint32_t)ids[h] << 8) | (u64)(lane + 32 * h);
+#pragma unroll 8
   for (int src = 0; src < 64; ++src) {
-    const int other = __shfl_sync(0xffffffffu, ids[src >> 5], src & 31);
+    const int other = row_ids[src];
     const u64 okey = ((u64)(uint32_t)other << 8) | (u64)src;
 #pragma unroll
     for (int h = 0; h < 2; ++h) rank[h] += (okey < mykey[h]) ? 1 : 0;
@@ -517,7 +533,12 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
   // from here on; this region aliases them.
   u64 *merged = reinterpret_cast<u64 *>(smem_raw);              // [kMaxRows][kMaxTopK]
   int *mcount = reinterpret_cast<int *>(merged + kMaxRows * kMaxTopK);
-  u64 *stage = reinterpret_cast<u64 *>(mcount + kMaxRows + 1);  // [wave][C*ksel] (8-aligned)
+  // each row's filtered distribution, built by the warp that merged it:
+  // entry j at [row][j] (j = lane + 32 h of RowDist), and its support size
+  float *dist_p = reinterpret_cast<float *>(mcount + kMaxRows + 1);  // [kMaxRows][64]
+  int *dist_id = reinterpret_cast<int *>(dist_p + kMaxRows * 64);    // [kMaxRows][64]
+  int *dist_n = dist_id + kMaxRows * 64;                             // [kMaxRows + 1]
+  u64 *stage = reinterpret_cast<u64 *>(dist_n + kMaxRows + 1);  // [wave][C*ksel] (8-aligned)
   const int per_row = a.C * ksel;
   for (int r0 = 0; r0 < a.rows; r0 += a.rows_per_wave) {
     const int r = r0 + warp;
@@ -555,6 +576,16 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
         if (lane == 0) merged[r * kMaxTopK + j] = g;
       }
       if (lane == 0) mcount[r] = j;
+      if (a.temperature != 0.f) {  // the distribution, while the other rows merge
+        __syncwarp();
+        const RowDist D = row_dist(merged + r * kMaxTopK, j, a.temperature, a.top_p);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          dist_p[r * 64 + lane + 32 * h] = D.p[h];
+          dist_id[r * 64 + lane + 32 * h] = D.id[h];
+        }
+        if (lane == 0) dist_n[r] = D.n;
+      }
     }
     __syncthreads();
   }
@@ -600,9 +631,9 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
       break;
     }
     flags |= __shfl_sync(0xffffffffu, f_d, k);
-    const RowDist P = row_dist(merged + k * kMaxTopK, mcount[k], a.temperature, a.top_p);
-    const RowDist Q =
-        row_dist(merged + (K + 1 + k) * kMaxTopK, mcount[K + 1 + k], a.temperature, a.top_p);
+    const RowDist P = stored_dist(dist_p, dist_id, dist_n, k);
+    const int qrow = K + 1 + k;
+    const RowDist Q = stored_dist(dist_p, dist_id, dist_n, qrow);
     bool accept = false;
     if (!d_ok) {
       flags |= SV_FLAG_DRAFT_OUT_OF_RANGE;
@@ -620,11 +651,13 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
       ++nacc;
       continue;
     }
-    // residual max(0, p - q) over p's support
+    // residual max(0, p - q) over p's support (q's entries read from the
+    // stored distribution, all lanes the same address: broadcast)
     float R[2] = {P.p[0], P.p[1]};
+#pragma unroll 8
     for (int src = 0; src < 64; ++src) {
-      const int qid = __shfl_sync(0xffffffffu, Q.id[src >> 5], src & 31);
-      const float qp = __shfl_sync(0xffffffffu, Q.p[src >> 5], src & 31);
+      const int qid = dist_id[qrow * 64 + src];
+      const float qp = dist_p[qrow * 64 + src];
       if (qid >= 0 && qp > 0.f) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -638,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
       R[0] = P.p[0];
       R[1] = P.p[1];
     }
-    emitted = inverse_cdf_by_id(P.id, R, us_b, sR, sId);
+    emitted = inverse_cdf_by_id(P.id, R, us_b, sR, sId, dist_id + k * 64);
     break;
   }
   if (emitted == -2) {  // all K accepted: bonus from position K+1
@@ -646,9 +679,9 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
     if (greedy) {
       emitted = mcount[K] > 0 ? composite_id(merged[K * kMaxTopK]) : -1;
     } else {
-      const RowDist P = row_dist(merged + K * kMaxTopK, mcount[K], a.temperature, a.top_p);
+      const RowDist P = stored_dist(dist_p, dist_id, dist_n, K);
       float R[2] = {P.p[0], P.p[1]};
-      emitted = inverse_cdf_by_id(P.id, R, us_b, sR, sId);
+      emitted = inverse_cdf_by_id(P.id, R, us_b, sR, sId, dist_id + K * 64);
     }
   }
   if (emitted < 0) flags |= SV_FLAG_EMPTY_DIST;
@@ -755,6 +788,7 @@ extern "C" sv_status spec_accept(const float *target_logits, const float *draft_
   args.rows_per_wave = (int)std::max<size_t>(
       1, std::min<size_t>({(size_t)args.rows, (size_t)kWarps, (size_t)(48 * 1024) / per_row}));
   const size_t final_bytes = (size_t)kMaxRows * kMaxTopK * 8 + (kMaxRows + 1) * 4 +
+                             (size_t)kMaxRows * 64 * 8 + (kMaxRows + 1) * 4 +
                              std::max<size_t>((size_t)args.rows_per_wave * per_row, 64 * 8);
   const size_t smem = std::max(sizeof(ChunkSmem), final_bytes);
   static bool configured[64] = {};
