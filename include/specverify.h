@@ -20,6 +20,9 @@
  *   gdn_tape_replay   rebuild the recurrent state over an accepted prefix
  *   conv_window_*     short convolution windows: outputs, commit of a prefix
  *   qmv_identity_probe  start-up check: block verify rows == single-row calls
+ *   qmv_wide          the same product for wide blocks (M = 17..128, e.g. the
+ *                     verify blocks of 32 sequences against one LM head) on
+ *                     the tcgen05 tensor cores
  *
  * Conventions (all entry points):
  *  - Every tensor argument is a DEVICE pointer owned by the caller, to
@@ -215,6 +218,38 @@ sv_status qmv_identity_probe(const uint32_t *w_packed, const uint16_t *scales,
                              const uint16_t *biases, sv_dtype x_dtype, int M, int N, int K,
                              void *scratch, size_t scratch_bytes, int *mismatches,
                              sv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* qmv_wide: y[M][N] = x[M][K] . W^T for wide blocks, tcgen05 tensor cores.  */
+/* ------------------------------------------------------------------------ */
+/* Sources: "MTP in llama.cpp", section "Theoretical maximum tg t/s" (the
+ * verify step streams the quantised weights once, whatever the number of
+ * rows) and "MTPLX 2.24x faster TPS", section "Layer 0: MLX Runtime" (the
+ * verify block goes through every 4-bit projection, the LM head included).
+ * When the verify blocks of many sequences share one weight matrix (32
+ * sequences x (K+1) = 128 rows against the LM head) the product is a dense
+ * contraction of about 64 flops per weight byte.
+ *
+ * Same operation, weight format (w_packed, scales, biases) and output layout
+ * as qmv_smallm, for bf16 activations x [M][K]:
+ *   y[m][n] = sum_i x[m][i] * (s[n][i/64] * q[n][i] + b[n][i/64])  (fp32).
+ * Computed as two bf16 products against the exact split s*q = hi + lo plus
+ * sum_g b[n][g] * X[m][g] (X = the group sums of x, fp32, split into two bf16
+ * parts), all accumulated in fp32 on the tensor cores: the result is exact
+ * up to fp32 rounding of the sums and the 2^-17 relative split of X.
+ *
+ * Requires 0 <= M <= 128, N >= 0, K % 512 == 0; w_packed, scales, biases and
+ * x 16-byte aligned, y 4-byte aligned; y must not overlap any input.
+ * workspace: caller-owned device memory, 256-byte aligned, at least
+ * qmv_wide_workspace_bytes(M, K) bytes (0 on invalid input), not overlapping
+ * the inputs or y; it is overwritten (the split group sums of x).  Two
+ * launches on `stream` (the group sums, then the product); M = 0 or N = 0
+ * launches nothing.  A kernel wait that gives up (only if the device
+ * misbehaves) sets a word read by sv_device_status. */
+size_t qmv_wide_workspace_bytes(int M, int K);
+sv_status qmv_wide(const uint32_t *w_packed, const uint16_t *scales, const uint16_t *biases,
+                   const uint16_t *x, float *y, int M, int N, int K, void *workspace,
+                   size_t workspace_bytes, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* spec_accept: probability-ratio verification of K drafts per sequence.     */

@@ -95,6 +95,10 @@ def lib() -> ctypes.CDLL:
         L.qmv_identity_probe_bytes.restype = Z
         L.qmv_identity_probe.argtypes = [P, P, P, I, I, I, I, P, Z, ctypes.POINTER(I), P]
         L.qmv_identity_probe.restype = I
+        L.qmv_wide_workspace_bytes.argtypes = [I, I]
+        L.qmv_wide_workspace_bytes.restype = Z
+        L.qmv_wide.argtypes = [P, P, P, P, P, I, I, I, P, Z, P]
+        L.qmv_wide.restype = I
         L.conv_window_capture.argtypes = [P, P, P, I, I, I, I, P, P]
         L.conv_window_capture.restype = I
         L.conv_window_replay.argtypes = [P, P, P, I, I, I, I, I, I, P, P]
@@ -222,6 +226,53 @@ def qmv_identity_probe(w_packed: torch.Tensor, scales: torch.Tensor, biases: tor
                                   _stream(dev))
     _check(st, "qmv_identity_probe")
     return int(out.value)
+
+
+def make_wide_workspace(M: int, K: int, device) -> torch.Tensor:
+    """A workspace for qmv_wide with M activation rows of K inputs (256-byte
+    aligned: torch's allocator aligns far more)."""
+    nbytes = int(lib().qmv_wide_workspace_bytes(M, K))
+    if nbytes == 0:
+        _check(SV_ERR_INVALID_ARG, "qmv_wide_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def qmv_wide(w_packed: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+             x: torch.Tensor, y: torch.Tensor | None = None,
+             workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M, N] (fp32) = x[M, K] . W^T on the tcgen05 tensor cores, M <= 128.
+
+    Weight layout of qmv_smallm; x bf16 [M, K], K % 512 == 0.  ``workspace``
+    (uint8, from make_wide_workspace) is allocated per call when omitted.
+    """
+    dev = w_packed.device
+    N, K8 = w_packed.shape
+    K = K8 * 8
+    M = x.shape[0]
+    wdt = w_packed.dtype
+    if wdt not in (torch.int32, torch.uint32):
+        raise TypeError("w_packed must be int32 or uint32")
+    _need(w_packed, "w_packed", wdt, (N, K8), dev)
+    sdt = scales.dtype
+    if sdt not in (torch.bfloat16, torch.int16):
+        raise TypeError("scales must be bfloat16 (or int16 bit patterns)")
+    _need(scales, "scales", sdt, (N, K // 64), dev)
+    _need(biases, "biases", sdt, (N, K // 64), dev)
+    if x.dtype not in (torch.bfloat16, torch.int16):
+        raise TypeError("x must be bfloat16 (or int16 bit patterns)")
+    _need(x, "x", x.dtype, (M, K), dev)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    _need(y, "y", torch.float32, (M, N), dev)
+    if workspace is None:
+        nbytes = int(lib().qmv_wide_workspace_bytes(M, K))
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    if workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor on the weights' device")
+    st = lib().qmv_wide(_ptr(w_packed), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K,
+                        _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(st, "qmv_wide")
+    return y
 
 
 class QmvPlan:

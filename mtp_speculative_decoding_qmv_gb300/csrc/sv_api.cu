@@ -79,8 +79,9 @@ extern "C" sv_status sv_device_status(void) {
   const unsigned a = sv::take_device_error_accept();
   const unsigned g = sv::take_device_error_gdn();
   const unsigned p = sv::take_device_error_plan();
-  if (q | a | g | p)
-    return sv::fail(SV_ERR_DEVICE_FLAG, "device error words: qmv=%u accept=%u gdn=%u plan=%u", q,
-                    a, g, p);
+  const unsigned w = sv::take_device_error_wide();
+  if (q | a | g | p | w)
+    return sv::fail(SV_ERR_DEVICE_FLAG,
+                    "device error words: qmv=%u accept=%u gdn=%u plan=%u wide=%u", q, a, g, p, w);
   return SV_OK;
 }

@@ -34,5 +34,6 @@ unsigned take_device_error_qmv();
 unsigned take_device_error_accept();
 unsigned take_device_error_gdn();
 unsigned take_device_error_plan();
+unsigned take_device_error_wide();
 
 }  // namespace sv

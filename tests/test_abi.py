@@ -191,3 +191,26 @@ def test_identity_probe_sizes_and_rejects(L):
     assert L.qmv_identity_probe(w, s, b, 1, 4, 512, 512, w, n, ctypes.byref(out),
                                 None) == 1  # scratch overlaps the weights
     assert out.value == 7  # rejected before any work: left unchanged
+
+
+def test_wide_sizes_and_rejects(L):
+    # split group sums: M rows x (2 K/64 rounded up to 64) bf16, 256-byte multiple
+    assert L.qmv_wide_workspace_bytes(128, 5120) == 128 * 192 * 2
+    assert L.qmv_wide_workspace_bytes(3, 512) == 512
+    assert L.qmv_wide_workspace_bytes(129, 512) == 0
+    assert L.qmv_wide_workspace_bytes(4, 640) == 0
+    w, s, b, x, y, ws = (A + i * 0x1000000 for i in range(6))
+    n = L.qmv_wide_workspace_bytes(64, 1024)
+    assert L.qmv_wide(w, s, b, x, y, 0, 300, 1024, None, 0, None) == 0  # M = 0: no launch
+    assert L.qmv_wide(w, s, b, x, y, 64, 0, 1024, None, 0, None) == 0   # N = 0: no launch
+    assert L.qmv_wide(w, s, b, x, y, 129, 300, 1024, ws, n, None) == 2
+    assert L.qmv_wide(w, s, b, x, y, 64, 300, 1000, ws, n, None) == 1   # K % 512
+    assert L.qmv_wide(w, s, b, x, y, -1, 300, 1024, ws, n, None) == 1
+    assert L.qmv_wide(None, s, b, x, y, 64, 300, 1024, ws, n, None) == 1
+    assert L.qmv_wide(w, s, b, x, y, 64, 300, 1024, None, n, None) == 1
+    assert L.qmv_wide(w + 8, s, b, x, y, 64, 300, 1024, ws, n, None) == 1  # 16-byte alignment
+    assert L.qmv_wide(w, s, b, x, y + 2, 64, 300, 1024, ws, n, None) == 1  # 4-byte alignment
+    assert L.qmv_wide(w, s, b, x, y, 64, 300, 1024, ws + 16, n, None) == 1  # 256-byte alignment
+    assert L.qmv_wide(w, s, b, x, y, 64, 300, 1024, ws, n - 1, None) == 1  # too small
+    assert L.qmv_wide(w, s, b, x, x, 64, 300, 1024, ws, n, None) == 1      # y overlaps x
+    assert L.qmv_wide(w, s, b, x, y, 64, 300, 1024, x, n, None) == 1       # workspace = x
