@@ -60,8 +60,11 @@ def measured_peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
         d = json.loads(p.read_text())
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        out = {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+        if "bf16_tflops" in d:
+            out["bf16_tflops"] = float(d["bf16_tflops"])
+        return out
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 # DRAM bytes (read + written) per algorithmic byte of one qmv_plan launch,
@@ -837,6 +840,61 @@ def run_qmv(args):
     return 0
 
 
+def run_wide(args):
+    """qmv_wide on one wide block (--rows M, default the 128 verify rows of 32
+    sequences at K = 3) against --wide-shape N K (default the LM head
+    5120 -> 151936), on enough weight copies that they stream from HBM, in one
+    CUDA graph; TFLOP/s of the product against the measured bf16 peak.  Also
+    the case the ncu captures of the tcgen05 kernel run."""
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    N, K = args.wide_shape
+    M = args.rows
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.MASTER_SEED + 41)
+    per = qmv_bytes(M, N, K)
+    copies = max(1, -(-300_000_000 // per))
+    weights = []
+    for _ in range(copies):
+        w = torch.randint(-(2 ** 31), 2 ** 31 - 1, (N, K // 8), generator=g, device=dev,
+                          dtype=torch.int32)
+        s_ = (torch.randn((N, K // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        b_ = (torch.randn((N, K // GROUP), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        weights.append((w, s_, b_))
+    x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty((M, N), device=dev)
+    ws = sv.make_wide_workspace(M, K, dev)
+
+    def fn():
+        for w, s_, b_ in weights:
+            sv.qmv_wide(w, s_, b_, x, y=y, workspace=ws)
+
+    stream = torch.cuda.Stream(dev)
+    graph = capture(torch, fn, stream)
+    ms = time_graph(torch, graph, stream, args.steps, args.warmup)
+    us = ms / args.steps / copies * 1e3
+    peaks = measured_peaks()
+    tflops = 2 * M * N * K / (us / 1e6) / 1e12
+    n_mma = -(-M // 16) * 16
+    issued = 2 * n_mma * N * (2 * K + 64 * (-(-2 * (K // GROUP) // 64))) / (us / 1e6) / 1e12
+    line = {"metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"qmv_wide {K}->{N}, M={M}, {copies} weight copies in one "
+                                   "CUDA graph", "l2": "inputs larger than L2"},
+            "us_per_call": us, "gbs": per / (us / 1e6) / 1e9,
+            "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
+            "tensor_tflops_issued": issued,
+            "issued_frac_of_bf16_peak": issued / peaks["bf16_tflops"],
+            "peak": peaks}
+    print(json.dumps(line), flush=True)
+    sv.device_status()
+    return 0
+
+
 def run_stream(args):
     """The 27B-class verify weight stream (--layers decoder layers of q, k,
     v, o 5120x5120, gate, up 5120->17408, down 17408->5120, plus the LM head
@@ -1113,7 +1171,7 @@ def main(argv=None):
     ap.add_argument("--no-depth-sweep", action="store_true",
                     help="cycle: skip the draft depths K = 2..5 other than --depth")
     ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn", "qmv", "stream",
-                                           "conv"],
+                                           "conv", "wide"],
                     default="cycle")
     ap.add_argument("--layers", type=int, default=wl.N_LAYERS,
                     help="decoder layers of the --workload stream plan")
@@ -1124,13 +1182,18 @@ def main(argv=None):
     ap.add_argument("--shape", type=int, nargs=2, metavar=("N", "K"),
                     default=[wl.INTERMEDIATE, wl.HIDDEN],
                     help="output and input size of the --workload qmv projection")
+    ap.add_argument("--wide-shape", type=int, nargs=2, metavar=("N", "K"),
+                    default=[wl.VOCAB, wl.HIDDEN],
+                    help="output and input size of the --workload wide product")
+    ap.add_argument("--rows", type=int, default=128,
+                    help="activation rows M of the --workload wide product")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
     return {"cycle": run_cycle, "mlp": run_mlp, "lmhead": run_lmhead, "gdn": run_gdn,
-            "qmv": run_qmv, "stream": run_stream, "conv": run_conv}[
+            "qmv": run_qmv, "stream": run_stream, "conv": run_conv, "wide": run_wide}[
         args.workload](args)
 
 

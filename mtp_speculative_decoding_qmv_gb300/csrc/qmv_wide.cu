@@ -24,12 +24,15 @@
 //
 // One persistent CTA per SM, 128 weight rows (the MMA's M) per tile, tiles
 // strided over the grid.  Warp roles:
-//   warp 13     TMA producer: packed weights (128 rows x 256 inputs, 128-byte
-//               swizzle) and activation stages (64 inputs x rows, 128-byte
-//               swizzle, the MMA's K-major B operand), each on an mbarrier ring;
+//   warp 13     TMA producer of the packed weights (128 rows x 256 inputs,
+//               128-byte swizzle) on its own mbarrier ring;
+//   warp 14     TMA producer of the activation stages (64 inputs x rows,
+//               128-byte swizzle, the MMA's K-major B operand) on a deep ring:
+//               the tiles come from L2, every CTA re-reading them, and each
+//               takes ~1.5 us to land;
 //   warps 4-11  widen a 64-input group of their 32 rows (two warps per TMEM
-//               lane quarter, one half of the group each) into bf16 hi and lo
-//               and store them into a tensor-memory A stage (tcgen05.st);
+//               lane quarter, 32 inputs each) into bf16 hi and -lo and store
+//               them into a tensor-memory A stage (tcgen05.st);
 //   warp 12     allocates tensor memory and issues tcgen05.mma (A from tensor
 //               memory, B from shared memory) into one of two fp32
 //               accumulators, releasing stages with tcgen05.commit;
@@ -60,13 +63,14 @@ constexpr int kMaxRowsX = 128;        // activation rows (MMA N <= 128)
 constexpr int kGroup = 64;            // inputs per quantisation group = one stage
 constexpr int kWBoxWords = 32;        // packed words per weight box row (128 B)
 constexpr int kGroupsPerWBox = kWBoxWords * 8 / kGroup;  // 4
-constexpr int kXStages = 6;           // activation ring
-constexpr int kWStages = 3;           // packed-weight ring
+constexpr int kXStages = 9;           // activation ring: covers the L2 latency
+constexpr int kWStages = 4;           // packed-weight ring
 constexpr int kAStages = 4;           // tensor-memory A stages
 constexpr int kEpiWarps = 4, kDeqWarps = 8;
 constexpr int kMmaWarp = kEpiWarps + kDeqWarps;  // 12
-constexpr int kTmaWarp = kMmaWarp + 1;           // 13
-constexpr int kWideThreads = (kTmaWarp + 1) * 32;  // 448
+constexpr int kWTmaWarp = kMmaWarp + 1;          // 13
+constexpr int kXTmaWarp = kWTmaWarp + 1;         // 14
+constexpr int kWideThreads = (kXTmaWarp + 1) * 32;  // 480
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCols = 128;                   // one accumulator
 constexpr uint32_t kAColBase = 2 * kDCols;         // A stages after the two accumulators
@@ -195,6 +199,32 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n) {
          | ((uint32_t)(kTileRows >> 4) << 24);  // M / 16
 }
 
+// Warp-uniform wait: one non-blocking test first (a blocking test costs more
+// even when the phase is already complete), then the bounded wait.
+__device__ __forceinline__ bool mbar_test_u32(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// One lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+__device__ __forceinline__ bool warp_wait_fast(uint32_t bar, uint32_t parity) {
+  if (__all_sync(0xffffffffu, mbar_test_u32(bar, parity))) return true;
+  return qmv::warp_wait_stage(bar, parity);
+}
+
 // ---- bf16x2 arithmetic (each a single rounding) ------------------------------
 __device__ __forceinline__ uint32_t bf2_sub(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -232,11 +262,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 }
 
 // Eight nibbles (inputs 8 w .. 8 w + 7 of the row, LSB first) -> four bf16x2
-// pairs of s q in natural input order, split as hi = rn(s q) and lo = s q - hi
-// (exact).  A pair (q_2p, q_2p+1) is widened to bf16 (128 + q) by placing byte
-// p of the word and of the word shifted by one nibble in the two halves.
-__device__ __forceinline__ void widen_word(uint32_t wd, uint32_t s2, uint32_t *hi,
-                                           uint32_t *lo) {
+// pairs of s q in natural input order, split as hi = rn(s q) and
+// nlo = hi - s q = -(s q - hi) (exact; the MMA of the lo part negates A).  A
+// pair (q_2p, q_2p+1) is widened to bf16 (128 + q) by placing byte p of the
+// word and of the word shifted by one nibble in the two halves.
+__device__ __forceinline__ void widen_word(uint32_t wd, uint32_t s2, uint32_t ns2, uint32_t *hi,
+                                           uint32_t *nlo) {
   const uint32_t t = wd >> 4;
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
@@ -245,7 +276,7 @@ __device__ __forceinline__ void widen_word(uint32_t wd, uint32_t s2, uint32_t *h
     const uint32_t q2 = bf2_sub(v, qmv::kBf16Base);  // (q, q') exactly
     const uint32_t h = bf2_mul(s2, q2);
     hi[p] = h;
-    lo[p] = bf2_fma(s2, q2, h ^ 0x80008000u);       // s q - hi, exact
+    nlo[p] = bf2_fma(ns2, q2, h);  // hi - s q, exact
   }
 }
 
@@ -341,34 +372,44 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const uint32_t tmem = *slot;
   pdl_launch_dependents();
 
-  if (warp == kTmaWarp) {
-    // ------------------------------ producer ------------------------------
+  if (warp == kWTmaWarp) {
+    // --------------------------- weight producer --------------------------
+    // weights do not depend on earlier kernels: no griddepcontrol.wait here
     if (lane == 0) {
       const uint64_t wpol = l2_policy_evict_first();
-      long long i = 0, ib = 0;
-      bool ok = true, waited = false;
+      long long ib = 0;
+      bool ok = true;
       for (int t = 0; ok && t < n_local; ++t) {
         const int n0 = ((int)blockIdx.x + t * (int)gridDim.x) * kTileRows;
+        for (int j = 0; j < a.G; j += kGroupsPerWBox, ++ib) {
+          const int sw = (int)(ib % kWStages);
+          if (ib >= kWStages &&
+              !mbar_wait_u32(w_empty + 8u * sw, (uint32_t)((ib / kWStages - 1) & 1))) {
+            atomicOr(&g_wide_device_error, 1u);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx_u32(w_full + 8u * sw, kWBoxBytes);
+          tma_load_2d(ws0 + sw * kWBoxBytes, &wmap, j * 8, n0, w_full + 8u * sw, wpol);
+        }
+      }
+      // every copy issued has landed before the CTA may exit (normally the
+      // consumers have waited for all of them already)
+      for (long long k = std::max(0ll, ib - kWStages); k < ib; ++k)
+        (void)mbar_wait_u32(w_full + 8u * (uint32_t)(k % kWStages),
+                            (uint32_t)((k / kWStages) & 1));
+    }
+    __syncwarp();
+  } else if (warp == kXTmaWarp) {
+    // ------------------------- activation producer ------------------------
+    if (lane == 0) {
+      pdl_wait();  // the activations and their group sums are earlier kernels' output
+      long long i = 0;
+      uint32_t sx = 0, px = 0;  // slot and phase of stage i
+      bool ok = true;
+      for (int t = 0; ok && t < n_local; ++t) {
         for (int j = 0; j < Gt; ++j, ++i) {
-          if (j < a.G && j % kGroupsPerWBox == 0) {
-            const int sw = (int)(ib % kWStages);
-            if (ib >= kWStages &&
-                !mbar_wait_u32(w_empty + 8u * sw, (uint32_t)((ib / kWStages - 1) & 1))) {
-              atomicOr(&g_wide_device_error, 1u);
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx_u32(w_full + 8u * sw, kWBoxBytes);
-            tma_load_2d(ws0 + sw * kWBoxBytes, &wmap, j * 8, n0, w_full + 8u * sw, wpol);
-            ++ib;
-          }
-          if (!waited) {  // the activations are the preceding kernels' output
-            pdl_wait();
-            waited = true;
-          }
-          const int sx = (int)(i % kXStages);
-          if (i >= kXStages &&
-              !mbar_wait_u32(x_empty + 8u * sx, (uint32_t)((i / kXStages - 1) & 1))) {
+          if (i >= kXStages && !mbar_wait_u32(x_empty + 8u * sx, px ^ 1u)) {
             atomicOr(&g_wide_device_error, 2u);
             ok = false;
             break;
@@ -379,64 +420,88 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           else
             tma_load_2d_keep(xs0 + sx * kXStageBytes, &xbmap, (j - a.G) * kGroup, 0,
                              x_full + 8u * sx);
+          if (++sx == (uint32_t)kXStages) {
+            sx = 0;
+            px ^= 1u;
+          }
         }
       }
-      // every copy issued has landed before the CTA may exit (normally the
-      // consumers have waited for all of them already)
       for (long long k = std::max(0ll, i - kXStages); k < i; ++k)
         (void)mbar_wait_u32(x_full + 8u * (uint32_t)(k % kXStages),
                             (uint32_t)((k / kXStages) & 1));
-      for (long long k = std::max(0ll, ib - kWStages); k < ib; ++k)
-        (void)mbar_wait_u32(w_full + 8u * (uint32_t)(k % kWStages),
-                            (uint32_t)((k / kWStages) & 1));
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ----------------------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(a.n_mma);
-      long long i = 0;
-      bool ok = true;
-      for (int t = 0; ok && t < n_local; ++t) {
-        const int tb = t & 1;
-        if (t >= 2 && !mbar_wait_u32(d_empty + 8u * tb, (uint32_t)(((t >> 1) - 1) & 1))) {
-          atomicOr(&g_wide_device_error, 4u);
+    // The whole warp runs the loop (descriptors and addresses stay
+    // warp-uniform); one elected lane issues each MMA and commit.
+    const uint32_t idesc = idesc_bf16(a.n_mma);
+    const uint32_t idesc_neg = idesc | (1u << 13);  // negate A: the stored lo parts are -lo
+    uint32_t sa = 0, pa = 0, sx = 0, px = 0;        // slot and phase of the next stage
+    bool ok = true;
+    for (int t = 0; ok && t < n_local; ++t) {
+      const int tb = t & 1;
+      if (t >= 2 &&
+          !qmv::warp_wait_stage(d_empty + 8u * tb, (uint32_t)(((t >> 1) - 1) & 1))) {
+        if (lane == 0) atomicOr(&g_wide_device_error, 4u);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)tb * kDCols;
+      for (int j = 0; j < Gt; ++j) {
+        if (!qmv::warp_wait_stage(a_full + 8u * sa, pa) ||
+            !qmv::warp_wait_stage(x_full + 8u * sx, px)) {
+          if (lane == 0) atomicOr(&g_wide_device_error, 8u);
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)tb * kDCols;
-        for (int j = 0; j < Gt; ++j, ++i) {
-          const int sa = (int)(i % kAStages), sx = (int)(i % kXStages);
-          if (!mbar_wait_u32(a_full + 8u * sa, (uint32_t)((i / kAStages) & 1)) ||
-              !mbar_wait_u32(x_full + 8u * sx, (uint32_t)((i / kXStages) & 1))) {
-            atomicOr(&g_wide_device_error, 8u);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t at = tmem + kAColBase + (uint32_t)sa * kAStageCols;
-          const uint64_t bd = smem_desc_sw128(xs0 + (uint32_t)sx * kXStageBytes);
+        const uint32_t at = tmem + kAColBase + sa * kAStageCols;
+        const uint64_t bd = smem_desc_sw128(xs0 + sx * kXStageBytes);
+        if (elect_one()) {
+          if (j < a.G) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            tc_mma_ts(d, at + 8u * ks, bd + 2u * ks, idesc, (j > 0 || ks > 0) ? 1u : 0u);
-            if (j < a.G) tc_mma_ts(d, at + 32u + 8u * ks, bd + 2u * ks, idesc, 1u);
+            for (int ks = 0; ks < 4; ++ks) {
+              tc_mma_ts(d, at + 8u * ks, bd + 2u * ks, idesc, (j > 0 || ks > 0) ? 1u : 0u);
+              tc_mma_ts(d, at + 32u + 8u * ks, bd + 2u * ks, idesc_neg, 1u);
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc_mma_ts(d, at + 8u * ks, bd + 2u * ks, idesc, 1u);
           }
           tc_commit(a_empty + 8u * sa);
           tc_commit(x_empty + 8u * sx);
         }
-        if (ok) tc_commit(d_full + 8u * tb);
+        __syncwarp();
+        if (++sa == (uint32_t)kAStages) {
+          sa = 0;
+          pa ^= 1u;
+        }
+        if (++sx == (uint32_t)kXStages) {
+          sx = 0;
+          px ^= 1u;
+        }
       }
-      // every MMA issued has completed before the tensor memory is freed
+      if (ok && elect_one()) tc_commit(d_full + 8u * tb);
+      __syncwarp();
+    }
+    // every MMA issued has completed before the tensor memory is freed
+    if (elect_one()) {
       tc_commit(mma_done);
       (void)mbar_wait_u32(mma_done, 0);
     }
     __syncwarp();
   } else if (warp >= kEpiWarps) {
     // ------------------------------ widening ------------------------------
+    // two warps per TMEM lane quarter, each one half (32 inputs) of a group of
+    // its 32 rows; weight groups go two at a time (the waits, the store
+    // completion and the loop cost once per pair, the two groups' math
+    // interleaved), the bias stages one at a time
     const int qd = warp & 3, hf = (warp - kEpiWarps) >> 2;
     const int r = qd * 32 + lane;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const uint32_t arow = tmem + lane_base + kAColBase;
     long long i = 0, ib = 0;
     bool ok = true;
     for (int t = 0; ok && t < n_local; ++t) {
@@ -446,59 +511,86 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const uint16_t *brow = a.b + (size_t)(valid ? n : 0) * a.G;
       uint4 scur = make_uint4(0, 0, 0, 0), snext = make_uint4(0, 0, 0, 0);
       if (valid) snext = __ldg(reinterpret_cast<const uint4 *>(srow));
-      for (int j = 0; j < Gt; ++j, ++i) {
-        const int sa = (int)(i % kAStages);
-        if (j < a.G && (j & 7) == 0) {
+      for (int j = 0; j < a.G; j += 2, i += 2) {
+        const int sa0 = (int)(i % kAStages), sa1 = (int)((i + 1) % kAStages);
+        if ((j & 7) == 0) {
           scur = snext;
           if (valid && j + 8 < a.G) snext = __ldg(reinterpret_cast<const uint4 *>(srow + j + 8));
         }
+        // both A slots free: the MMAs of stages i - 4 and i - 3 have completed
+        if ((i >= kAStages &&
+             !warp_wait_fast(a_empty + 8u * sa0, (uint32_t)((i / kAStages - 1) & 1))) ||
+            (i + 1 >= kAStages &&
+             !warp_wait_fast(a_empty + 8u * sa1, (uint32_t)(((i + 1) / kAStages - 1) & 1)))) {
+          if (lane == 0) atomicOr(&g_wide_device_error, 16u);
+          ok = false;
+          break;
+        }
+        const int sw = (int)(ib % kWStages);
+        if ((j & 3) == 0 &&
+            !warp_wait_fast(w_full + 8u * sw, (uint32_t)((ib / kWStages) & 1))) {
+          if (lane == 0) atomicOr(&g_wide_device_error, 32u);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // 16-byte chunks 2 (j % 4) + hf and 2 (j % 4 + 1) + hf of the box row
+        const uint32_t rbase = ws0 + (uint32_t)sw * kWBoxBytes + (uint32_t)r * 128u;
+        const int c0 = 2 * (j & 3) + hf, c1 = c0 + 2;
+        const uint4 w0 = lds128(rbase + ((uint32_t)(c0 ^ (r & 7)) << 4));
+        const uint4 w1 = lds128(rbase + ((uint32_t)(c1 ^ (r & 7)) << 4));
+        const uint32_t sword = (j & 4) ? ((j & 2) ? scur.w : scur.z) : ((j & 2) ? scur.y : scur.x);
+        const uint32_t s0 = prmt(sword, 0u, 0x1010u), s1 = prmt(sword, 0u, 0x3232u);
+        const uint32_t ns0 = s0 ^ 0x80008000u, ns1 = s1 ^ 0x80008000u;
+        uint32_t hi0[16], nlo0[16], hi1[16], nlo1[16];
+        widen_word(w0.x, s0, ns0, hi0 + 0, nlo0 + 0);
+        widen_word(w1.x, s1, ns1, hi1 + 0, nlo1 + 0);
+        widen_word(w0.y, s0, ns0, hi0 + 4, nlo0 + 4);
+        widen_word(w1.y, s1, ns1, hi1 + 4, nlo1 + 4);
+        widen_word(w0.z, s0, ns0, hi0 + 8, nlo0 + 8);
+        widen_word(w1.z, s1, ns1, hi1 + 8, nlo1 + 8);
+        widen_word(w0.w, s0, ns0, hi0 + 12, nlo0 + 12);
+        widen_word(w1.w, s1, ns1, hi1 + 12, nlo1 + 12);
+        if ((j & 3) == 2) {  // the box's last pair: its rows are read
+          __syncwarp();
+          if (lane == 0) mbar_arrive_u32(w_empty + 8u * sw);
+          ++ib;
+        }
+        const uint32_t col0 = arow + (uint32_t)sa0 * kAStageCols + 16u * hf;
+        const uint32_t col1 = arow + (uint32_t)sa1 * kAStageCols + 16u * hf;
+        tc_st_x16(col0, hi0);
+        tc_st_x16(col0 + 32u, nlo0);
+        tc_st_x16(col1, hi1);
+        tc_st_x16(col1 + 32u, nlo1);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_u32(a_full + 8u * sa0);
+          mbar_arrive_u32(a_full + 8u * sa1);
+        }
+      }
+      // bias columns k' = 64 e + 32 hf + 2 p (+1): b[n][k' mod G] below 2 G
+      for (int e = 0; ok && e < a.E; ++e, ++i) {
+        const int sa = (int)(i % kAStages);
+        uint32_t hi[16];
+        const int kb = 64 * e + 32 * hf;
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {
+          const int kp = kb + 2 * p;
+          uint32_t v = 0;
+          if (valid && kp < 2 * a.G)
+            v = __ldg(reinterpret_cast<const uint32_t *>(brow + (kp < a.G ? kp : kp - a.G)));
+          hi[p] = v;
+        }
         if (i >= kAStages &&
-            !qmv::warp_wait_stage(a_empty + 8u * sa, (uint32_t)((i / kAStages - 1) & 1))) {
+            !warp_wait_fast(a_empty + 8u * sa, (uint32_t)((i / kAStages - 1) & 1))) {
           if (lane == 0) atomicOr(&g_wide_device_error, 16u);
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t hi[16], lo[16];
-        const uint32_t acol = tmem + lane_base + kAColBase + (uint32_t)sa * kAStageCols;
-        if (j < a.G) {
-          const int sw = (int)(ib % kWStages);
-          if ((j & 3) == 0 &&
-              !qmv::warp_wait_stage(w_full + 8u * sw, (uint32_t)((ib / kWStages) & 1))) {
-            if (lane == 0) atomicOr(&g_wide_device_error, 32u);
-            ok = false;
-            break;
-          }
-          const int c = 2 * (j & 3) + hf;  // 16-byte chunk of the 128-byte box row
-          const uint4 wv =
-              lds128(ws0 + (uint32_t)sw * kWBoxBytes + (uint32_t)r * 128u +
-                     ((uint32_t)(c ^ (r & 7)) << 4));
-          const uint32_t sw2 = (j & 4) ? ((j & 2) ? scur.w : scur.z) : ((j & 2) ? scur.y : scur.x);
-          const uint32_t s2 = prmt(sw2, 0u, (j & 1) ? 0x3232u : 0x1010u);
-          widen_word(wv.x, s2, hi + 0, lo + 0);
-          widen_word(wv.y, s2, hi + 4, lo + 4);
-          widen_word(wv.z, s2, hi + 8, lo + 8);
-          widen_word(wv.w, s2, hi + 12, lo + 12);
-          if ((j & 3) == 3) {  // the box's last group: its rows are read
-            __syncwarp();
-            if (lane == 0) mbar_arrive_u32(w_empty + 8u * sw);
-            ++ib;
-          }
-          tc_st_x16(acol + 16u * hf, hi);
-          tc_st_x16(acol + 32u + 16u * hf, lo);
-        } else {
-          // bias columns k' = 64 e + 32 hf + 2 p (+1): b[n][k' mod G] below 2 G
-          const int kb = 64 * (j - a.G) + 32 * hf;
-#pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            const int kp = kb + 2 * p;
-            uint32_t v = 0;
-            if (valid && kp < 2 * a.G)
-              v = __ldg(reinterpret_cast<const uint32_t *>(brow + (kp < a.G ? kp : kp - a.G)));
-            hi[p] = v;
-          }
-          tc_st_x16(acol + 16u * hf, hi);
-        }
+        tc_st_x16(arow + (uint32_t)sa * kAStageCols + 16u * hf, hi);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
