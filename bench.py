@@ -75,6 +75,13 @@ PLAN_TRAFFIC_RATIO = 1.292094 / 1.283004
 E_DRAWS = 16  # seeded draft/uniform draws the end-to-end steps rotate through
 
 
+def wide_bias_columns(K: int) -> int:
+    """Extra MMA input columns qmv_wide spends on the bias term: the split
+    group sums (2 K/64 columns) padded to whole two-group stages."""
+    groups = -(-2 * (K // GROUP) // 64)
+    return 64 * (-(-groups // 2) * 2)
+
+
 def qmv_bytes(M: int, N: int, K: int) -> int:
     """Algorithmic bytes of one qmv_smallm call: packed nibbles, bf16 scales
     and biases, bf16 rows in, fp32 rows out."""
@@ -879,7 +886,7 @@ def run_wide(args):
     peaks = measured_peaks()
     tflops = 2 * M * N * K / (us / 1e6) / 1e12
     n_mma = -(-M // 16) * 16
-    issued = 2 * n_mma * N * (2 * K + 64 * (-(-2 * (K // GROUP) // 64))) / (us / 1e6) / 1e12
+    issued = 2 * n_mma * N * (2 * K + wide_bias_columns(K)) / (us / 1e6) / 1e12
     line = {"metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -1048,7 +1055,7 @@ def run_lmhead(args):
                              "gbs": qmv_bytes(B * M, V, H) / (lms / 1e3 / args.steps) / 1e9,
                              "tflops": 2 * B * M * V * H / (lms / 1e3 / args.steps) / 1e12,
                              "tensor_tflops_issued":
-                                 2 * B * M * V * (2 * H + 64 * ((2 * (H // 64) + 63) // 64))
+                                 2 * B * M * V * (2 * H + wide_bias_columns(H))
                                  / (lms / 1e3 / args.steps) / 1e12},
             "per_sequence_plan": {"sequence_cycles_per_s": B / (ms_plan / 1e3 / args.steps),
                                   "ms_per_step": ms_plan / args.steps,

@@ -60,12 +60,13 @@ using qmv::tma_load_2d;
 
 constexpr int kTileRows = 128;        // weight rows per tile (MMA M)
 constexpr int kMaxRowsX = 128;        // activation rows (MMA N <= 128)
-constexpr int kGroup = 64;            // inputs per quantisation group = one stage
+constexpr int kGroup = 64;            // inputs per quantisation group
+constexpr int kStageGroups = 2;       // groups per pipeline stage
 constexpr int kWBoxWords = 32;        // packed words per weight box row (128 B)
 constexpr int kGroupsPerWBox = kWBoxWords * 8 / kGroup;  // 4
-constexpr int kXStages = 9;           // activation ring: covers the L2 latency
-constexpr int kWStages = 4;           // packed-weight ring
-constexpr int kAStages = 4;           // tensor-memory A stages
+constexpr int kXStages = 4;           // activation ring (8 groups): covers the L2 latency
+constexpr int kWStages = 4;           // packed-weight ring (16 groups)
+constexpr int kAStages = 2;           // tensor-memory A stages (4 groups)
 constexpr int kEpiWarps = 4, kDeqWarps = 8;
 constexpr int kMmaWarp = kEpiWarps + kDeqWarps;  // 12
 constexpr int kWTmaWarp = kMmaWarp + 1;          // 13
@@ -74,12 +75,15 @@ constexpr int kWideThreads = (kXTmaWarp + 1) * 32;  // 480
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCols = 128;                   // one accumulator
 constexpr uint32_t kAColBase = 2 * kDCols;         // A stages after the two accumulators
-constexpr uint32_t kAStageCols = 64;               // hi 32 + lo 32 columns
+constexpr uint32_t kAGroupCols = 64;               // per group: hi 32 + (-lo) 32 columns
+constexpr uint32_t kAStageCols = kStageGroups * kAGroupCols;
 constexpr uint32_t kWBoxBytes = kTileRows * 128;   // 16 KB
-constexpr uint32_t kXStageBytes = kMaxRowsX * 128; // 16 KB at 128 rows
+constexpr uint32_t kXGroupBytes = kMaxRowsX * 128; // 16 KB at 128 rows
+constexpr uint32_t kXStageBytes = kStageGroups * kXGroupBytes;
 constexpr int kPrepThreads = 256;
 
 static_assert(kAColBase + kAStages * kAStageCols <= kTmemCols, "tensor memory budget");
+static_assert(kGroupsPerWBox % kStageGroups == 0, "a weight box holds whole stages");
 
 __device__ unsigned int g_wide_device_error;
 
@@ -104,8 +108,8 @@ struct WideArgs {
   const uint16_t *s, *b;  // [N][G] bf16 scales, biases
   float *y;               // [M][N]
   int M, N, K;
-  int G;                  // K / 64 groups
-  int E;                  // bias stages: ceil(2 G / 64)
+  int G;                  // K / 64 groups (a multiple of 8)
+  int E;                  // bias groups: ceil(2 G / 64), rounded up to even
   int n_mma;              // MMA N: M rounded up to 16
 };
 
@@ -316,10 +320,9 @@ __global__ void __launch_bounds__(kPrepThreads) wide_xsum_kernel(const uint16_t 
   }
 }
 
-// Stages of a tile: j < G are the weight groups, G <= j < G + E the bias
-// columns.  Ring positions follow one running stage count per role, so every
-// role walks the same sequence: stage i uses X/A slot i % k*Stages in phase
-// (i / k*Stages) & 1; weight box ib (four groups) uses W slot ib % kWStages.
+// Stages of a tile: two groups each; stage p < G / 2 holds weight groups
+// 2p, 2p + 1, the last E / 2 stages the bias columns.  Every role walks the
+// same sequence of stages; ring slots and phases advance incrementally.
 __global__ void __launch_bounds__(kWideThreads, 1)
     qmv_wide_kernel(const __grid_constant__ CUtensorMap wmap,
                     const __grid_constant__ CUtensorMap xmap,
@@ -340,7 +343,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const int tiles = (a.N + kTileRows - 1) / kTileRows;
   const int n_local =
       (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const int Gt = a.G + a.E;
+  const int Pw = a.G / kStageGroups;             // weight stages per tile
+  const int Pt = Pw + a.E / kStageGroups;        // all stages per tile
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kXStages; ++i) {
@@ -378,19 +382,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (lane == 0) {
       const uint64_t wpol = l2_policy_evict_first();
       long long ib = 0;
+      uint32_t sw = 0, pw = 0;  // slot and phase of box ib
       bool ok = true;
       for (int t = 0; ok && t < n_local; ++t) {
         const int n0 = ((int)blockIdx.x + t * (int)gridDim.x) * kTileRows;
         for (int j = 0; j < a.G; j += kGroupsPerWBox, ++ib) {
-          const int sw = (int)(ib % kWStages);
-          if (ib >= kWStages &&
-              !mbar_wait_u32(w_empty + 8u * sw, (uint32_t)((ib / kWStages - 1) & 1))) {
+          if (ib >= kWStages && !mbar_wait_u32(w_empty + 8u * sw, pw ^ 1u)) {
             atomicOr(&g_wide_device_error, 1u);
             ok = false;
             break;
           }
           mbar_arrive_expect_tx_u32(w_full + 8u * sw, kWBoxBytes);
           tma_load_2d(ws0 + sw * kWBoxBytes, &wmap, j * 8, n0, w_full + 8u * sw, wpol);
+          if (++sw == (uint32_t)kWStages) {
+            sw = 0;
+            pw ^= 1u;
+          }
         }
       }
       // every copy issued has landed before the CTA may exit (normally the
@@ -407,19 +414,24 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       long long i = 0;
       uint32_t sx = 0, px = 0;  // slot and phase of stage i
       bool ok = true;
+      const uint32_t bytes = (uint32_t)kStageGroups * (uint32_t)a.n_mma * 128u;
       for (int t = 0; ok && t < n_local; ++t) {
-        for (int j = 0; j < Gt; ++j, ++i) {
+        for (int p = 0; p < Pt; ++p, ++i) {
           if (i >= kXStages && !mbar_wait_u32(x_empty + 8u * sx, px ^ 1u)) {
             atomicOr(&g_wide_device_error, 2u);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx_u32(x_full + 8u * sx, (uint32_t)a.n_mma * 128u);
-          if (j < a.G)
-            tma_load_2d_keep(xs0 + sx * kXStageBytes, &xmap, j * kGroup, 0, x_full + 8u * sx);
-          else
-            tma_load_2d_keep(xs0 + sx * kXStageBytes, &xbmap, (j - a.G) * kGroup, 0,
-                             x_full + 8u * sx);
+          mbar_arrive_expect_tx_u32(x_full + 8u * sx, bytes);
+          const uint32_t dst = xs0 + sx * kXStageBytes;
+          for (int g2 = 0; g2 < kStageGroups; ++g2) {
+            if (p < Pw)
+              tma_load_2d_keep(dst + g2 * kXGroupBytes, &xmap, (kStageGroups * p + g2) * kGroup,
+                               0, x_full + 8u * sx);
+            else
+              tma_load_2d_keep(dst + g2 * kXGroupBytes, &xbmap,
+                               (kStageGroups * (p - Pw) + g2) * kGroup, 0, x_full + 8u * sx);
+          }
           if (++sx == (uint32_t)kXStages) {
             sx = 0;
             px ^= 1u;
@@ -449,7 +461,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       }
       tc_fence_after();
       const uint32_t d = tmem + (uint32_t)tb * kDCols;
-      for (int j = 0; j < Gt; ++j) {
+      for (int p = 0; p < Pt; ++p) {
         if (!qmv::warp_wait_stage(a_full + 8u * sa, pa) ||
             !qmv::warp_wait_stage(x_full + 8u * sx, px)) {
           if (lane == 0) atomicOr(&g_wide_device_error, 8u);
@@ -458,17 +470,23 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         }
         tc_fence_after();
         const uint32_t at = tmem + kAColBase + sa * kAStageCols;
-        const uint64_t bd = smem_desc_sw128(xs0 + sx * kXStageBytes);
+        const uint32_t xb = xs0 + sx * kXStageBytes;
         if (elect_one()) {
-          if (j < a.G) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              tc_mma_ts(d, at + 8u * ks, bd + 2u * ks, idesc, (j > 0 || ks > 0) ? 1u : 0u);
-              tc_mma_ts(d, at + 32u + 8u * ks, bd + 2u * ks, idesc_neg, 1u);
+          for (int g2 = 0; g2 < kStageGroups; ++g2) {
+            const uint32_t ag = at + (uint32_t)g2 * kAGroupCols;
+            const uint64_t bd = smem_desc_sw128(xb + (uint32_t)g2 * kXGroupBytes);
+            if (p < Pw) {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                tc_mma_ts(d, ag + 8u * ks, bd + 2u * ks, idesc,
+                          (p > 0 || g2 > 0 || ks > 0) ? 1u : 0u);
+                tc_mma_ts(d, ag + 32u + 8u * ks, bd + 2u * ks, idesc_neg, 1u);
+              }
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) tc_mma_ts(d, ag + 8u * ks, bd + 2u * ks, idesc, 1u);
             }
-          } else {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) tc_mma_ts(d, at + 8u * ks, bd + 2u * ks, idesc, 1u);
           }
           tc_commit(a_empty + 8u * sa);
           tc_commit(x_empty + 8u * sx);
@@ -494,15 +512,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     __syncwarp();
   } else if (warp >= kEpiWarps) {
     // ------------------------------ widening ------------------------------
-    // two warps per TMEM lane quarter, each one half (32 inputs) of a group of
-    // its 32 rows; weight groups go two at a time (the waits, the store
-    // completion and the loop cost once per pair, the two groups' math
-    // interleaved), the bias stages one at a time
+    // two warps per TMEM lane quarter, each one half (32 inputs) of every
+    // group of its 32 rows; a stage's two groups are widened together (their
+    // math interleaved)
     const int qd = warp & 3, hf = (warp - kEpiWarps) >> 2;
     const int r = qd * 32 + lane;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-    const uint32_t arow = tmem + lane_base + kAColBase;
-    long long i = 0, ib = 0;
+    const uint32_t arow = tmem + lane_base + kAColBase + 16u * (uint32_t)hf;
+    long long i = 0;
+    uint32_t sa = 0, pa = 0, sw = 0, pw = 0;  // A slot/phase of stage i, W slot/phase
     bool ok = true;
     for (int t = 0; ok && t < n_local; ++t) {
       const int n = ((int)blockIdx.x + t * (int)gridDim.x) * kTileRows + r;
@@ -511,90 +529,85 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const uint16_t *brow = a.b + (size_t)(valid ? n : 0) * a.G;
       uint4 scur = make_uint4(0, 0, 0, 0), snext = make_uint4(0, 0, 0, 0);
       if (valid) snext = __ldg(reinterpret_cast<const uint4 *>(srow));
-      for (int j = 0; j < a.G; j += 2, i += 2) {
-        const int sa0 = (int)(i % kAStages), sa1 = (int)((i + 1) % kAStages);
-        if ((j & 7) == 0) {
-          scur = snext;
-          if (valid && j + 8 < a.G) snext = __ldg(reinterpret_cast<const uint4 *>(srow + j + 8));
-        }
-        // both A slots free: the MMAs of stages i - 4 and i - 3 have completed
-        if ((i >= kAStages &&
-             !warp_wait_fast(a_empty + 8u * sa0, (uint32_t)((i / kAStages - 1) & 1))) ||
-            (i + 1 >= kAStages &&
-             !warp_wait_fast(a_empty + 8u * sa1, (uint32_t)(((i + 1) / kAStages - 1) & 1)))) {
-          if (lane == 0) atomicOr(&g_wide_device_error, 16u);
-          ok = false;
-          break;
-        }
-        const int sw = (int)(ib % kWStages);
-        if ((j & 3) == 0 &&
-            !warp_wait_fast(w_full + 8u * sw, (uint32_t)((ib / kWStages) & 1))) {
-          if (lane == 0) atomicOr(&g_wide_device_error, 32u);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // 16-byte chunks 2 (j % 4) + hf and 2 (j % 4 + 1) + hf of the box row
-        const uint32_t rbase = ws0 + (uint32_t)sw * kWBoxBytes + (uint32_t)r * 128u;
-        const int c0 = 2 * (j & 3) + hf, c1 = c0 + 2;
-        const uint4 w0 = lds128(rbase + ((uint32_t)(c0 ^ (r & 7)) << 4));
-        const uint4 w1 = lds128(rbase + ((uint32_t)(c1 ^ (r & 7)) << 4));
-        const uint32_t sword = (j & 4) ? ((j & 2) ? scur.w : scur.z) : ((j & 2) ? scur.y : scur.x);
-        const uint32_t s0 = prmt(sword, 0u, 0x1010u), s1 = prmt(sword, 0u, 0x3232u);
-        const uint32_t ns0 = s0 ^ 0x80008000u, ns1 = s1 ^ 0x80008000u;
+      for (int p = 0; p < Pt; ++p, ++i) {
+        const int j = kStageGroups * p;  // first group of the stage
         uint32_t hi0[16], nlo0[16], hi1[16], nlo1[16];
-        widen_word(w0.x, s0, ns0, hi0 + 0, nlo0 + 0);
-        widen_word(w1.x, s1, ns1, hi1 + 0, nlo1 + 0);
-        widen_word(w0.y, s0, ns0, hi0 + 4, nlo0 + 4);
-        widen_word(w1.y, s1, ns1, hi1 + 4, nlo1 + 4);
-        widen_word(w0.z, s0, ns0, hi0 + 8, nlo0 + 8);
-        widen_word(w1.z, s1, ns1, hi1 + 8, nlo1 + 8);
-        widen_word(w0.w, s0, ns0, hi0 + 12, nlo0 + 12);
-        widen_word(w1.w, s1, ns1, hi1 + 12, nlo1 + 12);
-        if ((j & 3) == 2) {  // the box's last pair: its rows are read
-          __syncwarp();
-          if (lane == 0) mbar_arrive_u32(w_empty + 8u * sw);
-          ++ib;
-        }
-        const uint32_t col0 = arow + (uint32_t)sa0 * kAStageCols + 16u * hf;
-        const uint32_t col1 = arow + (uint32_t)sa1 * kAStageCols + 16u * hf;
-        tc_st_x16(col0, hi0);
-        tc_st_x16(col0 + 32u, nlo0);
-        tc_st_x16(col1, hi1);
-        tc_st_x16(col1 + 32u, nlo1);
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_u32(a_full + 8u * sa0);
-          mbar_arrive_u32(a_full + 8u * sa1);
-        }
-      }
-      // bias columns k' = 64 e + 32 hf + 2 p (+1): b[n][k' mod G] below 2 G
-      for (int e = 0; ok && e < a.E; ++e, ++i) {
-        const int sa = (int)(i % kAStages);
-        uint32_t hi[16];
-        const int kb = 64 * e + 32 * hf;
+        if (p < Pw) {
+          if ((j & 7) == 0) {
+            scur = snext;
+            if (valid && j + 8 < a.G)
+              snext = __ldg(reinterpret_cast<const uint4 *>(srow + j + 8));
+          }
+        } else {
+          // bias columns k' = 64 e + 32 hf + 2 q (+1): b[n][k' mod G] below 2 G
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-          const int kp = kb + 2 * p;
-          uint32_t v = 0;
-          if (valid && kp < 2 * a.G)
-            v = __ldg(reinterpret_cast<const uint32_t *>(brow + (kp < a.G ? kp : kp - a.G)));
-          hi[p] = v;
+          for (int g2 = 0; g2 < kStageGroups; ++g2) {
+            const int kb = kGroup * (j - a.G + g2) + 32 * hf;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const int kp = kb + 2 * q;
+              uint32_t v = 0;
+              if (valid && kp < 2 * a.G)
+                v = __ldg(reinterpret_cast<const uint32_t *>(brow + (kp < a.G ? kp : kp - a.G)));
+              (g2 == 0 ? hi0 : hi1)[q] = v;
+            }
+          }
         }
-        if (i >= kAStages &&
-            !warp_wait_fast(a_empty + 8u * sa, (uint32_t)((i / kAStages - 1) & 1))) {
+        if (i >= kAStages && !warp_wait_fast(a_empty + 8u * sa, pa ^ 1u)) {
           if (lane == 0) atomicOr(&g_wide_device_error, 16u);
           ok = false;
           break;
         }
-        tc_fence_after();
-        tc_st_x16(arow + (uint32_t)sa * kAStageCols + 16u * hf, hi);
+        const uint32_t col = arow + sa * kAStageCols;
+        if (p < Pw) {
+          if ((j & 3) == 0 && !warp_wait_fast(w_full + 8u * sw, pw)) {
+            if (lane == 0) atomicOr(&g_wide_device_error, 32u);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // 16-byte chunks 2 (j % 4) + hf and 2 (j % 4 + 1) + hf of the box row
+          const uint32_t rbase = ws0 + sw * kWBoxBytes + (uint32_t)r * 128u;
+          const int c0 = 2 * (j & 3) + hf, c1 = c0 + 2;
+          const uint4 w0 = lds128(rbase + ((uint32_t)(c0 ^ (r & 7)) << 4));
+          const uint4 w1 = lds128(rbase + ((uint32_t)(c1 ^ (r & 7)) << 4));
+          const uint32_t sword =
+              (j & 4) ? ((j & 2) ? scur.w : scur.z) : ((j & 2) ? scur.y : scur.x);
+          const uint32_t s0 = prmt(sword, 0u, 0x1010u), s1 = prmt(sword, 0u, 0x3232u);
+          const uint32_t ns0 = s0 ^ 0x80008000u, ns1 = s1 ^ 0x80008000u;
+          widen_word(w0.x, s0, ns0, hi0 + 0, nlo0 + 0);
+          widen_word(w1.x, s1, ns1, hi1 + 0, nlo1 + 0);
+          widen_word(w0.y, s0, ns0, hi0 + 4, nlo0 + 4);
+          widen_word(w1.y, s1, ns1, hi1 + 4, nlo1 + 4);
+          widen_word(w0.z, s0, ns0, hi0 + 8, nlo0 + 8);
+          widen_word(w1.z, s1, ns1, hi1 + 8, nlo1 + 8);
+          widen_word(w0.w, s0, ns0, hi0 + 12, nlo0 + 12);
+          widen_word(w1.w, s1, ns1, hi1 + 12, nlo1 + 12);
+          if ((j & 3) == 2) {  // the box's last stage: its rows are read
+            __syncwarp();
+            if (lane == 0) mbar_arrive_u32(w_empty + 8u * sw);
+            if (++sw == (uint32_t)kWStages) {
+              sw = 0;
+              pw ^= 1u;
+            }
+          }
+          tc_st_x16(col, hi0);
+          tc_st_x16(col + 32u, nlo0);
+          tc_st_x16(col + kAGroupCols, hi1);
+          tc_st_x16(col + kAGroupCols + 32u, nlo1);
+        } else {
+          tc_fence_after();
+          tc_st_x16(col, hi0);
+          tc_st_x16(col + kAGroupCols, hi1);
+        }
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_u32(a_full + 8u * sa);
+        if (++sa == (uint32_t)kAStages) {
+          sa = 0;
+          pa ^= 1u;
+        }
       }
     }
   } else {
@@ -637,7 +650,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   }
 }
 
-int wide_bias_stages(int K) { return (2 * (K / kGroup) + kGroup - 1) / kGroup; }
+int wide_bias_stages(int K) {
+  const int e = (2 * (K / kGroup) + kGroup - 1) / kGroup;
+  return (e + kStageGroups - 1) / kStageGroups * kStageGroups;
+}
 size_t wide_ws_bytes(int M, int K) {
   const size_t kb = (size_t)wide_bias_stages(K) * kGroup;
   return ((size_t)M * kb * 2 + 255) / 256 * 256;

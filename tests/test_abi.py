@@ -194,9 +194,9 @@ def test_identity_probe_sizes_and_rejects(L):
 
 
 def test_wide_sizes_and_rejects(L):
-    # split group sums: M rows x (2 K/64 rounded up to 64) bf16, 256-byte multiple
-    assert L.qmv_wide_workspace_bytes(128, 5120) == 128 * 192 * 2
-    assert L.qmv_wide_workspace_bytes(3, 512) == 512
+    # split group sums: M rows x (2 K/64 rounded up to 128) bf16, 256-byte multiple
+    assert L.qmv_wide_workspace_bytes(128, 5120) == 128 * 256 * 2
+    assert L.qmv_wide_workspace_bytes(3, 512) == 768
     assert L.qmv_wide_workspace_bytes(129, 512) == 0
     assert L.qmv_wide_workspace_bytes(4, 640) == 0
     w, s, b, x, y, ws = (A + i * 0x1000000 for i in range(6))
