@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
         D = ctypes.c_double
         L.oracle_qmv.argtypes = [P, P, P, P, I, P, I, I, I, I]
         L.oracle_qmv.restype = I
+        L.oracle_requantize.argtypes = [P, I, I, P, P, P]
+        L.oracle_requantize.restype = I
         L.oracle_filter_row.argtypes = [P, I, D, I, D, P, P, P]
         L.oracle_filter_row.restype = I
         L.oracle_spec_accept.argtypes = [P, P, P, P, P, I, I, I, D, I, D, P, P, P, P]
@@ -112,6 +114,21 @@ def qmv(w_packed, scales, biases, x, group_size: int = 64) -> np.ndarray:
     if rc:
         raise ValueError("oracle_qmv rejected the shapes")
     return y
+
+
+def requantize(w_bf16, group_size: int = 64):
+    """4-bit affine group-64 requantisation of a bf16 matrix [N, K] (uint16 bit
+    patterns): returns (w_packed uint32 [N, K/8], scales, biases uint16 bf16
+    bits [N, K/64]) -- the qmv weight layout, min/max affine per group."""
+    assert group_size == 64
+    w = _c(w_bf16, np.uint16)
+    N, K = w.shape
+    wp = np.empty((N, K // 8), np.uint32)
+    s = np.empty((N, K // 64), np.uint16)
+    b = np.empty((N, K // 64), np.uint16)
+    if lib().oracle_requantize(_ptr(w), N, K, _ptr(wp), _ptr(s), _ptr(b)):
+        raise ValueError("oracle_requantize rejected the shapes")
+    return wp, s, b
 
 
 # ----------------------------------------------------------------------------

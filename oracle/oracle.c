@@ -104,6 +104,79 @@ int oracle_qmv(const uint32_t *w_packed, const uint16_t *scales, const uint16_t 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Requantisation of a bf16 weight matrix to the 4-bit affine group format.  */
+/* ------------------------------------------------------------------------ */
+/*
+ * [MTPLX] "Layer 0: MLX Runtime", the draft-only requantised LM head: the
+ * target keeps its LM head at model precision and a separate 4-bit copy is
+ * built in memory for the drafter.  The pages do not print the quantiser;
+ * the reading adopted is the plain min/max affine one, in the qmv layout:
+ *   per group of 64 inputs of a row:  lo = min w, hi = max w
+ *   s = rn_bf16((hi - lo) / 15),  b = lo (a bf16 value already)
+ *   q = 0 if s == 0, else clamp(rint((w - b) / s), 0, 15)
+ * with every step an fp32 operation (subtraction, division, round half to
+ * even): the code is an integer decided by floating point, so the oracle
+ * takes the decision in the precision the product takes it in.
+ */
+static uint16_t bf16_rn_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)(u >> 16); /* inf: no rounding */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb; /* round to nearest, ties to even */
+    return (uint16_t)(u >> 16);
+}
+
+static float bf16_float(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+int oracle_requantize(const uint16_t *w, int N, int K, uint32_t *w_packed, uint16_t *scales,
+                      uint16_t *biases) {
+    if (N < 0 || K <= 0 || K % 64 != 0) return 1;
+    const int groups = K / 64;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(g_threads)
+#endif
+    for (int n = 0; n < N; ++n) {
+        for (int g = 0; g < groups; ++g) {
+            const uint16_t *src = w + (size_t)n * K + (size_t)g * 64;
+            float lo = bf16_float(src[0]), hi = lo;
+            for (int i = 1; i < 64; ++i) {
+                float v = bf16_float(src[i]);
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+            }
+            volatile float range = hi - lo;         /* fp32, one rounding */
+            volatile float step = range / 15.0f;    /* fp32, one rounding */
+            uint16_t s_bits = bf16_rn_bits(step);
+            uint16_t b_bits = bf16_rn_bits(lo);     /* exact: lo is a bf16 value */
+            float s = bf16_float(s_bits), b = bf16_float(b_bits);
+            scales[(size_t)n * groups + g] = s_bits;
+            biases[(size_t)n * groups + g] = b_bits;
+            for (int word = 0; word < 8; ++word) {
+                uint32_t packed = 0;
+                for (int j = 0; j < 8; ++j) {
+                    int q = 0;
+                    if (s != 0.0f) {
+                        volatile float diff = bf16_float(src[8 * word + j]) - b;
+                        volatile float ratio = diff / s;
+                        float r = rintf(ratio);
+                        q = r < 0.0f ? 0 : (r > 15.0f ? 15 : (int)r);
+                    }
+                    packed |= (uint32_t)q << (4 * j);
+                }
+                w_packed[(size_t)n * (K / 8) + (size_t)g * 8 + word] = packed;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Sampling distribution of one logits row: temperature -> top-k -> top-p.   */
 /* ------------------------------------------------------------------------ */
 typedef struct {
