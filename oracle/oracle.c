@@ -116,7 +116,9 @@ int oracle_qmv(const uint32_t *w_packed, const uint16_t *scales, const uint16_t 
  *   q = 0 if s == 0, else clamp(rint((w - b) / s), 0, 15)
  * with every step an fp32 operation (subtraction, division, round half to
  * even): the code is an integer decided by floating point, so the oracle
- * takes the decision in the precision the product takes it in.
+ * takes the decision in the precision the product takes it in.  A zero
+ * minimum is stored as +0 (which zero is smallest is no property of the
+ * group).  The weights are finite.
  */
 static uint16_t bf16_rn_bits(float f) {
     uint32_t u;
@@ -150,6 +152,7 @@ int oracle_requantize(const uint16_t *w, int N, int K, uint32_t *w_packed, uint1
                 if (v < lo) lo = v;
                 if (v > hi) hi = v;
             }
+            if (lo == 0.0f) lo = 0.0f;              /* +0 */
             volatile float range = hi - lo;         /* fp32, one rounding */
             volatile float step = range / 15.0f;    /* fp32, one rounding */
             uint16_t s_bits = bf16_rn_bits(step);

@@ -79,6 +79,14 @@ def test_constant_groups_and_zero(oracle):
     assert (wp == 0).all()
 
 
+def test_zero_minimum_is_positive_zero(oracle):
+    w = np.zeros((1, 64), np.float32)
+    w[0, 5] = -0.0
+    w[0, 9] = 1.5
+    wp, s, b = oracle.requantize(_bits(w))
+    assert b[0, 0] == 0x0000 and s[0, 0] == _bits(np.float32(1.5) / np.float32(15))
+
+
 def test_nibble_order_is_lsb_first(oracle):
     """inputs 0..63 of one group hold levels 0, 1, ..., 15, 0, 1, ...: the
     first packed word of the row is 0x76543210."""
