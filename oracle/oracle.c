@@ -117,8 +117,8 @@ int oracle_qmv(const uint32_t *w_packed, const uint16_t *scales, const uint16_t 
  * with every step an fp32 operation (subtraction, division, round half to
  * even): the code is an integer decided by floating point, so the oracle
  * takes the decision in the precision the product takes it in.  A zero
- * minimum is stored as +0 (which zero is smallest is no property of the
- * group).  The weights are finite.
+ * minimum or maximum is taken as +0 (which zero is smallest or largest is no
+ * property of the group).  The weights are finite.
  */
 static uint16_t bf16_rn_bits(float f) {
     uint32_t u;
@@ -153,6 +153,7 @@ int oracle_requantize(const uint16_t *w, int N, int K, uint32_t *w_packed, uint1
                 if (v > hi) hi = v;
             }
             if (lo == 0.0f) lo = 0.0f;              /* +0 */
+            if (hi == 0.0f) hi = 0.0f;
             volatile float range = hi - lo;         /* fp32, one rounding */
             volatile float step = range / 15.0f;    /* fp32, one rounding */
             uint16_t s_bits = bf16_rn_bits(step);

@@ -79,12 +79,14 @@ def test_constant_groups_and_zero(oracle):
     assert (wp == 0).all()
 
 
-def test_zero_minimum_is_positive_zero(oracle):
-    w = np.zeros((1, 64), np.float32)
+def test_zero_extremes_are_positive_zero(oracle):
+    w = np.zeros((2, 64), np.float32)
     w[0, 5] = -0.0
     w[0, 9] = 1.5
+    w[1, ::2] = -0.0          # a group of signed zeros only
     wp, s, b = oracle.requantize(_bits(w))
     assert b[0, 0] == 0x0000 and s[0, 0] == _bits(np.float32(1.5) / np.float32(15))
+    assert b[1, 0] == 0x0000 and s[1, 0] == 0x0000 and wp[1].max() == 0
 
 
 def test_nibble_order_is_lsb_first(oracle):
