@@ -902,6 +902,63 @@ def run_wide(args):
     return 0
 
 
+def run_drafthead(args):
+    """The drafter's own 4-bit LM head: requantise the bf16 LM head (5120 ->
+    151936) with qmv_requantize, then the draft step's logits as qmv_smallm at
+    M = 1 on it, beside the bf16 head read by a plain library GEMV (context
+    for the draft-time saving the pages report)."""
+    import torch
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.MASTER_SEED + 43)
+    N, K = wl.VOCAB, wl.HIDDEN
+    w16 = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    wp = torch.empty((N, K // 8), dtype=torch.int32, device=dev)
+    s_ = torch.empty((N, K // GROUP), dtype=torch.bfloat16, device=dev)
+    b_ = torch.empty((N, K // GROUP), dtype=torch.bfloat16, device=dev)
+    x = torch.randn((1, K), generator=g, device=dev).to(torch.bfloat16)
+    y4 = torch.empty((1, N), device=dev)
+    y16 = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def requant():
+        sv.qmv_requantize(w16, out=(wp, s_, b_))
+
+    def draft4():
+        sv.qmv_smallm(wp, s_, b_, x, y4)
+
+    def draft16():
+        torch.matmul(x, w16.t(), out=y16)
+
+    requant()
+    torch.cuda.synchronize()
+    rq = time_graph(torch, capture(torch, requant, stream), stream, args.steps, args.warmup)
+    d4 = time_graph(torch, capture(torch, draft4, stream), stream, args.steps, args.warmup)
+    d16 = time_graph(torch, capture(torch, draft16, stream), stream, args.steps, args.warmup)
+    rq_us, d4_us, d16_us = (t / args.steps * 1e3 for t in (rq, d4, d16))
+    peaks = measured_peaks()
+    rq_bytes = N * K * 2 + N * K // 2 + 2 * 2 * N * (K // GROUP)
+    line = {"metric": METRIC, "value": qmv_bytes(1, N, K) / (d4_us / 1e6) / 1e9, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"draft-only 4-bit LM head {K}->{N}: requantise the bf16 "
+                                   "head, then the draft step's logits at M=1",
+                       "l2": "inputs larger than L2"},
+            "draft_logits_us_4bit": d4_us, "draft_logits_us_bf16_library_gemv": d16_us,
+            "draft_lm_head_time_saved": 1.0 - d4_us / d16_us,
+            "requantize_us": rq_us,
+            "requantize_gbs": rq_bytes / (rq_us / 1e6) / 1e9,
+            "requantize_frac": rq_bytes / (rq_us / 1e6) / 1e9 / peaks["hbm_gbs"],
+            "frac": qmv_bytes(1, N, K) / (d4_us / 1e6) / 1e9 / peaks["hbm_gbs"],
+            "peak": peaks}
+    print(json.dumps(line), flush=True)
+    sv.device_status()
+    return 0
+
+
 def run_stream(args):
     """The 27B-class verify weight stream (--layers decoder layers of q, k,
     v, o 5120x5120, gate, up 5120->17408, down 17408->5120, plus the LM head
@@ -1178,7 +1235,7 @@ def main(argv=None):
     ap.add_argument("--no-depth-sweep", action="store_true",
                     help="cycle: skip the draft depths K = 2..5 other than --depth")
     ap.add_argument("--workload", choices=["cycle", "mlp", "lmhead", "gdn", "qmv", "stream",
-                                           "conv", "wide"],
+                                           "conv", "wide", "drafthead"],
                     default="cycle")
     ap.add_argument("--layers", type=int, default=wl.N_LAYERS,
                     help="decoder layers of the --workload stream plan")
@@ -1200,7 +1257,8 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     return {"cycle": run_cycle, "mlp": run_mlp, "lmhead": run_lmhead, "gdn": run_gdn,
-            "qmv": run_qmv, "stream": run_stream, "conv": run_conv, "wide": run_wide}[
+            "qmv": run_qmv, "stream": run_stream, "conv": run_conv, "wide": run_wide,
+            "drafthead": run_drafthead}[
         args.workload](args)
 
 

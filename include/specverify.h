@@ -20,6 +20,8 @@
  *   gdn_tape_replay   rebuild the recurrent state over an accepted prefix
  *   conv_window_*     short convolution windows: outputs, commit of a prefix
  *   qmv_identity_probe  start-up check: block verify rows == single-row calls
+ *   qmv_requantize    a bf16 weight matrix -> the 4-bit layout above (the
+ *                     drafter's own 4-bit LM head)
  *   qmv_wide          the same product for wide blocks (M = 17..128, e.g. the
  *                     verify blocks of 32 sequences against one LM head) on
  *                     the tcgen05 tensor cores
@@ -246,6 +248,27 @@ sv_status qmv_identity_probe(const uint32_t *w_packed, const uint16_t *scales,
  * launches on `stream` (the group sums, then the product); M = 0 or N = 0
  * launches nothing.  A kernel wait that gives up (only if the device
  * misbehaves) sets a word read by sv_device_status. */
+/* ------------------------------------------------------------------------ */
+/* qmv_requantize: bf16 weights -> the 4-bit affine group-64 layout.         */
+/* ------------------------------------------------------------------------ */
+/* Source: "MTPLX 2.24x faster TPS", section "Layer 0: MLX Runtime": the
+ * target keeps its LM head at model precision while a separate 4-bit LM head,
+ * built in memory, serves the drafter only (draft time down, target accuracy
+ * unchanged).  The drafter's logits are then qmv_smallm(w_packed, scales,
+ * biases, x) at M = 1.
+ *
+ * w_bf16 [N][K] bf16 (finite values), row-major, 16-byte aligned.  Writes
+ * w_packed [N][K/8] (4-byte aligned), scales and biases [N][K/64] bf16
+ * (2-byte aligned), the layout of qmv_smallm.  Per group of 64 inputs of a
+ * row, every step one IEEE fp32 operation:
+ *   lo = min w, hi = max w (a zero extreme taken as +0),
+ *   s = rn_bf16((hi - lo) / 15), b = lo,
+ *   q = 0 if s == 0, else clamp(rint((w - b) / s), 0, 15)   (ties to even).
+ * Requires N >= 0, K % 64 == 0; no two buffers may overlap.  One launch on
+ * `stream` (PDL-capable); N = 0 launches nothing. */
+sv_status qmv_requantize(const uint16_t *w_bf16, uint32_t *w_packed, uint16_t *scales,
+                         uint16_t *biases, int N, int K, sv_stream_t stream);
+
 size_t qmv_wide_workspace_bytes(int M, int K);
 sv_status qmv_wide(const uint32_t *w_packed, const uint16_t *scales, const uint16_t *biases,
                    const uint16_t *x, float *y, int M, int N, int K, void *workspace,

@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
         L.qmv_identity_probe_bytes.restype = Z
         L.qmv_identity_probe.argtypes = [P, P, P, I, I, I, I, P, Z, ctypes.POINTER(I), P]
         L.qmv_identity_probe.restype = I
+        L.qmv_requantize.argtypes = [P, P, P, P, I, I, P]
+        L.qmv_requantize.restype = I
         L.qmv_wide_workspace_bytes.argtypes = [I, I]
         L.qmv_wide_workspace_bytes.restype = Z
         L.qmv_wide.argtypes = [P, P, P, P, P, I, I, I, P, Z, P]
@@ -226,6 +228,30 @@ def qmv_identity_probe(w_packed: torch.Tensor, scales: torch.Tensor, biases: tor
                                   _stream(dev))
     _check(st, "qmv_identity_probe")
     return int(out.value)
+
+
+def qmv_requantize(w: torch.Tensor, out=None):
+    """4-bit affine group-64 requantisation of a bf16 matrix [N, K] (the
+    drafter's own LM head): returns (w_packed int32 [N, K/8], scales, biases
+    bf16 [N, K/64]), the qmv_smallm layout; ``out`` may supply that triple."""
+    dev = w.device
+    if w.dtype not in (torch.bfloat16, torch.int16):
+        raise TypeError("w must be bfloat16 (or int16 bit patterns)")
+    if w.dim() != 2:
+        raise ValueError("w must be [N, K]")
+    N, K = w.shape
+    _need(w, "w", w.dtype, (N, K), dev)
+    if out is None:
+        out = (torch.empty((N, K // 8), dtype=torch.int32, device=dev),
+               torch.empty((N, K // 64), dtype=torch.bfloat16, device=dev),
+               torch.empty((N, K // 64), dtype=torch.bfloat16, device=dev))
+    wp, s, b = out
+    _need(wp, "w_packed", torch.int32, (N, K // 8), dev)
+    _need(s, "scales", torch.bfloat16, (N, K // 64), dev)
+    _need(b, "biases", torch.bfloat16, (N, K // 64), dev)
+    _check(lib().qmv_requantize(_ptr(w), _ptr(wp), _ptr(s), _ptr(b), N, K, _stream(dev)),
+           "qmv_requantize")
+    return wp, s, b
 
 
 def make_wide_workspace(M: int, K: int, device) -> torch.Tensor:

@@ -214,3 +214,16 @@ def test_wide_sizes_and_rejects(L):
     assert L.qmv_wide(w, s, b, x, y, 64, 300, 1024, ws, n - 1, None) == 1  # too small
     assert L.qmv_wide(w, s, b, x, x, 64, 300, 1024, ws, n, None) == 1      # y overlaps x
     assert L.qmv_wide(w, s, b, x, y, 64, 300, 1024, x, n, None) == 1       # workspace = x
+
+
+def test_requantize_rejects(L):
+    w, wp, s, b = (A + i * 0x1000000 for i in range(4))
+    assert L.qmv_requantize(w, wp, s, b, 0, 128, None) == 0        # N = 0: no launch
+    assert L.qmv_requantize(w, wp, s, b, 4, 100, None) == 1        # K % 64
+    assert L.qmv_requantize(w, wp, s, b, -1, 128, None) == 1
+    assert L.qmv_requantize(None, wp, s, b, 4, 128, None) == 1
+    assert L.qmv_requantize(w + 8, wp, s, b, 4, 128, None) == 1    # 16-byte alignment
+    assert L.qmv_requantize(w, wp + 2, s, b, 4, 128, None) == 1    # 4-byte alignment
+    assert L.qmv_requantize(w, wp, s + 1, b, 4, 128, None) == 1    # 2-byte alignment
+    assert L.qmv_requantize(w, w, s, b, 4, 128, None) == 1         # w_packed overlaps w
+    assert L.qmv_requantize(w, wp, s, s, 4, 128, None) == 1        # scales = biases
