@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define SV_ABI_VERSION 1
+#define SV_ABI_VERSION 2
 
 /* A CUDA stream (cudaStream_t); NULL selects the legacy default stream. */
 typedef struct CUstream_st *sv_stream_t;
@@ -173,9 +173,19 @@ typedef struct {
     const uint16_t *scales;
     const uint16_t *biases;
     const void *x;  /* [M][K] of the plan's dtype */
-    float *y;       /* [M][N] */
+    float *y;       /* [M][N]; NULL when topk is set */
     int N, K;
     int after;      /* 1: x is written by an earlier problem of the list */
+    /* NULL, or the per-row top-64 epilogue (at most one problem per plan):
+     * instead of y, each of the plan's G CTAs writes, for every output row
+     * m, the 64 largest (logit, index) pairs among the columns it computed
+     * as descending 64-bit keys (the ordered float bits of the logit, then
+     * the inverted index; 0 = empty), followed by one flag word per (CTA, m)
+     * that is nonzero when a NaN or +inf logit was met.  Layout:
+     * uint64 [G][M][64] then uint32 [G][M]; qmv_plan_topk_bytes gives its
+     * size.  spec_accept_lists reads it ("MTP in llama.cpp", one evaluation
+     * boundary per cycle; the logits never travel through memory). */
+    uint64_t *topk;
 } sv_qmv_problem;
 
 typedef struct sv_qmv_plan sv_qmv_plan;
@@ -189,6 +199,9 @@ sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream);
 void qmv_plan_destroy(sv_qmv_plan *plan);
 /* CTAs of the plan's launch (the co-resident count), 0 for NULL. */
 int qmv_plan_grid(const sv_qmv_plan *plan);
+/* Bytes of a top-64 epilogue buffer for plans of M rows and this dtype on the
+ * current device (G x M x (64 x 8 + 4)); 0 on invalid input. */
+size_t qmv_plan_topk_bytes(int M, sv_dtype x_dtype);
 
 /* ------------------------------------------------------------------------ */
 /* qmv_identity_probe: start-up check that block verification is exact.      */
@@ -325,6 +338,30 @@ sv_status spec_accept(const float *target_logits, const float *draft_logits,
                       int B, int K, int V, sv_sampling sampling, int32_t *out_tokens,
                       int32_t *n_accepted, int32_t *err_flags, void *workspace,
                       size_t workspace_bytes, sv_stream_t stream);
+
+/* spec_accept_lists: the same acceptance with the target rows given as the
+ * per-CTA top-64 lists of a fused LM head (the top-k epilogue of a qmv plan
+ * problem, sv_qmv_problem.topk) instead of logits: "MTP in llama.cpp", one
+ * evaluation boundary per cycle; the target logits never travel through
+ * memory.  target_lists holds B blocks of spec_accept_lists_block_bytes(G, K)
+ * bytes, 16-byte aligned; block b is the plan's buffer for sequence b (G
+ * CTAs, K+1 rows): uint64 keys [G][K+1][64] (descending, 0 = empty) then
+ * uint32 flags [G][K+1] (nonzero: a NaN or +inf logit was met).  Each list
+ * holds the 64 largest keys among the columns its CTA computed, so for
+ * top_k <= 64 (and greedy) the filtered target distribution is exactly the
+ * one spec_accept forms from the full logits; the result is identical to
+ * spec_accept on the logits the plan would have written.  Requires
+ * 1 <= G <= 2048.  The workspace is spec_accept's, sized by
+ * spec_accept_lists_workspace_bytes (equal to spec_accept_workspace_bytes
+ * when G <= 32 ceil(V / 16384), e.g. the 151936-token LM head on one GB300);
+ * everything else as spec_accept. */
+size_t spec_accept_lists_workspace_bytes(int B, int K, int V, int G);
+size_t spec_accept_lists_block_bytes(int G, int K);
+sv_status spec_accept_lists(const uint64_t *target_lists, int G, const float *draft_logits,
+                            const int32_t *draft_tokens, const float *u_accept,
+                            const float *u_sample, int B, int K, int V, sv_sampling sampling,
+                            int32_t *out_tokens, int32_t *n_accepted, int32_t *err_flags,
+                            void *workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /* spec_accept_noalloc: spec_accept on a scratch area that the library holds
  * as a fixed-size device global (spec_accept_noalloc_scratch_bytes() bytes,

@@ -47,7 +47,8 @@ class _Sampling(ctypes.Structure):
 class _QmvProblem(ctypes.Structure):
     _fields_ = [("w_packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("biases", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
-                ("N", ctypes.c_int), ("K", ctypes.c_int), ("after", ctypes.c_int)]
+                ("N", ctypes.c_int), ("K", ctypes.c_int), ("after", ctypes.c_int),
+                ("topk", ctypes.c_void_p)]
 
 
 _lib = None
@@ -76,6 +77,12 @@ def lib() -> ctypes.CDLL:
         L.spec_accept_workspace_bytes.restype = Z
         L.spec_accept.argtypes = [P, P, P, P, P, I, I, I, _Sampling, P, P, P, P, Z, P]
         L.spec_accept.restype = I
+        L.spec_accept_lists_workspace_bytes.argtypes = [I, I, I, I]
+        L.spec_accept_lists_workspace_bytes.restype = Z
+        L.spec_accept_lists_block_bytes.argtypes = [I, I]
+        L.spec_accept_lists_block_bytes.restype = Z
+        L.spec_accept_lists.argtypes = [P, I, P, P, P, P, I, I, I, _Sampling, P, P, P, P, Z, P]
+        L.spec_accept_lists.restype = I
         L.spec_accept_noalloc_scratch_bytes.argtypes = []
         L.spec_accept_noalloc_scratch_bytes.restype = Z
         L.spec_accept_noalloc.argtypes = [P, P, P, P, P, I, I, I, _Sampling, P, P, P, P]
@@ -89,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.qmv_plan_run.restype = I
         L.qmv_plan_destroy.argtypes = [P]
         L.qmv_plan_destroy.restype = None
+        L.qmv_plan_topk_bytes.argtypes = [I, I]
+        L.qmv_plan_topk_bytes.restype = Z
         L.qmv_plan_grid.argtypes = [P]
         L.qmv_plan_grid.restype = I
         L.qmv_identity_probe_bytes.argtypes = [I, I, I, I]
@@ -304,10 +313,12 @@ def qmv_wide(w_packed: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
 class QmvPlan:
     """An ordered list of qmv_smallm problems run by one persistent launch.
 
-    ``problems``: sequence of (w_packed, scales, biases, x, y, after) with the
-    shapes of :func:`qmv_smallm`; ``after`` = True when x is the output of an
-    earlier problem of the list.  All x share dtype and M.  The plan keeps
-    references to every tensor and to its device buffer."""
+    ``problems``: sequence of (w_packed, scales, biases, x, y, after[, topk])
+    with the shapes of :func:`qmv_smallm`; ``after`` = True when x is the
+    output of an earlier problem of the list.  ``topk`` (at most one problem;
+    a uint8 tensor from :func:`make_topk_lists`, y then None) makes that
+    problem write per-CTA top-64 lists instead of y.  All x share dtype and M.
+    The plan keeps references to every tensor and to its device buffer."""
 
     def __init__(self, problems):
         if not problems:
@@ -316,17 +327,25 @@ class QmvPlan:
         dev = x0.device
         M = x0.shape[0]
         arr = (_QmvProblem * len(problems))()
-        for i, (w, s_, b_, x, y, after) in enumerate(problems):
+        dt = SV_BF16 if x0.dtype == torch.bfloat16 else SV_F32
+        for i, prob in enumerate(problems):
+            w, s_, b_, x, y, after = prob[:6]
+            topk = prob[6] if len(prob) > 6 else None
             N, K8 = w.shape
             K = K8 * 8
             _need(w, f"problems[{i}].w_packed", torch.int32, (N, K8), dev)
             _need(s_, f"problems[{i}].scales", torch.bfloat16, (N, K // 64), dev)
             _need(b_, f"problems[{i}].biases", torch.bfloat16, (N, K // 64), dev)
             _need(x, f"problems[{i}].x", x0.dtype, (M, K), dev)
-            _need(y, f"problems[{i}].y", torch.float32, (M, N), dev)
+            if topk is None:
+                _need(y, f"problems[{i}].y", torch.float32, (M, N), dev)
+            else:
+                _need(topk, f"problems[{i}].topk", torch.uint8, None, dev)
+                if topk.numel() < int(lib().qmv_plan_topk_bytes(M, dt)):
+                    raise ValueError(f"problems[{i}].topk is smaller than qmv_plan_topk_bytes")
             arr[i] = _QmvProblem(w.data_ptr(), s_.data_ptr(), b_.data_ptr(), x.data_ptr(),
-                                 y.data_ptr(), N, K, 1 if after else 0)
-        dt = SV_BF16 if x0.dtype == torch.bfloat16 else SV_F32
+                                 None if y is None else y.data_ptr(), N, K, 1 if after else 0,
+                                 None if topk is None else topk.data_ptr())
         with torch.cuda.device(dev):
             n = int(lib().qmv_plan_device_bytes(arr, len(problems), M, dt))
             if n == 0:  # invalid: qmv_plan_create reports why, with its status
@@ -360,6 +379,17 @@ class QmvPlan:
             self.close()
         except Exception:
             pass
+
+
+def make_topk_lists(M: int, x_dtype: torch.dtype, device) -> torch.Tensor:
+    """A buffer (uint8) for a plan problem's top-64 epilogue: per CTA and row
+    64 keys (uint64), then one flag word per CTA and row."""
+    dt = SV_BF16 if x_dtype == torch.bfloat16 else SV_F32
+    with torch.cuda.device(device):
+        n = int(lib().qmv_plan_topk_bytes(M, dt))
+    if n == 0:
+        _check(SV_ERR_INVALID_ARG, "qmv_plan_topk_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def spec_accept_workspace_bytes(B: int, K: int, V: int) -> int:
@@ -405,6 +435,49 @@ def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor | None,
                            _ptr(n_accepted), _ptr(err_flags), _ptr(workspace),
                            workspace.numel(), _stream(dev))
     _check(st, "spec_accept")
+    return out_tokens, n_accepted, err_flags
+
+
+def spec_accept_lists(target_lists: torch.Tensor, G: int, V: int,
+                      draft_logits: torch.Tensor | None, draft_tokens: torch.Tensor,
+                      u_accept: torch.Tensor, u_sample: torch.Tensor, temperature: float,
+                      top_k: int, top_p: float, workspace: torch.Tensor | None = None,
+                      out_tokens: torch.Tensor | None = None,
+                      n_accepted: torch.Tensor | None = None,
+                      err_flags: torch.Tensor | None = None):
+    """spec_accept with the target rows as per-CTA top-64 lists of a fused LM
+    head (a plan problem's ``topk`` buffer, uint8, one block per sequence of
+    spec_accept_lists_block_bytes(G, K) bytes).  Same returns as spec_accept."""
+    dev = target_lists.device
+    B, K = draft_tokens.shape
+    _need(target_lists, "target_lists", torch.uint8, None, dev)
+    blk = int(lib().spec_accept_lists_block_bytes(G, K))
+    if target_lists.numel() < B * blk:
+        raise ValueError(f"target_lists holds {target_lists.numel()} bytes, need {B * blk}")
+    if draft_logits is not None:
+        _need(draft_logits, "draft_logits", torch.float32, (B, K, V), dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
+    _need(u_accept, "u_accept", torch.float32, (B, K), dev)
+    _need(u_sample, "u_sample", torch.float32, (B,), dev)
+    if workspace is None:
+        n = int(lib().spec_accept_lists_workspace_bytes(B, K, V, int(G)))
+        workspace = torch.zeros(max(n, 16), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if err_flags is None:
+        err_flags = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K + 1), dev)
+    _need(n_accepted, "n_accepted", torch.int32, (B,), dev)
+    _need(err_flags, "err_flags", torch.int32, (B,), dev)
+    samp = _Sampling(float(temperature), int(top_k), float(top_p))
+    st = lib().spec_accept_lists(_ptr(target_lists), int(G), _ptr(draft_logits),
+                                 _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), B, K, V,
+                                 samp, _ptr(out_tokens), _ptr(n_accepted), _ptr(err_flags),
+                                 _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(st, "spec_accept_lists")
     return out_tokens, n_accepted, err_flags
 
 

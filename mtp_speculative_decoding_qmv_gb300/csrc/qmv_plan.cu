@@ -60,6 +60,7 @@ struct PlanProblem {  // CUtensorMap's own alignment (>= 64 bytes) carries over
   CUtensorMap wmap, smap, bmap;
   const void *x;
   float *y;
+  unsigned long long *topk;  // per-CTA top-64 lists instead of y (or null)
   int N, K;
   int tiles, chunks;  // 64-row tiles, 512-input stages
   int chunk_off;      // first flat stage index in its phase
@@ -102,18 +103,82 @@ struct PlanParams {
   int n_phases;
   int M;
   int stages;
+  int topk;  // 1: one problem has the top-64 epilogue (lists in shared memory)
+  unsigned long long *topk_out;  // that problem's lists [G][M][64], then flags [G][M]
 };
 
+constexpr int kTopK = 64;        // keys kept per CTA and output row by the epilogue
+constexpr int kTopKRows = 8;     // M <= 8
+constexpr uint32_t kTopKBytes = kTopKRows * kTopK * 8 + kTopKRows * 4;
+
 struct PlanLayout {
-  uint32_t ring, red, bar, total;
+  uint32_t ring, red, topk, bar, total;
 };
-__host__ __device__ inline PlanLayout plan_layout(int stages) {
+__host__ __device__ inline PlanLayout plan_layout(int stages, bool topk) {
   PlanLayout L;
   L.ring = (uint32_t)stages * kStageBytesStream;
   L.red = L.ring;
-  L.bar = L.red + kRedBytes;
+  L.topk = L.red + kRedBytes;
+  L.bar = L.topk + (topk ? kTopKBytes : 0u);
+  L.bar = (L.bar + 7u) & ~7u;
   L.total = L.bar + (uint32_t)(2 * stages + 2) * 8u + 1024u;
   return L;
+}
+
+// Ordered key of a logit: larger float -> larger key; 0 = never kept (NaN,
+// +inf, -inf); NaN and +inf also set `nonfinite`.  Equal floats (-0, +0) give
+// equal keys; the composite with the inverted index puts the lower index
+// first among equal logits.
+__device__ __forceinline__ uint32_t topk_logit_key(float v, int &nonfinite) {
+  uint32_t u = __float_as_uint(v);
+  if ((u & 0x7F800000u) == 0x7F800000u) {
+    if ((u & 0x007FFFFFu) != 0 || (u >> 31) == 0) nonfinite = 1;
+    return 0u;
+  }
+  if ((u & 0x7FFFFFFFu) == 0) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp merges a tile's values of output row m (lane: rows n0 + lane and
+// n0 + lane + 32) into the descending list `list` [kTopK] (shared memory):
+// the values above the list's last key are inserted largest first, each by
+// counting the larger entries and shifting the rest down one place.
+__device__ void topk_merge_tile(unsigned long long *list, unsigned int *flag, float c0, float c1,
+                                int n0, int N) {
+  const int lane = threadIdx.x & 31;
+  int nf = 0;
+  const int r0 = n0 + lane, r1 = n0 + lane + 32;
+  const uint32_t k0 = r0 < N ? topk_logit_key(c0, nf) : 0u;
+  const uint32_t k1 = r1 < N ? topk_logit_key(c1, nf) : 0u;
+  if (__any_sync(0xffffffffu, nf) && lane == 0) *flag = 1u;
+  unsigned long long e0 = k0 ? ((unsigned long long)k0 << 32) | (0xFFFFFFFFu - (uint32_t)r0) : 0ull;
+  unsigned long long e1 = k1 ? ((unsigned long long)k1 << 32) | (0xFFFFFFFFu - (uint32_t)r1) : 0ull;
+  unsigned long long l0 = list[lane], l1 = list[lane + 32];
+  unsigned long long thr = __shfl_sync(0xffffffffu, l1, 31);
+  if (e0 <= thr) e0 = 0ull;
+  if (e1 <= thr) e1 = 0ull;
+  while (__any_sync(0xffffffffu, (e0 | e1) != 0ull)) {
+    const unsigned long long g = warp_max_u64(e0 > e1 ? e0 : e1);
+    const int pos = __popc(__ballot_sync(0xffffffffu, l0 > g)) +
+                    __popc(__ballot_sync(0xffffffffu, l1 > g));
+    // shift entries pos.. down one place, g at pos
+    unsigned long long p0 = __shfl_up_sync(0xffffffffu, l0, 1);
+    unsigned long long p1 = __shfl_up_sync(0xffffffffu, l1, 1);
+    const unsigned long long l0_31 = __shfl_sync(0xffffffffu, l0, 31);
+    if (lane == 0) p1 = l0_31;
+    const unsigned long long n0v = lane < pos ? l0 : (lane == pos ? g : p0);
+    const unsigned long long n1v = lane + 32 < pos ? l1 : (lane + 32 == pos ? g : p1);
+    l0 = n0v;
+    l1 = n1v;
+    if (e0 == g) e0 = 0ull;
+    if (e1 == g) e1 = 0ull;
+    thr = __shfl_sync(0xffffffffu, l1, 31);
+    if (e0 <= thr) e0 = 0ull;
+    if (e1 <= thr) e1 = 0ull;
+  }
+  list[lane] = l0;
+  list[lane + 32] = l1;
+  __syncwarp();
 }
 
 __device__ __forceinline__ int atom_add_acq_rel(int *p, int v) {
@@ -195,7 +260,7 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
   uint8_t *smem = smem_raw + (base - raw);
   const int G = gridDim.x, cta = blockIdx.x;
   const int stages = P.stages;
-  const PlanLayout L = plan_layout(stages);
+  const PlanLayout L = plan_layout(stages, P.topk != 0);
   const uint32_t full0 = base + L.bar;
   const uint32_t empty0 = full0 + 8u * stages;
   const uint32_t red_full = empty0 + 8u * stages;  // consumers' tile sums are in red
@@ -263,6 +328,14 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     // run order) and count the tile when a later phase waits for it.
     unsigned nseg = 0;
     const float4 *red4 = reinterpret_cast<const float4 *>(red);
+    // the top-64 lists of this CTA (empty = key 0) and their non-finite flags
+    unsigned long long *tk_list = reinterpret_cast<unsigned long long *>(smem + L.topk);
+    unsigned int *tk_flag = reinterpret_cast<unsigned int *>(tk_list + kTopKRows * kTopK);
+    if (P.topk) {
+      for (int i = lane; i < kTopKRows * kTopK; i += 32) tk_list[i] = 0ull;
+      if (lane < kTopKRows) tk_flag[lane] = 0u;
+      __syncwarp();
+    }
     pdl_wait();  // y and the plan's counters belong to the preceding kernel until here
     int cur_phase = -1, max_splits = 1, signal = 0;
     const RunList runs(P, cta);
@@ -345,15 +418,26 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
           }
         }
         if (write) {
+          if (q.topk) {
+            // the tile's columns go into this CTA's top-64 lists, not to y
+            const float c0[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+            const float c1[8] = {v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int row = n0 + lane + 32 * h;
-            if (row < N) {
-              const float c[8] = {v[2 * h].x, v[2 * h].y, v[2 * h].z, v[2 * h].w,
-                                  v[2 * h + 1].x, v[2 * h + 1].y, v[2 * h + 1].z, v[2 * h + 1].w};
+            for (int col = 0; col < 8; ++col)
+              if (col < P.M)
+                topk_merge_tile(tk_list + col * kTopK, tk_flag + col, c0[col], c1[col], n0, N);
+          } else {
 #pragma unroll
-              for (int col = 0; col < 8; ++col)
-                if (col < P.M) q.y[(size_t)col * N + row] = c[col];
+            for (int h = 0; h < 2; ++h) {
+              const int row = n0 + lane + 32 * h;
+              if (row < N) {
+                const float c[8] = {v[2 * h].x, v[2 * h].y, v[2 * h].z, v[2 * h].w,
+                                    v[2 * h + 1].x, v[2 * h + 1].y, v[2 * h + 1].z,
+                                    v[2 * h + 1].w};
+#pragma unroll
+                for (int col = 0; col < 8; ++col)
+                  if (col < P.M) q.y[(size_t)col * N + row] = c[col];
+              }
             }
           }
           __syncwarp();
@@ -363,6 +447,14 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
           }
         }
       }
+    }
+    if (P.topk) {
+      // every CTA writes its lists (empty ones included) and flags
+      unsigned long long *dst = P.topk_out + (size_t)cta * P.M * kTopK;
+      for (int i = lane; i < P.M * kTopK; i += 32) dst[i] = tk_list[i];
+      unsigned int *fdst =
+          reinterpret_cast<unsigned int *>(P.topk_out + (size_t)G * P.M * kTopK) + cta * P.M;
+      if (lane < P.M) fdst[lane] = tk_flag[lane];
     }
   } else {
     // ------------------------------ consumers -----------------------------
@@ -516,6 +608,7 @@ sv_status plan_shape(const sv_qmv_problem *pr, int n, int G, PlanShape &S) {
       q.K = pr[j].K;
       q.x = pr[j].x;
       q.y = pr[j].y;
+      q.topk = reinterpret_cast<unsigned long long *>(pr[j].topk);
       q.tiles = (q.N + kRows - 1) / kRows;
       q.chunks = q.K / kStageInputs;
       q.chunk_off = (int)work;
@@ -618,7 +711,7 @@ sv_status plan_shape(const sv_qmv_problem *pr, int n, int G, PlanShape &S) {
 }
 
 template <bool kXF32>
-sv_status plan_config(int dev, int &grid, int &stages, uint32_t &smem) {
+sv_status plan_config(int dev, bool topk, int &grid, int &stages, uint32_t &smem) {
   int optin = 0, smem_sm = 0, sms = device_sm_count();
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
@@ -639,8 +732,8 @@ sv_status plan_config(int dev, int &grid, int &stages, uint32_t &smem) {
   const uint32_t budget = (uint32_t)smem_sm / per_sm - 1024u - (uint32_t)fa.sharedSizeBytes;
   stages = 2;
   const uint32_t cap = std::min<uint32_t>(budget, (uint32_t)optin - (uint32_t)fa.sharedSizeBytes);
-  while (stages < 16 && plan_layout(stages + 1).total <= cap) ++stages;
-  smem = plan_layout(stages).total;
+  while (stages < 16 && plan_layout(stages + 1, topk).total <= cap) ++stages;
+  smem = plan_layout(stages, topk).total;
   if (smem > (uint32_t)optin) return fail(SV_ERR_UNSUPPORTED, "qmv_plan: shared memory");
   int fit = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, qmv_plan_kernel<kXF32>, kPlanThreads,
@@ -651,12 +744,22 @@ sv_status plan_config(int dev, int &grid, int &stages, uint32_t &smem) {
   return SV_OK;
 }
 
+bool has_topk(const sv_qmv_problem *pr, int n) {
+  for (int i = 0; i < n; ++i)
+    if (pr[i].topk) return true;
+  return false;
+}
+
+size_t topk_bytes(int grid, int M) {
+  return (size_t)grid * M * (kTopK * sizeof(unsigned long long) + sizeof(unsigned int));
+}
+
 sv_status validate_problems(const sv_qmv_problem *pr, int n, int M, sv_dtype x_dtype) {
   if (n < 1 || !pr) return fail(SV_ERR_INVALID_ARG, "qmv_plan: need n_problems >= 1");
   if (M < 1 || M > 8) return fail(SV_ERR_UNSUPPORTED, "qmv_plan: M=%d outside [1, 8]", M);
   if (x_dtype != SV_F32 && x_dtype != SV_BF16)
     return fail(SV_ERR_INVALID_ARG, "qmv_plan: unknown x_dtype %d", (int)x_dtype);
-  int phase_start = 0;
+  int phase_start = 0, n_topk = 0;
   for (int i = 0; i < n; ++i) {
     const sv_qmv_problem &q = pr[i];
     if (q.N < 1 || q.K < 1)
@@ -666,20 +769,25 @@ sv_status validate_problems(const sv_qmv_problem *pr, int n, int M, sv_dtype x_d
                   q.K, kStageInputs);
     if (q.N > (1 << 30) || q.K > (1 << 30))
       return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d too large", i);
-    if (!q.w_packed || !q.scales || !q.biases || !q.x || !q.y)
+    if (!q.w_packed || !q.scales || !q.biases || !q.x || (!q.y && !q.topk))
       return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d: null pointer", i);
     if (!aligned(q.w_packed, 16) || !aligned(q.scales, 16) || !aligned(q.biases, 16) ||
-        !aligned(q.x, 16) || !aligned(q.y, 4))
+        !aligned(q.x, 16) || !aligned(q.y, 4) || !aligned(q.topk, 8))
       return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d: misaligned pointer", i);
+    if (q.topk && ++n_topk > 1)
+      return fail(SV_ERR_UNSUPPORTED, "qmv_plan: more than one problem with a top-64 epilogue");
     const size_t wb = (size_t)q.N * q.K / 2, sbb = (size_t)q.N * (q.K / 64) * 2;
-    const size_t xb = (size_t)M * q.K * (x_dtype == SV_F32 ? 4 : 2), yb = (size_t)M * q.N * 4;
-    if (overlaps(q.y, yb, q.w_packed, wb) || overlaps(q.y, yb, q.scales, sbb) ||
-        overlaps(q.y, yb, q.biases, sbb) || overlaps(q.y, yb, q.x, xb))
+    const size_t xb = (size_t)M * q.K * (x_dtype == SV_F32 ? 4 : 2);
+    // the output: y, or the top-64 lists (their size is checked at create)
+    const void *out = q.topk ? static_cast<const void *>(q.topk) : q.y;
+    const size_t ob = q.topk ? (size_t)1 : (size_t)M * q.N * 4;
+    if (overlaps(out, ob, q.w_packed, wb) || overlaps(out, ob, q.scales, sbb) ||
+        overlaps(out, ob, q.biases, sbb) || overlaps(out, ob, q.x, xb))
       return fail(SV_ERR_INVALID_ARG, "qmv_plan: problem %d: y overlaps an input", i);
     // an output read later in the same phase would be read before it is written
     if (i == 0 || q.after) phase_start = i;
     for (int j = phase_start; j < i; ++j)
-      if (overlaps(pr[j].y, (size_t)M * pr[j].N * 4, q.x, xb))
+      if (!pr[j].topk && overlaps(pr[j].y, (size_t)M * pr[j].N * 4, q.x, xb))
         return fail(SV_ERR_INVALID_ARG,
                     "qmv_plan: problem %d reads problem %d's output without `after`", i, j);
   }
@@ -695,8 +803,9 @@ extern "C" size_t qmv_plan_device_bytes(const sv_qmv_problem *problems, int n_pr
   int grid = 0, stages = 0;
   uint32_t smem = 0;
   const int dev = current_device();
-  const sv_status st = x_dtype == SV_BF16 ? plan_config<false>(dev, grid, stages, smem)
-                                          : plan_config<true>(dev, grid, stages, smem);
+  const bool topk = has_topk(problems, n_problems);
+  const sv_status st = x_dtype == SV_BF16 ? plan_config<false>(dev, topk, grid, stages, smem)
+                                          : plan_config<true>(dev, topk, grid, stages, smem);
   if (st != SV_OK) return 0;
   PlanShape S;
   if (plan_shape(problems, n_problems, grid, S) != SV_OK) return 0;
@@ -714,8 +823,9 @@ extern "C" sv_status qmv_plan_create(const sv_qmv_problem *problems, int n_probl
   const int dev = current_device();
   int grid = 0, stages = 0;
   uint32_t smem = 0;
-  st = x_dtype == SV_BF16 ? plan_config<false>(dev, grid, stages, smem)
-                          : plan_config<true>(dev, grid, stages, smem);
+  const bool topk = has_topk(problems, n_problems);
+  st = x_dtype == SV_BF16 ? plan_config<false>(dev, topk, grid, stages, smem)
+                          : plan_config<true>(dev, topk, grid, stages, smem);
   if (st != SV_OK) return st;
   PlanShape S;
   st = plan_shape(problems, n_problems, grid, S);
@@ -725,6 +835,10 @@ extern "C" sv_status qmv_plan_create(const sv_qmv_problem *problems, int n_probl
   if (device_bytes < S.total)
     return fail(SV_ERR_INVALID_ARG, "qmv_plan_create: device buffer of %zu bytes, need %zu",
                 device_bytes, S.total);
+  for (int i = 0; i < n_problems; ++i)
+    if (problems[i].topk &&
+        overlaps(problems[i].topk, topk_bytes(grid, M), device_buffer, S.total))
+      return fail(SV_ERR_INVALID_ARG, "qmv_plan_create: the top-64 buffer overlaps the plan");
   for (int i = 0; i < n_problems; ++i) {
     const sv_qmv_problem &q = problems[i];
     PlanProblem &d = S.probs[i];
@@ -768,6 +882,10 @@ extern "C" sv_status qmv_plan_create(const sv_qmv_problem *problems, int n_probl
   P.n_phases = (int)S.phases.size();
   P.M = M;
   P.stages = stages;
+  P.topk = topk ? 1 : 0;
+  P.topk_out = nullptr;
+  for (int i = 0; i < n_problems; ++i)
+    if (problems[i].topk) P.topk_out = reinterpret_cast<unsigned long long *>(problems[i].topk);
   *plan_out = plan;
   return SV_OK;
 }
@@ -808,3 +926,17 @@ extern "C" sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream) {
 extern "C" void qmv_plan_destroy(sv_qmv_plan *plan) { delete plan; }
 
 extern "C" int qmv_plan_grid(const sv_qmv_plan *plan) { return plan ? plan->grid : 0; }
+
+extern "C" size_t qmv_plan_topk_bytes(int M, sv_dtype x_dtype) {
+  clear_error();
+  if (M < 1 || M > 8 || (x_dtype != SV_F32 && x_dtype != SV_BF16)) {
+    fail(SV_ERR_INVALID_ARG, "qmv_plan_topk_bytes: M=%d or dtype %d invalid", M, (int)x_dtype);
+    return 0;
+  }
+  int grid = 0, stages = 0;
+  uint32_t smem = 0;
+  const int dev = current_device();
+  const sv_status st = x_dtype == SV_BF16 ? plan_config<false>(dev, true, grid, stages, smem)
+                                          : plan_config<true>(dev, true, grid, stages, smem);
+  return st == SV_OK ? topk_bytes(grid, M) : 0;
+}

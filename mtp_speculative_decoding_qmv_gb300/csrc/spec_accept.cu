@@ -66,6 +66,11 @@ struct AcceptArgs {
   float top_p;
   int32_t *out, *nacc, *flags;
   u64 *cand;      // [B][rows_max][C][kMaxTopK]
+  // target rows given as per-CTA top-64 lists of a fused LM head (or null):
+  // per sequence, [G][K+1][kMaxTopK] keys then [G][K+1] flag words
+  const u64 *tlists;
+  long long tstride;  // u64 units per sequence
+  int G;
   int *counters;  // [B]
   int *rowflags;  // [B][rows_max]
   int rows;       // rows read per sequence (K+1 greedy, 2K+1 sampling)
@@ -79,14 +84,24 @@ struct AcceptArgs {
 struct WsLayout {
   size_t rowflags, cand, total;
 };
-__host__ __device__ inline WsLayout ws_layout(int B, int K, int V) {
+// C: chunks per row (ceil(V / kChunk), more for target rows given as lists)
+__host__ __device__ inline WsLayout ws_layout_c(int B, int K, size_t C) {
   const size_t rows_max = 2 * (size_t)K + 1;
-  const size_t C = ((size_t)V + kChunk - 1) / kChunk;
   WsLayout L;
   L.rowflags = ((size_t)B * 4 + 15) / 16 * 16;
   L.cand = L.rowflags + ((size_t)B * rows_max * 4 + 15) / 16 * 16;
   L.total = L.cand + (size_t)B * rows_max * C * kMaxTopK * 8;
   return L;
+}
+__host__ __device__ inline WsLayout ws_layout(int B, int K, int V) {
+  return ws_layout_c(B, K, ((size_t)V + kChunk - 1) / kChunk);
+}
+// chunks per row when the target rows come as G per-CTA lists: a chunk CTA
+// of a target row merges at most kListsPerChunk lists
+constexpr int kListsPerChunk = 32;
+__host__ inline int lists_chunks(int V, int G) {
+  const int cv = (V + kChunk - 1) / kChunk, cl = (G + kListsPerChunk - 1) / kListsPerChunk;
+  return cv > cl ? cv : cl;
 }
 
 // ordered key of a logit: larger float -> larger key; 0 marks an excluded
@@ -321,6 +336,40 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
   const int base = cx * kChunk;
   const int ksel = a.ksel;
 
+  if (a.tlists != nullptr && rloc <= K) {
+    // ---- target row from the fused LM head: chunk cx merges the per-CTA
+    // lists g0..g1-1 of this row into its sorted top-ksel (each list is
+    // sorted, so its first ksel keys are all it can contribute)
+    const int g0 = (int)((long long)cx * a.G / a.C), g1 = (int)((long long)(cx + 1) * a.G / a.C);
+    const int n = g1 - g0;
+    const u64 *blk = a.tlists + (size_t)b * a.tstride;
+    const unsigned *tfl = reinterpret_cast<const unsigned *>(blk + (size_t)a.G * (K + 1) * kMaxTopK);
+    for (int i = tid; i < n * ksel; i += kThreads) {
+      const int l = i / ksel, h = i - l * ksel;
+      S.buf[i] = __ldcg(blk + ((size_t)(g0 + l) * (K + 1) + rloc) * kMaxTopK + h);
+    }
+    int nf = 0;
+    for (int l = tid; l < n; l += kThreads) nf |= __ldcg(tfl + (size_t)(g0 + l) * (K + 1) + rloc) != 0u;
+    const int any_nf = __syncthreads_or(nf);
+    if (warp == 0) {
+      u64 *dst = a.cand + ((size_t)b * a.rows_max + rloc) * (size_t)a.C * kMaxTopK +
+                 (size_t)cx * kMaxTopK;
+      int h0 = 0, h1 = 0;  // heads of lists lane and lane + 32
+      int j = 0;
+      for (; j < ksel; ++j) {
+        const u64 v0 = (lane < n && h0 < ksel) ? S.buf[lane * ksel + h0] : 0ull;
+        const u64 v1 = (lane + 32 < n && h1 < ksel) ? S.buf[(lane + 32) * ksel + h1] : 0ull;
+        const u64 g = warp_max_u64(v0 > v1 ? v0 : v1);
+        if (g == 0ull) break;
+        if (v0 == g) ++h0;
+        else if (v1 == g) ++h1;
+        if (lane == 0) dst[j] = g;
+      }
+      for (int i = j + lane; i < ksel; i += 32) dst[i] = 0ull;  // empty slots
+      if (lane == 0 && any_nf)
+        atomicOr(&a.rowflags[b * a.rows_max + rloc], SV_FLAG_NONFINITE_LOGIT);
+    }
+  } else {
   // ---- load the chunk (values past V read as -inf: key 0, never kept) ------
   float v[kPerThread];
   float vsum = 0.f;  // finite iff every value of this thread's share is
@@ -513,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptAr
   else if (tid < ksel) dst[tid] = 0;  // empty slots
   }
   if (tid == 0 && any_nonfinite) atomicOr(&a.rowflags[b * a.rows_max + rloc], SV_FLAG_NONFINITE_LOGIT);
+  }  // chunk of logits
 
   // ---- the last CTA of this sequence finishes it ---------------------------
   // every thread's candidate stores precede thread 0's release (CTA barrier,
@@ -707,12 +757,24 @@ extern "C" size_t spec_accept_workspace_bytes(int B, int K, int V) {
   return ws_layout(B, K, V).total;
 }
 
-extern "C" sv_status spec_accept(const float *target_logits, const float *draft_logits,
-                                 const int32_t *draft_tokens, const float *u_accept,
-                                 const float *u_sample, int B, int K, int V, sv_sampling sampling,
-                                 int32_t *out_tokens, int32_t *n_accepted, int32_t *err_flags,
-                                 void *workspace, size_t workspace_bytes, sv_stream_t stream) {
-  clear_error();
+namespace sv {
+namespace {
+
+// Bytes of one sequence's block of per-CTA target lists (G CTAs, K+1 rows):
+// keys [G][K+1][kMaxTopK] then flag words [G][K+1], rounded up to 16 bytes.
+size_t lists_block_bytes(int G, int K) {
+  const size_t b = (size_t)G * (K + 1) * (kMaxTopK * 8 + 4);
+  return (b + 15) / 16 * 16;
+}
+
+// Both entry points: the target rows come either as logits or (target_lists
+// non-null) as the per-CTA lists of a fused LM head.
+sv_status accept_impl(const float *target_logits, const u64 *target_lists, int G,
+                      const float *draft_logits, const int32_t *draft_tokens,
+                      const float *u_accept, const float *u_sample, int B, int K, int V,
+                      sv_sampling sampling, int32_t *out_tokens, int32_t *n_accepted,
+                      int32_t *err_flags, void *workspace, size_t workspace_bytes,
+                      sv_stream_t stream) {
   if (B < 0 || K < 1 || V < 1)
     return fail(SV_ERR_INVALID_ARG, "spec_accept: need B >= 0, K >= 1, V >= 1 (B=%d K=%d V=%d)", B,
                 K, V);
@@ -732,21 +794,32 @@ extern "C" sv_status spec_accept(const float *target_logits, const float *draft_
   if (B == 0) return SV_OK;
   if ((long long)B * (2 * K + 1) > 65535)
     return fail(SV_ERR_UNSUPPORTED, "spec_accept: B*(2K+1) = %lld > 65535", (long long)B * (2 * K + 1));
-  if (!target_logits || !draft_tokens || !u_accept || !u_sample || !out_tokens || !n_accepted ||
-      !workspace || (!greedy && !draft_logits))
+  if ((!target_logits && !target_lists) || !draft_tokens || !u_accept || !u_sample ||
+      !out_tokens || !n_accepted || !workspace || (!greedy && !draft_logits))
     return fail(SV_ERR_INVALID_ARG, "spec_accept: null pointer");
-  const WsLayout W = ws_layout(B, K, V);
+  if (target_lists) {
+    if (G < 1 || G > kListsPerChunk * kMaxChunks)
+      return fail(SV_ERR_UNSUPPORTED, "spec_accept_lists: G=%d outside [1, %d]", G,
+                  kListsPerChunk * kMaxChunks);
+    if (!aligned(target_lists, 16))
+      return fail(SV_ERR_INVALID_ARG, "spec_accept_lists: target_lists must be 16-byte aligned");
+  }
+  const int C = target_lists ? lists_chunks(V, G) : (V + kChunk - 1) / kChunk;
+  static_assert(kListsPerChunk * kMaxTopK <= kCap, "a chunk's lists fit the candidate buffer");
+  const WsLayout W = ws_layout_c(B, K, (size_t)C);
   if (workspace_bytes < W.total)
     return fail(SV_ERR_INVALID_ARG, "spec_accept: workspace of %zu bytes, need %zu",
                 workspace_bytes, W.total);
   if (!aligned(workspace, 16)) return fail(SV_ERR_INVALID_ARG, "spec_accept: workspace must be 16-byte aligned");
-  if (!aligned(target_logits, 4) || (draft_logits && !aligned(draft_logits, 4)) ||
+  if ((target_logits && !aligned(target_logits, 4)) || (draft_logits && !aligned(draft_logits, 4)) ||
       !aligned(draft_tokens, 4) || !aligned(u_accept, 4) || !aligned(u_sample, 4) ||
       !aligned(out_tokens, 4) || !aligned(n_accepted, 4) || (err_flags && !aligned(err_flags, 4)))
     return fail(SV_ERR_INVALID_ARG, "spec_accept: misaligned pointer");
-  const size_t tlb = (size_t)B * (K + 1) * V * 4, dlb = (size_t)B * K * V * 4;
+  const size_t tlb = target_lists ? (size_t)B * lists_block_bytes(G, K) : (size_t)B * (K + 1) * V * 4;
+  const size_t dlb = (size_t)B * K * V * 4;
   const size_t ob = (size_t)B * (K + 1) * 4, nb = (size_t)B * 4;
-  const void *ins[5] = {target_logits, draft_logits, draft_tokens, u_accept, u_sample};
+  const void *ins[5] = {target_lists ? static_cast<const void *>(target_lists) : target_logits,
+                        draft_logits, draft_tokens, u_accept, u_sample};
   const size_t insb[5] = {tlb, greedy ? 0 : dlb, (size_t)B * K * 4, (size_t)B * K * 4, nb};
   const void *outs[4] = {out_tokens, n_accepted, err_flags, workspace};
   const size_t outsb[4] = {ob, nb, err_flags ? nb : 0, W.total};
@@ -761,6 +834,9 @@ extern "C" sv_status spec_accept(const float *target_logits, const float *draft_
 
   AcceptArgs args;
   args.tl = target_logits;
+  args.tlists = target_lists;
+  args.tstride = target_lists ? (long long)(lists_block_bytes(G, K) / 8) : 0;
+  args.G = G;
   args.dl = draft_logits;
   args.dt = draft_tokens;
   args.ua = u_accept;
@@ -780,9 +856,10 @@ extern "C" sv_status spec_accept(const float *target_logits, const float *draft_
   args.cand = reinterpret_cast<u64 *>(ws + W.cand);
   args.rows = greedy ? K + 1 : 2 * K + 1;
   args.rows_max = 2 * K + 1;
-  args.C = (V + kChunk - 1) / kChunk;
+  args.C = C;
   args.ksel = greedy ? 1 : std::min(sampling.top_k, V);
-  args.vec = (V % 4 == 0) && aligned(target_logits, 16) && (greedy || aligned(draft_logits, 16));
+  args.vec = (V % 4 == 0) && (target_lists || aligned(target_logits, 16)) &&
+             (greedy || aligned(draft_logits, 16));
   // final-phase staging: one warp per row, C*ksel keys each, at most 48 KB
   const size_t per_row = (size_t)args.C * args.ksel * 8;
   args.rows_per_wave = (int)std::max<size_t>(
@@ -802,6 +879,44 @@ extern "C" sv_status spec_accept(const float *target_logits, const float *draft_
   dim3 grid((unsigned)args.C, (unsigned)(B * args.rows));
   spec_accept_kernel<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
   return check_launch("spec_accept");
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" sv_status spec_accept(const float *target_logits, const float *draft_logits,
+                                 const int32_t *draft_tokens, const float *u_accept,
+                                 const float *u_sample, int B, int K, int V, sv_sampling sampling,
+                                 int32_t *out_tokens, int32_t *n_accepted, int32_t *err_flags,
+                                 void *workspace, size_t workspace_bytes, sv_stream_t stream) {
+  clear_error();
+  if (!target_logits && B > 0) return fail(SV_ERR_INVALID_ARG, "spec_accept: null pointer");
+  return accept_impl(target_logits, nullptr, 0, draft_logits, draft_tokens, u_accept, u_sample,
+                     B, K, V, sampling, out_tokens, n_accepted, err_flags, workspace,
+                     workspace_bytes, stream);
+}
+
+extern "C" size_t spec_accept_lists_workspace_bytes(int B, int K, int V, int G) {
+  if (B < 0 || K < 1 || V < 1 || G < 1) return 0;
+  return ws_layout_c(B, K, (size_t)lists_chunks(V, G)).total;
+}
+
+extern "C" size_t spec_accept_lists_block_bytes(int G, int K) {
+  if (G < 1 || K < 1) return 0;
+  return lists_block_bytes(G, K);
+}
+
+extern "C" sv_status spec_accept_lists(const uint64_t *target_lists, int G,
+                                       const float *draft_logits, const int32_t *draft_tokens,
+                                       const float *u_accept, const float *u_sample, int B, int K,
+                                       int V, sv_sampling sampling, int32_t *out_tokens,
+                                       int32_t *n_accepted, int32_t *err_flags, void *workspace,
+                                       size_t workspace_bytes, sv_stream_t stream) {
+  clear_error();
+  if (!target_lists && B > 0) return fail(SV_ERR_INVALID_ARG, "spec_accept_lists: null pointer");
+  return accept_impl(nullptr, reinterpret_cast<const u64 *>(target_lists), G, draft_logits,
+                     draft_tokens, u_accept, u_sample, B, K, V, sampling, out_tokens, n_accepted,
+                     err_flags, workspace, workspace_bytes, stream);
 }
 
 // ---- spec_accept_noalloc: the same call on a fixed, statically sized scratch --

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.sv_abi_version() == 1
+    assert L.sv_abi_version() == 2
     assert L.sv_status_string(0) == b"ok"
     assert L.sv_status_string(1) == b"invalid argument"
     assert L.sv_status_string(99) == b"unknown status"
