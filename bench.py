@@ -158,9 +158,12 @@ class Cycle:
 
     def __init__(self, sv, torch, device, depth: int = 3, layers: int = wl.N_LAYERS,
                  heads: int = wl.GDN_HEADS, dim: int = wl.GDN_DIM, seed: int = 0,
-                 layout: str = "plans", weights_from=None):
+                 layout: str = "plans", weights_from=None, fused_head: bool = False):
         self.sv, self.torch, self.dev = sv, torch, device
         self.layout = layout
+        # the LM head writes per-CTA top-64 lists and accept merges them (the
+        # logits never go to memory); plan layouts only
+        self.fused_head = fused_head and layout in ("plans", "allplans")
         self.K = depth
         self.M = depth + 1
         self.layers = layers
@@ -216,6 +219,7 @@ class Cycle:
         self.ua = torch.from_numpy(ua).to(device)
         self.us = torch.from_numpy(us).to(device)
         self.ws = sv.make_accept_workspace(1, self.K, self.V, device)
+        self.topk = sv.make_topk_lists(self.M, torch.bfloat16, device) if self.fused_head else None
         self.out_tokens = torch.empty((1, self.M), device=device, dtype=torch.int32)
         self.n_acc = torch.empty((1,), device=device, dtype=torch.int32)
         self.flags = torch.empty((1,), device=device, dtype=torch.int32)
@@ -244,9 +248,15 @@ class Cycle:
             by = dict(zip(names, self.proj[layer * n:(layer + 1) * n]))
             for grp in groups:
                 self.plans.append(QmvPlan([tuple(by[k][:5]) + (False,) for k in grp]))
-        self.plans.append(QmvPlan([tuple(self.lm[:5]) + (False,)]))
+        if self.fused_head:
+            self.plans.append(QmvPlan([tuple(self.lm[:4]) + (None, False, self.topk)]))
+            self.head_grid = self.plans[-1].grid
+        else:
+            self.plans.append(QmvPlan([tuple(self.lm[:5]) + (False,)]))
         self.plan_bytes = sum(qmv_bytes(self.M, w.shape[0], w.shape[1] * 8)
                               for pl in self.plans for (w, *_rest) in pl.problems)
+        if self.fused_head:  # the head writes its lists, not M x V logits
+            self.plan_bytes += self.topk.numel() - 4 * self.M * self.V
 
     def _qmv_buffers(self, N, Kin):
         t, g, d = self.torch, self.g, self.dev
@@ -304,20 +314,26 @@ class Cycle:
         verify tokens -> o -> gate, up -> down; LM head; spec_accept; one
         tape replay committing the accepted prefix in every layer."""
         self._forward(with_gdn=True)
-        sv = self.sv
-        sv.spec_accept(self.target, self.draft, self.draft_tokens, self.ua, self.us,
-                       0.6, 20, 0.95, workspace=self.ws, out_tokens=self.out_tokens,
-                       n_accepted=self.n_acc, err_flags=self.flags)
-        sv.gdn_tape_replay(self.state, self.tape, self.n_acc, self.M, n_replay_bias=1)
+        self._accept()
+        self.sv.gdn_tape_replay(self.state, self.tape, self.n_acc, self.M, n_replay_bias=1)
+
+    def _accept(self):
+        if self.fused_head:
+            self.sv.spec_accept_lists(self.topk, self.head_grid, self.V, self.draft,
+                                      self.draft_tokens, self.ua, self.us, 0.6, 20, 0.95,
+                                      workspace=self.ws, out_tokens=self.out_tokens,
+                                      n_accepted=self.n_acc, err_flags=self.flags)
+        else:
+            self.sv.spec_accept(self.target, self.draft, self.draft_tokens, self.ua, self.us,
+                                0.6, 20, 0.95, workspace=self.ws, out_tokens=self.out_tokens,
+                                n_accepted=self.n_acc, err_flags=self.flags)
 
     def run_stream_accept(self):
         """The cycle as the weight-stream configuration lists it: every
         projection of every layer, the LM head and spec_accept (no
         GatedDeltaNet tape capture or replay)."""
         self._forward(with_gdn=False)
-        self.sv.spec_accept(self.target, self.draft, self.draft_tokens, self.ua, self.us,
-                            0.6, 20, 0.95, workspace=self.ws, out_tokens=self.out_tokens,
-                            n_accepted=self.n_acc, err_flags=self.flags)
+        self._accept()
 
     def run_qmv_only(self):
         self._forward(with_gdn=False)
@@ -552,7 +568,8 @@ def run_cycle(args):
         log(f"cpu oracle: {t1:.2f} s per cycle (extrapolated) on 1 thread")
 
     sv.set_pdl(True)
-    cyc = Cycle(sv, torch, device, depth=args.depth, seed=rank, layout=args.layout)
+    cyc = Cycle(sv, torch, device, depth=args.depth, seed=rank, layout=args.layout,
+                fused_head=args.lm_head == "fused")
     cyc.prepare_drafts()
     stream = torch.cuda.Stream(device)
     graph = capture(torch, cyc.run, stream)
@@ -651,6 +668,7 @@ def run_cycle(args):
             if k == args.depth:
                 continue
             other = Cycle(sv, torch, device, depth=k, seed=rank, layout=args.layout,
+                          fused_head=args.lm_head == "fused",
                           weights_from=cyc)
             other.prepare_drafts()
             og = capture(torch, other.run, stream)
@@ -1243,6 +1261,10 @@ def main(argv=None):
                     help="cycle: qmv plans for q,k,v / gate,up / down and qmv_smallm for o "
                          "(plans), plans for every projection (allplans), or one "
                          "qmv_smallm launch per projection (launches)")
+    ap.add_argument("--lm-head", choices=["fused", "logits"], default="logits",
+                    help="cycle: the LM-head plan writes the logits that spec_accept reads "
+                         "(logits), or keeps per-CTA top-64 lists that spec_accept_lists "
+                         "merges (fused; the logits never reach memory)")
     ap.add_argument("--shape", type=int, nargs=2, metavar=("N", "K"),
                     default=[wl.INTERMEDIATE, wl.HIDDEN],
                     help="output and input size of the --workload qmv projection")

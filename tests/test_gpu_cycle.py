@@ -1,14 +1,17 @@
 """The verify+accept cycle in the launch configuration the benchmark times:
 one CUDA graph with programmatic dependent launch; per layer a qmv plan for
 q, k, v, the GatedDeltaNet tape capture, qmv_smallm for o, a qmv plan for
-gate, up and qmv_smallm for down; then the LM-head plan (the full
+gate, up and a qmv plan for down; then the LM-head plan (the full
 151936-row vocabulary), spec_accept and one tape replay over all layers.
+The LM head either writes the logits (spec_accept reads them) or, fused,
+keeps per-CTA top-64 lists that spec_accept_lists merges.
 
 Two layers of the 27B-class shapes, every input replaced in place by the
 seeded generators, one graph replay.  Checked against the oracle: sampled
-rows of every projection, the whole LM head, the GatedDeltaNet outputs and
-tape, and each layer's committed state; the accept result must equal a
-standalone spec_accept launch on the same logits and be a valid outcome.
+rows of every projection, the LM head (every logit, or every listed logit
+and the rows' leading tokens), the GatedDeltaNet outputs and tape, and each
+layer's committed state; the accept result must equal a standalone accept
+launch on the same logits (lists) and be a valid outcome.
 """
 import numpy as np
 import pytest
@@ -50,11 +53,13 @@ def _split_tape(tape, B, Tn, H, dk, dv):
     return e, k, a
 
 
-def test_cycle_in_the_benchmark_launch_configuration(sv, oracle):
+@pytest.mark.parametrize("fused_head", [True, False])
+def test_cycle_in_the_benchmark_launch_configuration(sv, oracle, fused_head):
     M = DEPTH + 1
     sv.set_pdl(True)
     try:
-        cyc = bench.Cycle(sv, torch, dev(), depth=DEPTH, layers=LAYERS, layout="plans")
+        cyc = bench.Cycle(sv, torch, dev(), depth=DEPTH, layers=LAYERS, layout="plans",
+                          fused_head=fused_head)
         V = cyc.V
         host = []
         for i, (w_t, s_t, b_t, x_t, _) in enumerate(cyc.proj + [cyc.lm]):
@@ -101,12 +106,36 @@ def test_cycle_in_the_benchmark_launch_configuration(sv, oracle):
         rows = np.unique(np.concatenate([g.choice(N, 48, replace=False), [0, 63, 64, N - 1]]))
         assert_qmv_close(cyc.proj[i][4].cpu().numpy()[:, rows],
                          oracle.qmv(w[rows], s[rows], b[rows], x))
-    # the LM head: every row
-    assert_qmv_close(cyc.lm[4].cpu().numpy(), target_ref)
-
-    # accept: the cycle's result equals a standalone launch on the same logits
-    tok, nacc, flags = sv.spec_accept(cyc.target.clone(), cyc.draft, cyc.draft_tokens, cyc.ua,
-                                      cyc.us, T, TOP_K, TOP_P)
+    if fused_head:
+        # every listed logit against the oracle's, and each row's 20 leading
+        # tokens (ties within the tolerance excepted)
+        G = cyc.head_grid
+        raw = cyc.topk.cpu().numpy()
+        keys = raw[: G * M * 64 * 8].view(np.uint64).reshape(G, M, 64)
+        for m in range(M):
+            k = keys[:, m][keys[:, m] != 0]
+            hi = (k >> np.uint64(32)).astype(np.uint32)
+            ids = (0xFFFFFFFF - (k & np.uint64(0xFFFFFFFF))).astype(np.int64)
+            vals = np.where(hi & 0x80000000, hi & 0x7FFFFFFF, ~hi).astype(np.uint32).view(np.float32)
+            rms = np.sqrt((target_ref[m].astype(np.float64) ** 2).mean())
+            assert (np.abs(vals - target_ref[m, ids]) <= 2e-3 * np.maximum(np.abs(target_ref[m, ids]), rms)).all()
+            top = ids[np.argsort(-vals, kind="stable")][:TOP_K]
+            ref_sorted = np.sort(target_ref[m])[::-1]
+            margin = 4e-3 * max(abs(ref_sorted[0]), rms)
+            clear = ref_sorted[:TOP_K - 1] - ref_sorted[1:TOP_K] > margin
+            want = np.argsort(-target_ref[m], kind="stable")[:TOP_K]
+            for j in range(TOP_K):
+                if clear[: j + 1].all():
+                    assert top[j] == want[j]
+        # accept: the cycle's result equals a standalone launch on the same lists
+        tok, nacc, flags = sv.spec_accept_lists(cyc.topk.clone(), G, V, cyc.draft,
+                                                cyc.draft_tokens, cyc.ua, cyc.us, T, TOP_K, TOP_P)
+    else:
+        # the LM head: every row
+        assert_qmv_close(cyc.lm[4].cpu().numpy(), target_ref)
+        # accept: the cycle's result equals a standalone launch on the same logits
+        tok, nacc, flags = sv.spec_accept(cyc.target.clone(), cyc.draft, cyc.draft_tokens,
+                                          cyc.ua, cyc.us, T, TOP_K, TOP_P)
     torch.cuda.synchronize()
     assert torch.equal(tok, cyc.out_tokens) and torch.equal(nacc, cyc.n_acc)
     n = int(nacc[0])
