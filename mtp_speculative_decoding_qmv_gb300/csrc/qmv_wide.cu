@@ -462,8 +462,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       tc_fence_after();
       const uint32_t d = tmem + (uint32_t)tb * kDCols;
       for (int p = 0; p < Pt; ++p) {
-        if (!qmv::warp_wait_stage(a_full + 8u * sa, pa) ||
-            !qmv::warp_wait_stage(x_full + 8u * sx, px)) {
+        // a_full completes after the activation stage landed (the first
+        // widening warp waits for x_full before it arrives): one poll here
+        if (!qmv::warp_wait_stage(a_full + 8u * sa, pa)) {
           if (lane == 0) atomicOr(&g_wide_device_error, 8u);
           ok = false;
           break;
@@ -521,6 +522,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const uint32_t arow = tmem + lane_base + kAColBase + 16u * (uint32_t)hf;
     long long i = 0;
     uint32_t sa = 0, pa = 0, sw = 0, pw = 0;  // A slot/phase of stage i, W slot/phase
+    uint32_t sx = 0, px = 0;                  // X slot/phase (first widening warp)
     bool ok = true;
     for (int t = 0; ok && t < n_local; ++t) {
       const int n = ((int)blockIdx.x + t * (int)gridDim.x) * kTileRows + r;
@@ -602,12 +604,23 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         }
         tc_wait_st();
         tc_fence_before();
+        if (warp == kEpiWarps) {  // the stage's activations too, for the MMA warp
+          if (!qmv::warp_wait_stage(x_full + 8u * sx, px)) {
+            if (lane == 0) atomicOr(&g_wide_device_error, 128u);
+            ok = false;
+          }
+          if (++sx == (uint32_t)kXStages) {
+            sx = 0;
+            px ^= 1u;
+          }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive_u32(a_full + 8u * sa);
         if (++sa == (uint32_t)kAStages) {
           sa = 0;
           pa ^= 1u;
         }
+        if (!ok) break;
       }
     }
   } else {
