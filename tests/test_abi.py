@@ -227,3 +227,57 @@ def test_requantize_rejects(L):
     assert L.qmv_requantize(w, wp, s + 1, b, 4, 128, None) == 1    # 2-byte alignment
     assert L.qmv_requantize(w, w, s, b, 4, 128, None) == 1         # w_packed overlaps w
     assert L.qmv_requantize(w, wp, s, s, 4, 128, None) == 1        # scales = biases
+
+
+def _accept_lists(L, tl=A, G=304, dl=A + 0x1000000, dt=A + 0x2000000, ua=A + 0x2100000,
+                  us=A + 0x2200000, B=2, K=3, V=1000, T=0.6, top_k=20, top_p=0.95,
+                  out=A + 0x3000000, nacc=A + 0x3100000, flags=A + 0x3200000, ws=A + 0x4000000,
+                  ws_bytes=None):
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    if ws_bytes is None:
+        ws_bytes = max(L.spec_accept_lists_workspace_bytes(max(B, 0), max(K, 1), max(V, 1),
+                                                           max(G, 1)), 16)
+    return L.spec_accept_lists(tl, G, dl, dt, ua, us, B, K, V, sv._Sampling(T, top_k, top_p),
+                               out, nacc, flags, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"G": 0}, 2), ({"G": 4096}, 2), ({"tl": 0}, 1), ({"tl": A + 8}, 1), ({"K": 0}, 1),
+    ({"top_k": 65}, 2), ({"ws_bytes": 8}, 1), ({"out": A}, 1),
+])
+def test_accept_lists_rejects(L, kw, status):
+    assert _accept_lists(L, **kw) == status
+
+
+def test_accept_lists_sizes(L):
+    # a block per sequence: G x (K+1) x (64 keys x 8 B + one 4-byte flag), 16-byte multiple
+    assert L.spec_accept_lists_block_bytes(304, 3) == 304 * 4 * 516
+    assert L.spec_accept_lists_block_bytes(3, 1) == (3 * 2 * 516 + 15) // 16 * 16
+    assert L.spec_accept_lists_block_bytes(0, 3) == 0
+    # one chunk per 32 lists at least: more chunks than a small vocabulary fills
+    assert L.spec_accept_lists_workspace_bytes(1, 3, 151936, 304) == \
+        L.spec_accept_workspace_bytes(1, 3, 151936)
+    assert L.spec_accept_lists_workspace_bytes(1, 3, 1000, 304) > \
+        L.spec_accept_workspace_bytes(1, 3, 1000)
+    assert _accept_lists(L, B=0) == 0
+
+
+def test_plan_rejects_two_topk_problems(L):
+    import ctypes
+
+    import mtp_speculative_decoding_qmv_gb300 as sv
+
+    arr = (sv._QmvProblem * 2)()
+    for i in range(2):
+        arr[i] = sv._QmvProblem(A, A + 0x100000, A + 0x200000, A + 0x300000, None, 512, 512, 0,
+                                A + 0x1000000 * (i + 1))
+    h = ctypes.c_void_p()
+    assert L.qmv_plan_create(arr, 2, 4, 1, A + 0x8000000, 1 << 20, ctypes.byref(h)) == 2
+    assert b"top-64" in L.sv_last_error()
+    arr[0].topk = None   # neither y nor topk: a null output
+    arr[1].topk = None
+    assert L.qmv_plan_create(arr, 2, 4, 1, A + 0x8000000, 1 << 20, ctypes.byref(h)) == 1
+    arr[0].topk = A + 4  # top-k lists must be 8-byte aligned
+    assert L.qmv_plan_create(arr, 1, 4, 1, A + 0x8000000, 1 << 20, ctypes.byref(h)) == 1
+    assert L.qmv_plan_topk_bytes(0, 1) == 0 and L.qmv_plan_topk_bytes(9, 1) == 0
