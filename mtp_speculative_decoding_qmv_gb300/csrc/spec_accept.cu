@@ -53,6 +53,7 @@ constexpr int kMaxChunks = 64;                 // V <= 64 * 16384
 constexpr int kMaxK = 8;
 constexpr int kMaxRows = 2 * kMaxK + 1;
 constexpr int kStageBatch = 8;                 // candidate loads per lane in flight
+constexpr int kManySequences = 8;              // from here on, three CTAs per SM
 
 typedef unsigned long long u64;
 
@@ -323,7 +324,13 @@ __device__ int inverse_cdf_by_id(const int (&ids)[2], const float (&R)[2], float
   return result;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) spec_accept_kernel(const AcceptArgs a) {
+// kCtasPerSm: co-resident CTAs the register budget is cut for.  Three (40
+// registers, a few spilled) hide more load latency when many sequences fill
+// the GPU with chunk CTAs (batch 32: 74.0 -> 66.3 us); two keep the finish
+// path, which one CTA per sequence runs, free of spills (batch 1: 19.5
+// against 20.3 us).
+template <int kCtasPerSm>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_accept_kernel(const AcceptArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ChunkSmem &S = *reinterpret_cast<ChunkSmem *>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -871,13 +878,18 @@ sv_status accept_impl(const float *target_logits, const u64 *target_lists, int G
   static bool configured[64] = {};
   const int dev = current_device();
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(spec_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(spec_accept_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             160 * 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(spec_accept_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              160 * 1024) != cudaSuccess)
       return fail(SV_ERR_CUDA, "spec_accept: cudaFuncSetAttribute failed");
     configured[dev] = true;
   }
   dim3 grid((unsigned)args.C, (unsigned)(B * args.rows));
-  spec_accept_kernel<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+  if (B >= kManySequences)
+    spec_accept_kernel<3><<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+  else
+    spec_accept_kernel<2><<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
   return check_launch("spec_accept");
 }
 
