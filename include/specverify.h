@@ -82,13 +82,16 @@ const char *sv_status_string(int status);
 /* Message describing the most recent failure on the calling thread ("" if none). */
 const char *sv_last_error(void);
 
-/* Programmatic dependent launch (PDL) for qmv_smallm and qmv_plan_run,
- * process-wide, default 0.
+/* Programmatic dependent launch (PDL) for qmv_smallm, qmv_plan_run,
+ * qmv_wide and qmv_requantize, process-wide, default 0.
  * When enabled, such a kernel may start while the kernel enqueued before it
- * on the same stream is still running.  Before that kernel has finished it
- * reads only w_packed, scales and biases; x is read, and y written, after it
- * has finished.  Enable it only when no kernel enqueued right before such a
- * call writes those weights.  (The GatedDeltaNet kernels always start in
+ * on the same stream is still running.  Before that kernel has finished the
+ * products read only w_packed, scales and biases; x is read, and y (or the
+ * top-64 lists) written, after it has finished; qmv_requantize reads nothing
+ * before it has finished.  Enable it only when no kernel enqueued right
+ * before a product writes its weights (a qmv_requantize of those weights
+ * directly followed by the product needs PDL off for that launch, or any
+ * other kernel in between).  (The GatedDeltaNet kernels always start in
  * stream order but let the kernel after them start early.) */
 void sv_set_pdl(int enable);
 int sv_get_pdl(void);
