@@ -180,3 +180,37 @@ def test_rejections(sv):
         sv.lib().spec_accept_workspace_bytes(1, 3, 30000)
     assert sv.lib().spec_accept_lists_workspace_bytes(1, 3, 151936, 304) == \
         sv.lib().spec_accept_workspace_bytes(1, 3, 151936)
+
+
+def test_topk_problem_after_a_phase(sv):
+    """a two-phase plan: a projection, then the LM head with the top-64
+    epilogue reading its output; the lists equal those of the same head read
+    from the logits the plan writes without the epilogue"""
+    d = dev()
+    N1, K1 = 1024, 512
+    N2, K2 = 20000, 1024
+    w1, s1, b1 = wl.qmv_weights(560, N1, K1)
+    w2, s2, b2 = wl.qmv_weights(561, N2, N1)
+    x = wl.qmv_activations(560, M, K1, "f32")
+    p1 = qmv_to_device(w1, s1, b1, x)
+    wt2, st2, bt2, _ = qmv_to_device(w2, s2, b2, np.zeros((M, N1), np.float32))
+    h = torch.empty((M, N1), device=d)
+    y = torch.empty((M, N2), device=d)
+    lists = sv.make_topk_lists(M, torch.float32, d)
+    p_y = sv.QmvPlan([(*p1, h, False), (wt2, st2, bt2, h, y, True)])
+    p_t = sv.QmvPlan([(*p1, h, False), (wt2, st2, bt2, h, None, True, lists)])
+    p_y.run()
+    p_t.run()
+    p_t.run()  # twice: the lists are rebuilt, the plan's counters reset
+    torch.cuda.synchronize()
+    sv.device_status()
+    G = p_t.grid
+    keys, flags = _split(lists, G)
+    yn = y.cpu().numpy()
+    assert (flags == 0).all()
+    for m in range(M):
+        k = keys[:, m, :]
+        nz = k[k != 0]
+        vals, ids = _decode(nz)
+        assert np.array_equal(vals.view(np.uint32), yn[m, ids].astype(np.float32).view(np.uint32))
+        assert np.array_equal(np.sort(nz)[::-1][:64], np.sort(_keys_of(yn[m]))[::-1][:64])
