@@ -214,3 +214,31 @@ def test_topk_problem_after_a_phase(sv):
         vals, ids = _decode(nz)
         assert np.array_equal(vals.view(np.uint32), yn[m, ids].astype(np.float32).view(np.uint32))
         assert np.array_equal(np.sort(nz)[::-1][:64], np.sort(_keys_of(yn[m]))[::-1][:64])
+
+
+def test_two_sequences_from_stacked_blocks(sv):
+    """two sequences, each with its own fused LM-head run; their list blocks
+    stacked at spec_accept_lists_block_bytes give the same result as
+    spec_accept on the two sequences' logits"""
+    N, Kin = 30000, 512
+    d = dev()
+    runs = [_plans(sv, N, Kin, 570 + i) for i in range(2)]
+    G = runs[0][3]
+    blk = int(sv.lib().spec_accept_lists_block_bytes(G, K_DRAFT))
+    stacked = torch.zeros(2 * blk, dtype=torch.uint8, device=d)
+    for i, r in enumerate(runs):
+        n = r[2].numel()
+        assert n <= blk
+        stacked[i * blk:i * blk + n].copy_(r[2])
+    y = torch.stack([r[1] for r in runs])                       # [2, M, N]
+    draft = (y[:, :K_DRAFT] + torch.from_numpy(wl.noise(580, (2, K_DRAFT, N), 0.5)).to(d)).contiguous()
+    tokens = draft.argmax(dim=-1).to(torch.int32)               # the drafts' own top tokens
+    ua, us = wl.accept_uniforms(581, 2, K_DRAFT)
+    uat, ust = torch.from_numpy(ua).to(d), torch.from_numpy(us).to(d)
+    for T, top_k, top_p in ((0.6, 20, 0.95), (0.0, 1, 1.0)):
+        a = sv.spec_accept(y, None if T == 0 else draft, tokens, uat, ust, f32(T), top_k, f32(top_p))
+        b = sv.spec_accept_lists(stacked, G, N, None if T == 0 else draft, tokens, uat, ust, f32(T),
+                                 top_k, f32(top_p))
+        torch.cuda.synchronize()
+        for u, v in zip(a, b):
+            assert torch.equal(u, v)
