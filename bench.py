@@ -214,15 +214,23 @@ class Cycle:
         # accept: target logits = LM-head output [K+1, V] = [1][K+1][V]
         self.target = self.lm[4].view(1, self.M, self.V)
         self.draft = torch.zeros((1, self.K, self.V), device=device, dtype=f32)
-        self.draft_tokens = torch.zeros((1, self.K), device=device, dtype=torch.int32)
-        ua, us = wl.accept_uniforms(99 + seed, 1, self.K)
-        self.ua = torch.from_numpy(ua).to(device)
-        self.us = torch.from_numpy(us).to(device)
+        # the step's small inputs (draft tokens, u_accept, u_sample) and
+        # outputs (tokens, accepted count, flags) each in one 4-byte-word
+        # buffer, so that a step moves them with one copy each way
+        K = self.K
+        self.small_in = torch.zeros((2 * K + 1,), device=device, dtype=torch.int32)
+        self.draft_tokens = self.small_in[:K].view(1, K)
+        self.ua = self.small_in[K:2 * K].view(torch.float32).view(1, K)
+        self.us = self.small_in[2 * K:].view(torch.float32)
+        ua, us = wl.accept_uniforms(99 + seed, 1, K)
+        self.ua.copy_(torch.from_numpy(ua))
+        self.us.copy_(torch.from_numpy(us))
         self.ws = sv.make_accept_workspace(1, self.K, self.V, device)
         self.topk = sv.make_topk_lists(self.M, torch.bfloat16, device) if self.fused_head else None
-        self.out_tokens = torch.empty((1, self.M), device=device, dtype=torch.int32)
-        self.n_acc = torch.empty((1,), device=device, dtype=torch.int32)
-        self.flags = torch.empty((1,), device=device, dtype=torch.int32)
+        self.small_out = torch.empty((self.M + 2,), device=device, dtype=torch.int32)
+        self.out_tokens = self.small_out[:self.M].view(1, self.M)
+        self.n_acc = self.small_out[self.M:self.M + 1]
+        self.flags = self.small_out[self.M + 1:]
         self.plans = []
         if layout in ("plans", "allplans"):
             self._make_plans()
@@ -533,6 +541,7 @@ def workload_name(depth):
 
 
 def run_cycle(args):
+    import numpy as np
     import torch
 
     import mtp_speculative_decoding_qmv_gb300 as sv
@@ -617,29 +626,28 @@ def run_cycle(args):
     # draws both afresh every cycle), so the accepted lengths reported are a
     # sample mean, not one fixed draw.
     h_draft = cyc.draft.cpu().pin_memory()
-    h_tokens = cyc.sample_draft_tokens(E_DRAWS).cpu().pin_memory()
+    tokens = cyc.sample_draft_tokens(E_DRAWS).cpu().reshape(E_DRAWS, cyc.K)
     uni = [wl.accept_uniforms(1000 + 97 * rank + i, 1, cyc.K) for i in range(E_DRAWS)]
-    h_ua = torch.stack([torch.from_numpy(u[0]) for u in uni]).pin_memory()
-    h_us = torch.stack([torch.from_numpy(u[1]) for u in uni]).pin_memory()
-    h_out = torch.empty_like(cyc.out_tokens, device="cpu").pin_memory()
-    h_n = torch.empty_like(cyc.n_acc, device="cpu").pin_memory()
-    h2d = sum(t[0].numel() * t.element_size() for t in (h_tokens, h_ua, h_us))
-    h2d += h_draft.numel() * h_draft.element_size()
-    d2h = h_out.numel() * 4 + h_n.numel() * 4
+    # per draw, the step's small inputs packed as the device buffer holds them
+    h_small = torch.empty((E_DRAWS, 2 * cyc.K + 1), dtype=torch.int32).pin_memory()
+    for i, (ua_i, us_i) in enumerate(uni):
+        h_small[i, :cyc.K] = tokens[i]
+        h_small[i, cyc.K:].view(torch.float32).copy_(
+            torch.from_numpy(np.concatenate([ua_i.reshape(-1), us_i.reshape(-1)])))
+    h_out = torch.empty_like(cyc.small_out, device="cpu").pin_memory()
+    h2d = h_small[0].numel() * 4 + h_draft.numel() * h_draft.element_size()
+    d2h = h_out.numel() * 4
     accepted = []
 
     def e2e_step():
         i = len(accepted) % E_DRAWS
         with torch.cuda.stream(stream):
             cyc.draft.copy_(h_draft, non_blocking=True)
-            cyc.draft_tokens.copy_(h_tokens[i], non_blocking=True)
-            cyc.ua.copy_(h_ua[i], non_blocking=True)
-            cyc.us.copy_(h_us[i], non_blocking=True)
+            cyc.small_in.copy_(h_small[i], non_blocking=True)
             graph.replay()
-            h_out.copy_(cyc.out_tokens, non_blocking=True)
-            h_n.copy_(cyc.n_acc, non_blocking=True)
+            h_out.copy_(cyc.small_out, non_blocking=True)
         stream.synchronize()
-        accepted.append(int(h_n[0]))
+        accepted.append(int(h_out[cyc.M]))
 
     for _ in range(args.warmup):
         e2e_step()
