@@ -33,6 +33,10 @@
 //    is ready for the next launch.
 // The per-group math (nibble widening, bf16 MMA, scale/bias epilogue) is the
 // one of qmv_smallm (qmv_common.cuh).
+// One problem may carry a top-64 epilogue instead of y: the epilogue warp
+// merges each finished tile's values into per-output-row sorted lists of
+// (logit, index) keys in shared memory and every CTA writes its lists at the
+// end (the fused LM head that spec_accept_lists reads).
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>

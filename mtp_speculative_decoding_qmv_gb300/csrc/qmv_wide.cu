@@ -1,5 +1,6 @@
 // qmv_wide.cu -- the 4-bit affine (group 64) product for wide verify blocks,
-// M = 17..128 activation rows, on the 5th-generation tensor cores, sm_103a.
+// up to 128 activation rows (meant for 17..128; qmv_smallm is the faster
+// path at 16 or fewer), on the 5th-generation tensor cores, sm_103a.
 //
 // Sources: "MTP in llama.cpp", section "Theoretical maximum tg t/s" (the
 // verify step streams the quantised weights once per cycle, whatever the

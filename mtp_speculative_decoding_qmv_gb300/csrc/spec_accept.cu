@@ -30,6 +30,12 @@
 //    token-id order, bonus token.
 // The workspace counters are reset by the last CTA, so each completed call
 // leaves the workspace ready for the next.
+//
+// spec_accept_lists takes the target rows as the per-CTA top-64 lists of a
+// fused LM head ("MTP in llama.cpp": one evaluation boundary per cycle, the
+// logits never travel through memory): a target row's chunk CTA then merges
+// at most 32 of those sorted lists into its top-k instead of reading logits,
+// and everything after the chunk phase is the same.
 #include <cuda_runtime.h>
 
 #include <algorithm>
