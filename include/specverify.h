@@ -325,9 +325,10 @@ sv_status qmv_wide(const uint32_t *w_packed, const uint16_t *scales, const uint1
  * temperature > 0 then 1 <= top_k <= 64 and 0 < top_p <= 1.  No output may
  * overlap an input or another output.
  * workspace: device memory of spec_accept_workspace_bytes(B, K, V) bytes,
- * 16-byte aligned, zero-filled before its first use; each completed call
- * leaves it ready for the next.  Calls that run concurrently must use
- * different workspaces. */
+ * 16-byte aligned, with no required contents: every call first clears the
+ * counter words it needs (a memset on `stream`), so one workspace serves
+ * calls of any shape it is large enough for.  Calls that run concurrently
+ * must use different workspaces. */
 typedef struct {
     float temperature; /* 0 => greedy */
     int top_k;         /* 1..64 (ignored when temperature == 0) */
@@ -374,8 +375,9 @@ sv_status spec_accept_lists(const uint64_t *target_lists, int G, const float *dr
  * own, or a decode loop that must not call cudaMalloc / cudaFree per step
  * (cudaFree synchronises the device).
  * Arguments, outputs, flags and results are those of spec_accept without the
- * workspace pair; every call clears the scratch's counters and row flags on
- * `stream` before the kernel.
+ * workspace pair; like every spec_accept call it clears the counter words
+ * it needs on `stream` before the kernel, whatever shape the previous call
+ * on the scratch had.
  * Errors: SV_ERR_UNSUPPORTED when spec_accept_workspace_bytes(B, K, V)
  * exceeds the scratch size (nothing is launched; use spec_accept with a
  * caller workspace); SV_ERR_CUDA when the scratch address cannot be looked
@@ -401,10 +403,11 @@ sv_status spec_accept_noalloc(const float *target_logits, const float *draft_log
  * exact); "MTP와 DFlash" (mlxcel manual), section "Qwen3.8-Flash-Next
  * (qwen4_exp) MTP" (rollback replays the GatedDeltaNet recurrence over the
  * accepted tokens).  The update is the gated delta rule, per (b, h) with
- * S in R^{dv x dk}, in this order (fp32, no fused multiply-add in the state
- * update):
+ * S in R^{dv x dk}, in this order (fp32):
  *     S' = alpha_t * S;   u = S' k_t;   e_t = beta_t * (v_t - u);
  *     S_t = S' + e_t k_t^T;   o_t = S_t q_t.
+ * The state update rounds alpha_t * S, then adds e_t[i] * k_t[j] with one
+ * fused multiply-add per element (capture and replay alike).
  * Tape record (b,t,h) = (alpha_t, e_t, k_t).  Tape layout, fp32, in one
  * buffer of gdn_tape_bytes(B,T,H,dk,dv) bytes: B blocks of
  * F = T*H*(dv+dk) + 4*ceil(T*H/4) floats, block b at float offset b*F holding

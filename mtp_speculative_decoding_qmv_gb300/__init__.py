@@ -430,10 +430,11 @@ def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor | None,
     _need(n_accepted, "n_accepted", torch.int32, (B,), dev)
     _need(err_flags, "err_flags", torch.int32, (B,), dev)
     samp = _Sampling(float(temperature), int(top_k), float(top_p))
-    st = lib().spec_accept(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
-                           _ptr(u_accept), _ptr(u_sample), B, K, V, samp, _ptr(out_tokens),
-                           _ptr(n_accepted), _ptr(err_flags), _ptr(workspace),
-                           workspace.numel(), _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib().spec_accept(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
+                               _ptr(u_accept), _ptr(u_sample), B, K, V, samp, _ptr(out_tokens),
+                               _ptr(n_accepted), _ptr(err_flags), _ptr(workspace),
+                               workspace.numel(), _stream(dev))
     _check(st, "spec_accept")
     return out_tokens, n_accepted, err_flags
 
@@ -473,10 +474,12 @@ def spec_accept_lists(target_lists: torch.Tensor, G: int, V: int,
     _need(n_accepted, "n_accepted", torch.int32, (B,), dev)
     _need(err_flags, "err_flags", torch.int32, (B,), dev)
     samp = _Sampling(float(temperature), int(top_k), float(top_p))
-    st = lib().spec_accept_lists(_ptr(target_lists), int(G), _ptr(draft_logits),
-                                 _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), B, K, V,
-                                 samp, _ptr(out_tokens), _ptr(n_accepted), _ptr(err_flags),
-                                 _ptr(workspace), workspace.numel(), _stream(dev))
+    with torch.cuda.device(dev):
+        st = lib().spec_accept_lists(_ptr(target_lists), int(G), _ptr(draft_logits),
+                                     _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), B, K,
+                                     V, samp, _ptr(out_tokens), _ptr(n_accepted),
+                                     _ptr(err_flags), _ptr(workspace), workspace.numel(),
+                                     _stream(dev))
     _check(st, "spec_accept_lists")
     return out_tokens, n_accepted, err_flags
 
@@ -507,10 +510,12 @@ def spec_accept_noalloc(target_logits: torch.Tensor, draft_logits: torch.Tensor 
     if err_flags is not None:
         _need(err_flags, "err_flags", torch.int32, (B,), dev)
     samp = _Sampling(float(temperature), int(top_k), float(top_p))
-    st = lib().spec_accept_noalloc(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
-                                   _ptr(u_accept), _ptr(u_sample), B, K, V, samp,
-                                   _ptr(out_tokens), _ptr(n_accepted), _ptr(err_flags),
-                                   _stream(dev))
+    # the scratch is looked up on the current device: make it the tensors' one
+    with torch.cuda.device(dev):
+        st = lib().spec_accept_noalloc(_ptr(target_logits), _ptr(draft_logits),
+                                       _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), B, K,
+                                       V, samp, _ptr(out_tokens), _ptr(n_accepted),
+                                       _ptr(err_flags), _stream(dev))
     _check(st, "spec_accept_noalloc")
 
 

@@ -741,13 +741,13 @@ extern "C" sv_status qmv_wide(const uint32_t *w_packed, const uint16_t *scales,
   const uint32_t smem = wide_layout().total + 1024u;  // + alignment slack
   if (smem > (uint32_t)optin)
     return fail(SV_ERR_UNSUPPORTED, "qmv_wide: needs %u bytes of shared memory", smem);
-  static bool configured[64] = {};
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(qmv_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return fail(SV_ERR_CUDA, "qmv_wide: cudaFuncSetAttribute failed");
-    configured[dev] = true;
-  }
+  static PerDeviceOnce attrs_once;
+  const cudaError_t ce = attrs_once.run([&] {
+    return cudaFuncSetAttribute(qmv_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem);
+  });
+  if (ce != cudaSuccess)
+    return fail(SV_ERR_CUDA, "qmv_wide: cudaFuncSetAttribute failed: %s", cudaGetErrorString(ce));
 
   WideArgs args{scales, biases, y, M, N, K, K / kGroup, wide_bias_stages(K), (M + 15) / 16 * 16};
   const int kb = args.E * kGroup;

@@ -28,8 +28,8 @@
 //    softmax over the kept logits, top-p cut on the descending order,
 //    u < p/q test, residual (p - q)+ sampled by inverse CDF in ascending
 //    token-id order, bonus token.
-// The workspace counters are reset by the last CTA, so each completed call
-// leaves the workspace ready for the next.
+// Each call clears the workspace's counter words on the stream before the
+// launch, so a workspace needs no preparation and may be reused at any shape.
 //
 // spec_accept_lists takes the target rows as the per-CTA top-64 lists of a
 // fused LM head ("MTP in llama.cpp": one evaluation boundary per cycle, the
@@ -881,16 +881,23 @@ sv_status accept_impl(const float *target_logits, const u64 *target_lists, int G
                              (size_t)kMaxRows * 64 * 8 + (kMaxRows + 1) * 4 +
                              std::max<size_t>((size_t)args.rows_per_wave * per_row, 64 * 8);
   const size_t smem = std::max(sizeof(ChunkSmem), final_bytes);
-  static bool configured[64] = {};
-  const int dev = current_device();
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(spec_accept_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             160 * 1024) != cudaSuccess ||
-        cudaFuncSetAttribute(spec_accept_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             160 * 1024) != cudaSuccess)
-      return fail(SV_ERR_CUDA, "spec_accept: cudaFuncSetAttribute failed");
-    configured[dev] = true;
-  }
+  static PerDeviceOnce attrs_once;
+  const cudaError_t ce = attrs_once.run([] {
+    cudaError_t e = cudaFuncSetAttribute(spec_accept_kernel<2>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(spec_accept_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               160 * 1024);
+    return e;
+  });
+  if (ce != cudaSuccess)
+    return fail(SV_ERR_CUDA, "spec_accept: cudaFuncSetAttribute failed: %s", cudaGetErrorString(ce));
+  // Counters and row flags start at zero.  Where they sit depends on B and
+  // K, and a completed call clears only its own, so a workspace last used at
+  // another shape may hold candidate keys there: clear them on the stream.
+  if (cudaMemsetAsync(workspace, 0, W.cand, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return fail(SV_ERR_CUDA, "spec_accept: clearing the workspace counters failed: %s",
+                cudaGetErrorString(cudaGetLastError()));
   dim3 grid((unsigned)args.C, (unsigned)(B * args.rows));
   if (B >= kManySequences)
     spec_accept_kernel<3><<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
@@ -999,10 +1006,8 @@ extern "C" sv_status spec_accept_noalloc(const float *target_logits, const float
   void *scratch = nullptr;
   const sv_status st = static_scratch(&scratch);
   if (st != SV_OK) return st;
-  // counters and row flags must start at zero (a completed call leaves them
-  // so; clearing them here also covers a call that never completed)
-  if (cudaMemsetAsync(scratch, 0, W.cand, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return fail(SV_ERR_CUDA, "spec_accept_noalloc: clearing the scratch counters failed");
+  // spec_accept clears the counter words it needs on the stream, whatever
+  // shape the previous call on the scratch had
   return spec_accept(target_logits, draft_logits, draft_tokens, u_accept, u_sample, B, K, V,
                      sampling, out_tokens, n_accepted, err_flags, scratch, kStaticScratchBytes,
                      stream);

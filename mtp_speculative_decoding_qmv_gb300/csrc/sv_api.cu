@@ -12,7 +12,7 @@ namespace sv {
 namespace {
 thread_local char g_msg[512] = "";
 std::atomic<int> g_pdl{0};
-int g_sm_count[64] = {};
+std::atomic<int> g_sm_count[64] = {};
 }  // namespace
 
 sv_status fail(sv_status st, const char *fmt, ...) {
@@ -36,12 +36,13 @@ int current_device() {
 int device_sm_count() {
   const int d = current_device();
   if (d < 0 || d >= 64) return 1;
-  if (g_sm_count[d] == 0) {
-    int n = 0;
+  int n = g_sm_count[d].load(std::memory_order_relaxed);
+  if (n == 0) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
-    g_sm_count[d] = n > 0 ? n : 1;
+    if (n < 1) n = 1;
+    g_sm_count[d].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[d];
+  return n;
 }
 
 sv_status check_launch(const char *what) {

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "specverify.h"
 
 namespace sv {
@@ -24,6 +26,22 @@ inline bool overlaps(const void *a, size_t an, const void *b, size_t bn) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + bn && y < x + an;
 }
+
+// Per-device one-time set-up (function attributes): the first call on each
+// device runs fn with that device current, later calls (from any host
+// thread) return its result.
+struct PerDeviceOnce {
+  static constexpr int kDevices = 64;
+  std::once_flag flag[kDevices];
+  cudaError_t result[kDevices] = {};
+  template <class F>
+  cudaError_t run(F fn) {
+    const int d = current_device();
+    if (d < 0 || d >= kDevices) return fn();
+    std::call_once(flag[d], [&] { result[d] = fn(); });
+    return result[d];
+  }
+};
 
 // Checks cudaPeekAtLastError after a launch.
 sv_status check_launch(const char *what);

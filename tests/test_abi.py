@@ -69,7 +69,7 @@ def _qmv(L, w=A, s=A + 0x1000000, b=A + 0x2000000, x=A + 0x3000000, dt=1, y=A + 
 
 @pytest.mark.parametrize("kw,status", [
     ({"K": 100}, 1), ({"K": 0}, 1), ({"M": -1}, 1), ({"gs": 32}, 2), ({"bits": 8}, 2),
-    ({"M": 9}, 2), ({"dt": 7}, 1), ({"w": 0}, 1), ({"y": 0}, 1), ({"w": A + 4}, 1),
+    ({"M": 17}, 2), ({"dt": 7}, 1), ({"w": 0}, 1), ({"y": 0}, 1), ({"w": A + 4}, 1),
     ({"x": A + 0x3000008}, 1), ({"y": A + 2}, 1), ({"y": A + 0x3000000}, 1),
 ])
 def test_qmv_rejects(L, kw, status):

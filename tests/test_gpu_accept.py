@@ -123,6 +123,26 @@ def test_workspace_reuse_and_repeat(sv, oracle):
     assert int(ws[: 4 * B].view(torch.int32).abs().sum()) == 0  # counters reset
 
 
+def test_workspace_reused_across_shapes(sv, oracle):
+    """One workspace, sized for the largest call, serves calls of other
+    shapes in any order: batch 32 at K = 3, then batch 1 at K = 5 (its
+    counter words sit where the first call left candidate keys), then batch
+    32 at K = 3 again, each against the oracle."""
+    T, top_k, top_p = f32(0.6), 20, f32(0.95)
+    V = 12000
+    shapes = [(32, 3), (1, 5), (32, 3), (4, 8), (32, 3)]
+    ws_bytes = max(sv.spec_accept_workspace_bytes(B, K, V) for B, K in shapes)
+    ws = torch.full((ws_bytes,), 0xA5, dtype=torch.uint8, device=dev())  # never zeroed
+    for i, (B, K) in enumerate(shapes):
+        tl, dl = wl.accept_logits(60 + i, B, K, V, sigma=3.0, draft_noise=0.5)
+        dr = _drafts_from_q(oracle, dl, T, top_k, top_p, 60 + i)
+        ua, us = wl.accept_uniforms(60 + i, B, K)
+        r = oracle.spec_accept(tl, dl, dr, ua, us, T, top_k, top_p)
+        gpu = _gpu(sv, tl, dl, dr, ua, us, T, top_k, top_p, ws=ws)
+        _compare(r, gpu, dr, V)
+    sv.device_status()
+
+
 def test_error_flags_and_masks(sv, oracle):
     B, K, V = 8, 3, 5000
     T, top_k, top_p = f32(0.9), 12, f32(0.97)

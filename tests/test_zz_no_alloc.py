@@ -65,6 +65,26 @@ def test_noalloc_matches_workspace_entry_point(sv, B, K, V, T, top_k, top_p, sig
     sv.device_status()  # raises if a kernel reported a device error
 
 
+def test_noalloc_shape_changes_on_the_shared_scratch(sv):
+    """Calls of different shapes in a row on the one scratch: batch 32 at
+    K = 3, then batch 1 at K = 5, then batch 32 at K = 3 again.  Each must
+    equal spec_accept on its own fresh workspace, whatever the previous call
+    left in the scratch."""
+    V, T, top_k, top_p = 151936, f32(0.6), 20, f32(0.95)
+    d = dev()
+    for call, (B, K) in enumerate([(32, 3), (1, 5), (32, 3)]):
+        assert sv.spec_accept_workspace_bytes(B, K, V) <= sv.spec_accept_noalloc_scratch_bytes()
+        x = _inputs(970 + call, B, K, V, 3.0, 0.5)
+        ref = _with_workspace(sv, x, T, top_k, top_p)
+        outs = [torch.full((B, K + 1), -7, dtype=torch.int32, device=d),
+                torch.full((B,), -7, dtype=torch.int32, device=d),
+                torch.full((B,), -7, dtype=torch.int32, device=d)]
+        got = _noalloc(sv, x, T, top_k, top_p, outs)
+        for name, r, g in zip(("out_tokens", "n_accepted", "err_flags"), ref, got):
+            np.testing.assert_array_equal(g, r, err_msg=f"call {call} (B={B}, K={K}): {name}")
+    sv.device_status()
+
+
 def test_noalloc_rejects_sizes_beyond_the_scratch(sv):
     B, K, V = 64, 8, 151936
     assert sv.spec_accept_workspace_bytes(B, K, V) > sv.spec_accept_noalloc_scratch_bytes()
