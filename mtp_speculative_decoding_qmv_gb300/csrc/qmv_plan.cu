@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init_u32(full0 + 8u * i, 1);
-      mbar_init_u32(empty0 + 8u * i, kConsumerWarps);
+      mbar_init_u32(empty0 + 8u * i, kConsumerWarps * 32);  // every consumer lane
     }
     mbar_init_u32(red_full, kConsumerWarps * 32);
     mbar_init_u32(red_empty, 32);
@@ -479,8 +479,10 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     const int i_end = runs.n;
     int i = 0;
     int cur_phase = -1;
-    bool have_x = false;  // xnext holds the first stage of segment i
-    XRaw<kXF32> xnext;
+    // the activation side of the next stage to process (B fragments and
+    // sum of x), formed at the end of the stage before it
+    bool have_x = false;
+    XFrag<kXF32> xf;
     PlanSeg s;
     if (i < i_end) s = runs[0];
     while (i < i_end) {
@@ -496,35 +498,37 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
         have_x = false;
       }
       const void *xrow = static_cast<const uint8_t *>(s.x) + (size_t)xm * s.K * xbytes;
-      if (!have_x) xnext = load_x_l2<kXF32>(xrow, s.c0 * kConsumerWarps + gl, t);
+      if (!have_x) prepare_x<kXF32>(xf, load_x_l2<kXF32>(xrow, s.c0 * kConsumerWarps + gl, t));
       // the next run, for the activation prefetch (same phase only)
       const bool have2 = i + 1 < i_end;
       PlanSeg s2 = s;
       if (have2) s2 = runs[i + 1];
       const bool same = have2 && s2.phase == s.phase;
+      const void *xrow2 = static_cast<const uint8_t *>(s2.x) + (size_t)xm * s2.K * xbytes;
       int g = s.c0 * kConsumerWarps + gl;
       for (int c = s.c0; c < s.c1; ++c, g += kConsumerWarps) {
-        const XRaw<kXF32> xcur = xnext;
-        if (c + 1 < s.c1)
-          xnext = load_x_l2<kXF32>(xrow, g + kConsumerWarps, t);
-        else if (same)
-          xnext = load_x_l2<kXF32>(static_cast<const uint8_t *>(s2.x) + (size_t)xm * s2.K * xbytes,
-                                   s2.c0 * kConsumerWarps + gl, t);
+        // the next stage's activations fly during this stage's work
+        const bool more = c + 1 < s.c1;
+        const bool next = more || same;
+        XRaw<kXF32> xraw;
+        if (next)
+          xraw = load_x_l2<kXF32>(more ? xrow : xrow2,
+                                  more ? g + kConsumerWarps : s2.c0 * kConsumerWarps + gl, t);
         if (ok && !warp_wait_stage(full0 + 8u * st, ph)) {
           ok = false;
           if (lane == 0) atomicOr(&g_plan_device_error, 2u);
         }
         if (ok) {
           const uint32_t stage = base + st * kStageBytesStream;
-          group_math<kXF32>(acc, stage + ldm_off, xcur, stage + sb_off, 16 * 16, 8 * 16,
-                            kRows * 16);
+          group_math_xf<kXF32>(acc, stage + ldm_off, xf, stage + sb_off, 16 * 16, 8 * 16,
+                               kRows * 16);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
+        mbar_arrive_u32(empty0 + 8u * st);
         if (++st == stages) {
           st = 0;
           ph ^= 1;
         }
+        if (next) prepare_x<kXF32>(xf, xraw);
       }
       // hand the run's sums to the epilogue warp: red[warp][row][col]
       if (nseg > 0 && !__all_sync(0xffffffffu, mbar_wait_u32(red_empty, (nseg - 1) & 1)) &&

@@ -32,13 +32,17 @@
 //    stage ahead; warps reduce through shared memory at the end in a fixed
 //    order;
 //  * each weight is read from shared memory once (ldmatrix on the swizzled
-//    box: conflict-free) and used for all M rows: nibbles are widened in
-//    registers to bf16 (128 + q, exact) and fed to the tensor cores as the
-//    16-row A operand of mma.m16n8k16 with the (<= 8) activation rows as B;
-//    per group the fp32 result is scaled,
-//        acc += s * D + (b - 128 s) * sum(x),
-//    with sum(x) taken from an all-ones MMA.  Products are exact, the
-//    accumulation is fp32.  CUDA-core FMAs alone cannot keep up with the HBM
+//    box: conflict-free) and used for all M rows: nibbles are widened to
+//    bf16 (128 + q, exact) and fed to the tensor cores as the 16-row A
+//    operand of mma.m16n8k16 with the (<= 8) activation rows as B.  When K
+//    is a multiple of 128 the boxes are byte-expanded (the copy engine leaves
+//    a gap after every 8 bytes and ldmatrix.b4x16_p64 widens each nibble to
+//    a byte: one byte permute per two weights); otherwise packed boxes are
+//    widened with shifts and masks.  The format depends only on K and the
+//    weights' alignment, so every M of one matrix shares the arithmetic.
+//    Per group D = -128 sum(x) + sum (128 + q) x, the offset being the first
+//    MMA's accumulator, and acc += s * D + b * sum(x), with sum(x) taken from
+//    an all-ones MMA.  Products are exact, the accumulation is fp32.  CUDA-core FMAs alone cannot keep up with the HBM
 //    stream at M >= 2 on this part (4 FMAs + unpack per weight per row
 //    against ~3.3 issue slots per streamed weight); the MMA path costs the
 //    same at every M.
@@ -49,6 +53,7 @@
 //    preceding kernel on the stream ends; activations are read, and y
 //    written, only after griddepcontrol.wait.
 #include <algorithm>
+#include <atomic>
 
 #include "qmv_common.cuh"
 
@@ -86,10 +91,12 @@ __host__ __device__ inline uint32_t round_up_u32(uint32_t v, uint32_t a) {
 // [stages] then, if not streamed, the tile's scale/bias block, then the
 // mbarriers.  The end-of-kernel reductions reuse the drained ring (at least
 // kRedBytes long per 8 activation rows).  `total` includes 1 KB of
-// alignment slack.
-__host__ __device__ inline Layout qmv_layout(int groups, int stages, bool sb_stream, int nt) {
+// alignment slack.  p64: byte-expandable weight boxes (K % 128 == 0).
+__host__ __device__ inline Layout qmv_layout(int groups, int stages, bool sb_stream, int nt,
+                                             bool p64) {
   Layout L;
-  L.stage = sb_stream ? kStageBytesStream : kStageBytesBlock;
+  L.stage = p64 ? (sb_stream ? kStageBytesP64 : kStageBytesP64Block)
+                : (sb_stream ? kStageBytesStream : kStageBytesBlock);
   const uint32_t ring = (uint32_t)stages * L.stage;
   const uint32_t red = kRedBytes * (uint32_t)nt;
   L.sb = (ring > red ? ring : red);
@@ -120,21 +127,27 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 // Producer: expect chunk c's bytes on stage st's barrier and issue its boxes.
 // Rows past N, inputs past K and groups past K/64 are zero-filled by the copy
 // engine and still counted in the transaction bytes.
-template <bool kStream>
+template <bool kStream, bool kP64>
 __device__ __forceinline__ void issue_stage(const QmvArgs &a, const CUtensorMap *wmap,
                                             const CUtensorMap *smap, const CUtensorMap *bmap,
                                             uint32_t stage_addr, uint32_t bar, int c, int n0,
                                             uint64_t policy) {
   const int k0 = c * kStageInputs;
   const int kn = min(kStageInputs, a.K - k0);
-  const int boxes = (kn + kBoxWords * 8 - 1) / (kBoxWords * 8);
-  const uint32_t bytes = (uint32_t)(boxes * kRows * 128 + (kStream ? 2 * kRows * 16 : 0));
+  constexpr int kBoxInputs = kP64 ? kP64BoxInputs : kBoxWords * 8;
+  const int boxes = (kn + kBoxInputs - 1) / kBoxInputs;
+  // byte-expandable boxes take 8 KB of shared memory for 4 KB transferred
+  constexpr uint32_t kBoxSmem = kP64 ? kP64BoxBytes : kRows * 128;
+  constexpr uint32_t kBoxTx = kP64 ? kP64BoxTx : kRows * 128;
+  const uint32_t bytes = (uint32_t)(boxes * kBoxTx + (kStream ? 2 * kRows * 16 : 0));
   mbar_arrive_expect_tx_u32(bar, bytes);
   for (int bx = 0; bx < boxes; ++bx)
-    tma_load_2d(stage_addr + bx * kRows * 128, wmap, k0 / 8 + bx * kBoxWords, n0, bar, policy);
+    tma_load_2d(stage_addr + bx * kBoxSmem, wmap,
+                kP64 ? k0 + bx * kP64BoxInputs : k0 / 8 + bx * kBoxWords, n0, bar, policy);
   if (kStream) {
-    tma_load_2d(stage_addr + kSbOff, smap, k0 / 64, n0, bar, policy);
-    tma_load_2d(stage_addr + kSbOff + kRows * 16, bmap, k0 / 64, n0, bar, policy);
+    constexpr uint32_t kSb = kP64 ? kP64SbOff : kSbOff;
+    tma_load_2d(stage_addr + kSb, smap, k0 / 64, n0, bar, policy);
+    tma_load_2d(stage_addr + kSb + kRows * 16, bmap, k0 / 64, n0, bar, policy);
   }
 }
 
@@ -143,7 +156,9 @@ __device__ __forceinline__ void issue_stage(const QmvArgs &a, const CUtensorMap 
 // loaded once and groups past K/64 are skipped.
 //
 // kNT: 8-row MMA n-tiles of activation rows (1: M <= 8, 2: M <= 16).
-template <bool kXF32, bool kStream, int kNT>
+// kP64: byte-expandable weight boxes (K % 128 == 0, weights 32-byte aligned);
+// otherwise packed boxes widened with shifts and masks.
+template <bool kXF32, bool kStream, int kNT, bool kP64>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm<kNT>)
     qmv_smallm_kernel(const __grid_constant__ CUtensorMap wmap,
                       const __grid_constant__ CUtensorMap smap,
@@ -163,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm<kNT>)
   const int c_begin = (int)((long long)split * n_chunks / splits);
   const int c_end = (int)((long long)(split + 1) * n_chunks / splits);
   const int stages = a.stages;
-  const Layout L = qmv_layout(groups, stages, kStream, kNT);
+  const Layout L = qmv_layout(groups, stages, kStream, kNT, kP64);
   constexpr int kCols = 8 * kNT;          // activation rows a CTA's sums cover
   constexpr int kParts = 2 * kNT;         // output elements per consumer thread
   const uint32_t full0 = base + L.bar;          // full[i]  = full0 + 8 i
@@ -221,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm<kNT>)
                                 ((i - c_begin) / stages) & 1);
           break;
         }
-        issue_stage<kStream>(a, &wmap, &smap, &bmap, base + st * L.stage, full0 + 8u * st, c, n0,
-                    policy);
+        issue_stage<kStream, kP64>(a, &wmap, &smap, &bmap, base + st * L.stage, full0 + 8u * st,
+                                   c, n0, policy);
         if (++st == stages) {
           st = 0;
           ph ^= 1;
@@ -235,17 +250,32 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm<kNT>)
     // ------------------------------ consumers -----------------------------
     const int g8 = lane >> 2, t = lane & 3;  // fragment row (= activation row m) and column
     const int gl = warp;  // the stage's group this warp reduces
-    const uint32_t ldm_off = ldmatrix_offset(gl, lane);
+    uint32_t ldm_off = 0, ldm_off2 = 0;
+    if constexpr (kP64)
+      ldmatrix_p64_offsets(gl, lane, ldm_off, ldm_off2);
+    else
+      ldm_off = ldmatrix_offset(gl, lane);
     // scale / bias of rows g8 and g8+8 of tile 0, group gl (streamed layout)
-    const uint32_t sb_off = kSbOff + (uint32_t)(g8 * 16 + gl * 2);
+    const uint32_t sb_off = (kP64 ? kP64SbOff : kSbOff) + (uint32_t)(g8 * 16 + gl * 2);
     const uint32_t blk = base + L.sb;  // whole-tile block (not streamed)
-    // lanes of padding columns (m >= M) read row 0; their sums are never
-    // stored.  n-tile nt covers activation rows 8 nt .. 8 nt + 7.
+    // n-tile nt covers activation rows 8 nt .. 8 nt + 7; lanes of padding
+    // columns (m >= M) load nothing (byte-expanded format) or row 0 (packed
+    // format); their sums are never stored
     const void *xrow[kNT];
+    bool xvalid[kNT];
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
+    for (int nt = 0; nt < kNT; ++nt) {
+      xvalid[nt] = 8 * nt + g8 < a.M;
       xrow[nt] = static_cast<const uint8_t *>(a.x) +
-                 (size_t)(8 * nt + g8 < a.M ? 8 * nt + g8 : 0) * a.K * (kXF32 ? 4 : 2);
+                 (size_t)(xvalid[nt] ? 8 * nt + g8 : 0) * a.K * (kXF32 ? 4 : 2);
+    }
+    using XR = typename std::conditional<kP64, XRawP<kXF32>, XRaw<kXF32>>::type;
+    auto load = [&](int nt, int grp) -> XR {
+      if constexpr (kP64)
+        return load_x_p64<kXF32>(xrow[nt], xvalid[nt], grp, t);
+      else
+        return load_x<kXF32>(xrow[nt], true, grp, t);
+    };
     float acc[kNT][kTiles][4];
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt)
@@ -258,19 +288,18 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm<kNT>)
     int g = c_begin * kConsumerWarps + gl;
     // groups past K/64 (last stage of a ragged K) read a real group's
     // activations; their weights are skipped
-    XRaw<kXF32> xnext[kNT];
+    XR xnext[kNT];
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
-      xnext[nt] = load_x<kXF32>(xrow[nt], true, kStream ? g : min(g, groups - 1), t);
+    for (int nt = 0; nt < kNT; ++nt) xnext[nt] = load(nt, kStream ? g : min(g, groups - 1));
     int st = 0, ph = 0;  // stage of chunk c and the parity of its fill
     for (int c = c_begin; ok && c < c_end; ++c, g += kConsumerWarps) {
-      XRaw<kXF32> xcur[kNT];
+      XR xcur[kNT];
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) xcur[nt] = xnext[nt];
       // next stage's activations: the loads fly during this stage's work
       const int gn = min(g + kConsumerWarps, groups - 1);
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) xnext[nt] = load_x<kXF32>(xrow[nt], true, gn, t);
+      for (int nt = 0; nt < kNT; ++nt) xnext[nt] = load(nt, gn);
       if (!warp_wait_stage(full0 + 8u * st, ph)) {
         ok = false;
         break;
@@ -284,10 +313,19 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm<kNT>)
       const uint32_t srt = kStream ? 16 * 16 : 16 * gb, sr8 = kStream ? 8 * 16 : 8 * gb;
       const uint32_t sbb = kStream ? kRows * 16 : kRows * gb;
       if (real) {
-        if constexpr (kNT == 1)
-          group_math<kXF32>(acc[0], stage + ldm_off, xcur[0], sbp, srt, sr8, sbb);
-        else
-          group_math_x2<kXF32>(acc, stage + ldm_off, xcur, sbp, srt, sr8, sbb);
+        if constexpr (kP64) {
+          if constexpr (kNT == 1)
+            group_math_p64<kXF32>(acc[0], stage + ldm_off, stage + ldm_off2, xcur[0], sbp, srt,
+                                  sr8, sbb);
+          else
+            group_math_p64_x2<kXF32>(acc, stage + ldm_off, stage + ldm_off2, xcur, sbp, srt, sr8,
+                                     sbb);
+        } else {
+          if constexpr (kNT == 1)
+            group_math<kXF32>(acc[0], stage + ldm_off, xcur[0], sbp, srt, sr8, sbb);
+          else
+            group_math_x2<kXF32>(acc, stage + ldm_off, xcur, sbp, srt, sr8, sbb);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
@@ -360,45 +398,45 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm<kNT>)
 }
 
 // Co-resident CTAs per SM allowed by registers and threads (cached per device).
-template <bool kXF32, bool kStream, int kNT>
+template <bool kXF32, bool kStream, int kNT, bool kP64>
 int occupancy_without_smem(int dev) {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64] = {};
   if (dev < 0 || dev >= 64) return 1;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmv_smallm_kernel<kXF32, kStream, kNT>,
-                                                      kThreads, 0) != cudaSuccess || n < 1)
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, qmv_smallm_kernel<kXF32, kStream, kNT, kP64>, kThreads, 0) != cudaSuccess ||
+        n < 1)
       n = 1;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
-template <bool kXF32, bool kStream, int kNT>
+template <bool kXF32, bool kStream, int kNT, bool kP64>
 sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
-  static bool configured[64] = {};
+  static PerDeviceOnce attrs_once;
   const int dev = current_device();
-  auto kern = qmv_smallm_kernel<kXF32, kStream, kNT>;
+  auto kern = qmv_smallm_kernel<kXF32, kStream, kNT, kP64>;
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
-        cudaSuccess)
-      return fail(SV_ERR_CUDA, "qmv_smallm: cudaFuncSetAttribute failed");
-    configured[dev] = true;
-  }
+  const cudaError_t ce = attrs_once.run([&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  });
+  if (ce != cudaSuccess)
+    return fail(SV_ERR_CUDA, "qmv_smallm: cudaFuncSetAttribute failed: %s", cudaGetErrorString(ce));
   const int groups = args.K / 64;
   const int tiles = (args.N + kRows - 1) / kRows;
   const int n_chunks = (args.K + kStageInputs - 1) / kStageInputs;
   const int sms = device_sm_count();
-  const int occ = occupancy_without_smem<kXF32, kStream, kNT>(dev);
+  const int occ = occupancy_without_smem<kXF32, kStream, kNT, kP64>(dev);
   // split K over a cluster when the row tiles alone would leave CTA slots
   // idle, as far as the grid still fits in one wave of resident CTAs.  The
   // split decides the fp32 summation order, so it is chosen from the
   // occupancy of the <= 8-row kernel for every M: a row of a 9..16-row call
   // then equals the same row computed alone, bit for bit (at one CTA per SM
   // such a grid may take two waves).
-  const int occ_split = occupancy_without_smem<kXF32, kStream, 1>(dev);
+  const int occ_split = occupancy_without_smem<kXF32, kStream, 1, kP64>(dev);
   int splits = 1;
   if (kStream) {
     const int fit = (occ_split * sms) / tiles;
@@ -416,18 +454,23 @@ sv_status launch(const uint32_t *w, QmvArgs args, cudaStream_t stream) {
   const int per_cta_chunks = (n_chunks + splits - 1) / splits;
   const int max_stages = std::min(32, std::max(2, per_cta_chunks));
   int stages = 2;
-  while (stages < max_stages && qmv_layout(groups, stages + 1, sbs, kNT).total <= budget) ++stages;
-  Layout L = qmv_layout(groups, stages, sbs, kNT);
-  while (L.total > (uint32_t)optin && stages > 2) L = qmv_layout(groups, --stages, sbs, kNT);
+  while (stages < max_stages && qmv_layout(groups, stages + 1, sbs, kNT, kP64).total <= budget)
+    ++stages;
+  Layout L = qmv_layout(groups, stages, sbs, kNT, kP64);
+  while (L.total > (uint32_t)optin && stages > 2) L = qmv_layout(groups, --stages, sbs, kNT, kP64);
   if (L.total > (uint32_t)optin)
     return fail(SV_ERR_UNSUPPORTED, "qmv_smallm: K=%d needs %u bytes of shared memory",
                 args.K, L.total);
   args.stages = stages;
 
   CUtensorMap wmap, smap, bmap;
-  sv_status st = encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, w, (uint64_t)args.K / 8,
-                           (uint64_t)args.N, (uint64_t)args.K / 2, kBoxWords, kRows,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
+  sv_status st =
+      kP64 ? encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, (uint64_t)args.K,
+                       (uint64_t)args.N, (uint64_t)args.K / 2, kP64BoxInputs, kRows,
+                       CU_TENSOR_MAP_SWIZZLE_128B)
+           : encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, w, (uint64_t)args.K / 8,
+                       (uint64_t)args.N, (uint64_t)args.K / 2, kBoxWords, kRows,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != SV_OK) return st;
   if (sbs) {
     st = encode_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, args.s, (uint64_t)groups,
@@ -515,12 +558,35 @@ extern "C" sv_status qmv_smallm(const uint32_t *w_packed, const uint16_t *scales
   QmvArgs args{scales, biases, x, y, M, N, K, 0, 1, K % 512 == 0 ? 1 : 0};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool bf = x_dtype == SV_BF16;
+  // byte-expandable boxes need K % 128 == 0 and 32-byte aligned weights
+  // (always so when K % 512 == 0 and the caller's buffer is); the format is a
+  // function of (K, w_packed) only, so every M of one weight matrix takes the
+  // same per-row arithmetic
+  if (K % 128 == 0 && aligned(w_packed, 32)) {
+    if (M <= 8) {
+      if (args.sb_stream)
+        return bf ? launch<false, true, 1, true>(w_packed, args, s)
+                  : launch<true, true, 1, true>(w_packed, args, s);
+      return bf ? launch<false, false, 1, true>(w_packed, args, s)
+                : launch<true, false, 1, true>(w_packed, args, s);
+    }
+    if (args.sb_stream)
+      return bf ? launch<false, true, 2, true>(w_packed, args, s)
+                : launch<true, true, 2, true>(w_packed, args, s);
+    return bf ? launch<false, false, 2, true>(w_packed, args, s)
+              : launch<true, false, 2, true>(w_packed, args, s);
+  }
+  // K % 128 == 64 (never streamed: K % 512 != 0), or weights only 16-byte aligned
   if (M <= 8) {
     if (args.sb_stream)
-      return bf ? launch<false, true, 1>(w_packed, args, s) : launch<true, true, 1>(w_packed, args, s);
-    return bf ? launch<false, false, 1>(w_packed, args, s) : launch<true, false, 1>(w_packed, args, s);
+      return bf ? launch<false, true, 1, false>(w_packed, args, s)
+                : launch<true, true, 1, false>(w_packed, args, s);
+    return bf ? launch<false, false, 1, false>(w_packed, args, s)
+              : launch<true, false, 1, false>(w_packed, args, s);
   }
   if (args.sb_stream)
-    return bf ? launch<false, true, 2>(w_packed, args, s) : launch<true, true, 2>(w_packed, args, s);
-  return bf ? launch<false, false, 2>(w_packed, args, s) : launch<true, false, 2>(w_packed, args, s);
+    return bf ? launch<false, true, 2, false>(w_packed, args, s)
+              : launch<true, true, 2, false>(w_packed, args, s);
+  return bf ? launch<false, false, 2, false>(w_packed, args, s)
+            : launch<true, false, 2, false>(w_packed, args, s);
 }
