@@ -27,8 +27,9 @@
 //  * consumers read a phase's activations only after the device-wide count
 //    of finished tiles says every tile of the earlier phases has been
 //    written (one acquire load by one thread, bounded wait);
-//  * a tile whose stages fall in several CTAs' runs is reduced by the last of
-//    them to finish, summing the partials in run order -- deterministic;
+//  * a tile whose stages fall in several CTAs' runs: every run stores its
+//    partial and counts it, and the run that counts last sums the partials
+//    in run order -- deterministic, and nobody waits on another CTA;
 //  * counters are left at zero by the last CTA / last arriver, so the plan
 //    is ready for the next launch.
 // The per-group math (nibble widening, bf16 MMA, scale/bias epilogue) is the
@@ -371,46 +372,52 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
         ++nseg;
         const PlanProblem &q = P.problems[s.p];
         const int N = q.N, n0 = s.tile * kRows;
-        // A split tile is summed by its first run (split 0): that CTA's run
-        // ends with the tile, so it reaches it last and the later runs,
-        // which start their CTAs' ranges with it, have usually published
-        // their partials already.  They store and count without waiting.
+        // A split tile: every run stores its partial and counts it; the run
+        // that counts last sums all the partials in run order (the order,
+        // not who sums, fixes the result) and finishes the tile.  Nobody
+        // waits for another CTA.
         bool write = true;
-        float4 *slots = nullptr;
         if (s.n_splits > 1) {
-          slots = reinterpret_cast<float4 *>(P.partials) +
-                  (size_t)s.tile_in_phase * max_splits * (kPartial / 4);
+          const float4 *slots = reinterpret_cast<const float4 *>(P.partials) +
+                                (size_t)s.tile_in_phase * max_splits * (kPartial / 4);
+          float4 *mine = reinterpret_cast<float4 *>(P.partials) +
+                         ((size_t)s.tile_in_phase * max_splits + s.split) * (kPartial / 4);
           int *count = &P.tile_count[s.tile_in_phase];
-          if (s.split > 0) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              __stcg(&slots[(size_t)s.split * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)],
-                     v[i]);
-            __syncwarp();
-            if (lane == 0) red_add_release(count, 1);  // publishes this run's partial
+          for (int i = 0; i < 4; ++i) __stcg(&mine[(lane + 32 * (i >> 1)) * 2 + (i & 1)], v[i]);
+          __syncwarp();
+          int last = 0;
+          // acq_rel: publishes this run's partial, and the last arriver sees
+          // every other run's
+          if (lane == 0) last = atom_add_acq_rel(count, 1) == s.n_splits - 1;
+          last = __shfl_sync(0xffffffffu, last, 0);
+          __syncwarp();  // the other lanes read after lane 0's acquire
+          if (!last) {
             write = false;
           } else {
-            if (lane == 0 && !wait_count(count, s.n_splits - 1))
-              atomicOr(&g_plan_device_error, 32u);
-            __syncwarp();  // the other lanes read after lane 0's acquire
-            // own partial first, then the later runs in run order
+            const float4 own[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll 1
-            for (int r = 1; r < s.n_splits; r += 2) {
+            for (int r = 0; r < s.n_splits; r += 2) {
               float4 a[4], b[4];
               const bool two = r + 1 < s.n_splits;
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const size_t o = (size_t)(lane + 32 * (i >> 1)) * 2 + (i & 1);
-                a[i] = __ldcg(&slots[(size_t)r * (kPartial / 4) + o]);
-                b[i] = two ? __ldcg(&slots[(size_t)(r + 1) * (kPartial / 4) + o])
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                a[i] = r == s.split ? own[i] : __ldcg(&slots[(size_t)r * (kPartial / 4) + o]);
+                b[i] = !two ? make_float4(0.f, 0.f, 0.f, 0.f)
+                            : (r + 1 == s.split ? own[i]
+                                                : __ldcg(&slots[(size_t)(r + 1) * (kPartial / 4) + o]));
               }
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                v[i].x += a[i].x;
-                v[i].y += a[i].y;
-                v[i].z += a[i].z;
-                v[i].w += a[i].w;
+                if (r == 0) {
+                  v[i] = a[i];
+                } else {
+                  v[i].x += a[i].x;
+                  v[i].y += a[i].y;
+                  v[i].z += a[i].z;
+                  v[i].w += a[i].w;
+                }
                 if (two) {
                   v[i].x += b[i].x;
                   v[i].y += b[i].y;
@@ -419,6 +426,7 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
                 }
               }
             }
+            if (lane == 0) *count = 0;  // every run has counted: ready for the next launch
           }
         }
         if (write) {
@@ -445,10 +453,7 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
             }
           }
           __syncwarp();
-          if (lane == 0) {
-            if (slots) P.tile_count[s.tile_in_phase] = 0;  // ready for the next launch
-            if (signal) red_add_release(P.done_tiles, 1);
-          }
+          if (lane == 0 && signal) red_add_release(P.done_tiles, 1);
         }
       }
     }
