@@ -13,14 +13,17 @@
 //   S' = alpha_t S;  u = S' k_t;  e_t = beta_t (v_t - u);  S_t = S' + e_t k_t^T;
 //   o_t = S_t q_t.
 // Rows of S never interact: row i needs only v_t[i] and the shared k_t, q_t,
-// alpha_t, beta_t.  A CTA owns 16 rows of one head; eight lanes share a row,
-// each holding 16 of its fp32 elements in registers as four float4 chunks at
-// columns 32c + 4j (lane j of the row), so every load and store of the state
-// is a run of 128 contiguous bytes per row and a warp covers four rows; the
-// row's dot products are finished with three shuffles.  Small batches still
-// give (dv / 16) x H CTAs (384 at H = 48, dv = 128).  The state element
-// update is written as the same explicit roundings in both kernels -- a
-// round-to-nearest multiply by the gate, then one fused multiply-add of the
+// alpha_t, beta_t.  Eight lanes share a row, each holding 16 of its fp32
+// elements in registers at columns 32c + 4j + [0, 4) (lane j of the row), so
+// every load and store of the state is a run of 128 contiguous bytes per row;
+// the row's dot products are finished with three shuffles.  The capture CTA
+// owns 16 rows of one head, or 32 (two rows per thread, one read of each
+// token's keys and queries serving both) once a batch would fill more than
+// two waves of CTAs; small batches keep (dv / 16) x H CTAs (384 at H = 48,
+// dv = 128) for latency.  The capture's arithmetic is packed fp32
+// (fma.rn.f32x2 / mul.rn.f32x2: two independent IEEE operations each), and
+// the state element update is the same explicit roundings in both kernels --
+// a round-to-nearest multiply by the gate, then one fused multiply-add of the
 // rank-1 term -- so replaying the tape reproduces the capture's states bit
 // for bit.
 #include <cuda_runtime.h>
@@ -41,7 +44,7 @@ constexpr int kThreads = kRowsPerCta * kLanesPerRow;  // 128
 constexpr int kMaxT = 16;
 // float4 loads per thread to stage kMaxT tokens of one kMaxDim-wide vector
 constexpr int kStage4 = kMaxT * kMaxDim / 4 / kThreads;  // 4
-static_assert(kMaxT * (kRowsPerCta / 4) <= kThreads, "one float4 of values per thread");
+
 
 // Tape: one block per sequence b of tape_block_floats(T,H,dk,dv) floats, each
 // block holding e [T][H][dv], then k [T][H][dk], then alpha [T][H] (padded to
@@ -91,32 +94,45 @@ __device__ __forceinline__ float row_sum(float v) {
 }
 
 // kFull: dk == kMaxDim, so every lane's chunks are real columns (no checks).
-template <bool kFull>
+// kR: state rows per thread; the CTA covers 16 kR rows of one head, row
+// group g = tid / 8 holding rows r0 + g + 16 r.  One read of a token's keys
+// and queries from shared memory serves all kR rows.  Lane j keeps its row
+// elements as float2 pairs (columns 32c + 4j + {0,1} and + {2,3}) for the
+// packed fp32 instructions: per element the same IEEE roundings as scalar
+// code (the decay a round-to-nearest multiply, the rank-1 term one fused
+// multiply-add), so replay still reproduces the capture bit for bit.
+// kT > 0: the token count is known at compile time (the token loop unrolls).
+template <bool kFull, int kR, int kT>
 __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) {
+  constexpr int kRows = kRowsPerCta * kR;
+  const int T = kT > 0 ? kT : a.T;
+  static_assert(kMaxT * (kRows / 4) <= kThreads, "one float4 of values per thread");
   __shared__ __align__(16) float ks[kMaxT][kMaxDim];
   __shared__ __align__(16) float qs[kMaxT][kMaxDim];
-  __shared__ __align__(16) float vs[kMaxT][kRowsPerCta];
+  __shared__ __align__(16) float vs[kMaxT][kRows];
   __shared__ float als[kMaxT], bes[kMaxT];
   const int tid = threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
-  const int r0 = blockIdx.x * kRowsPerCta;
-  const int i = r0 + tid / kLanesPerRow;  // state row (value dim)
+  const int r0 = blockIdx.x * kRows;
+  const int rg = tid / kLanesPerRow;
   const int j = tid % kLanesPerRow;
-  const bool row_ok = i < a.dv;
   pdl_launch_dependents();
   // the committed state does not depend on the preceding kernel: its load
   // overlaps that kernel's tail under programmatic dependent launch
-  float S[kChunks * 4];
-  const float *src = a.state0 + (((size_t)b * a.H + h) * a.dv + (row_ok ? i : 0)) * a.dk;
+  float2 S[kR][2 * kChunks];
 #pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row_ok && chunk_col(j, c) < a.dk)
-      f = __ldcg(reinterpret_cast<const float4 *>(src + chunk_col(j, c)));
-    S[4 * c] = f.x;
-    S[4 * c + 1] = f.y;
-    S[4 * c + 2] = f.z;
-    S[4 * c + 3] = f.w;
+  for (int r = 0; r < kR; ++r) {
+    const int i = r0 + rg + kRowsPerCta * r;
+    const bool ok = i < a.dv;
+    const float *src = a.state0 + (((size_t)b * a.H + h) * a.dv + (ok ? i : 0)) * a.dk;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok && (kFull || chunk_col(j, c) < a.dk))
+        f = __ldcg(reinterpret_cast<const float4 *>(src + chunk_col(j, c)));
+      S[r][2 * c] = make_float2(f.x, f.y);
+      S[r][2 * c + 1] = make_float2(f.z, f.w);
+    }
   }
   pdl_wait();  // the verify tokens' q, k, v and gates are the preceding kernels' outputs
   // The tokens' keys, queries, gates and this CTA's values, once.  Every load
@@ -124,29 +140,29 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
   // shared-memory store: a generic load might alias those stores and would
   // wait behind each one, one round trip per load.
   {
-    const int dk4 = a.dk / 4, nk4 = a.T * dk4;
+    const int dk4 = a.dk / 4, nk4 = T * dk4;
     float4 kr[kStage4], qr[kStage4];
 #pragma unroll
     for (int u = 0; u < kStage4; ++u) {
       const int e = tid + u * kThreads;
       if (e < nk4) {
         const int t = e / dk4, c4 = e - t * dk4;
-        const size_t off = (((size_t)b * a.T + t) * a.H + h) * a.dk + 4 * c4;
+        const size_t off = (((size_t)b * T + t) * a.H + h) * a.dk + 4 * c4;
         kr[u] = __ldcg(reinterpret_cast<const float4 *>(a.k + off));
         qr[u] = __ldcg(reinterpret_cast<const float4 *>(a.q + off));
       }
     }
-    // this CTA's 16 value rows per token: 4 float4 (dv % 4 == 0, so a float4
-    // is either wholly inside the rows or wholly past them)
-    const int t_v = tid / (kRowsPerCta / 4), r_v = 4 * (tid % (kRowsPerCta / 4));
-    const bool has_v = tid < a.T * (kRowsPerCta / 4);
+    // this CTA's value rows per token as float4 (dv % 4 == 0, so a float4 is
+    // either wholly inside the rows or wholly past them)
+    const int t_v = tid / (kRows / 4), r_v = 4 * (tid % (kRows / 4));
+    const bool has_v = tid < T * (kRows / 4);
     float4 vr = make_float4(0.f, 0.f, 0.f, 0.f);
     if (has_v && r0 + r_v < a.dv)
       vr = __ldcg(reinterpret_cast<const float4 *>(
-          a.v + (((size_t)b * a.T + t_v) * a.H + h) * a.dv + r0 + r_v));
+          a.v + (((size_t)b * T + t_v) * a.H + h) * a.dv + r0 + r_v));
     float al_r = 0.f, be_r = 0.f;
-    if (tid < a.T) {
-      const size_t bth = ((size_t)b * a.T + tid) * a.H + h;
+    if (tid < T) {
+      const size_t bth = ((size_t)b * T + tid) * a.H + h;
       al_r = __ldcg(a.alpha + bth);
       be_r = __ldcg(a.beta + bth);
     }
@@ -160,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
       }
     }
     if (has_v) *reinterpret_cast<float4 *>(&vs[t_v][r_v]) = vr;
-    if (tid < a.T) {
+    if (tid < T) {
       als[tid] = al_r;
       bes[tid] = be_r;
     }
@@ -169,63 +185,68 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
   __syncthreads();
 
   // the token's records and outputs advance by fixed strides
-  float *e_out = a.tape.e(b, 0, h) + i;
-  float *o_out = a.out ? a.out + ((size_t)b * a.T * a.H + h) * a.dv + i : nullptr;
+  float *e_out = a.tape.e(b, 0, h) + r0 + rg;
+  float *o_out = a.out ? a.out + ((size_t)b * T * a.H + h) * a.dv + r0 + rg : nullptr;
   float *k_out = a.tape.k(b, 0, h);
   float *al_out = a.tape.alpha(b, 0, h);
   const size_t e_step = (size_t)a.H * a.dv, k_step = (size_t)a.H * a.dk;
-  for (int t = 0; t < a.T; ++t) {
+#pragma unroll
+  for (int t = 0; t < (kT > 0 ? kT : kMaxT); ++t) {
+    if (kT == 0 && t >= T) break;
     const float al = als[t], be = bes[t];
-    // this lane's key chunks, read once for both passes (chunks past dk hold
-    // zeros and contribute 0)
-    float4 kr[kChunks];
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c)
-      kr[c] = (kFull || chunk_col(j, c) < a.dk)
-                  ? *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)])
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    // S' = alpha S ; u = S' k   (one partial sum per chunk keeps four
-    // independent FMA chains)
-    float uc[kChunks];
+    const float2 al2 = make_float2(al, al);
+    // this lane's key columns (zeros past dk, where the state is zero too)
+    float2 kk[2 * kChunks];
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
-      S[4 * c] = __fmul_rn(al, S[4 * c]);
-      S[4 * c + 1] = __fmul_rn(al, S[4 * c + 1]);
-      S[4 * c + 2] = __fmul_rn(al, S[4 * c + 2]);
-      S[4 * c + 3] = __fmul_rn(al, S[4 * c + 3]);
-      uc[c] = 0.f;
-      if (kFull || chunk_col(j, c) < a.dk) {
-        const float4 kk = kr[c];
-        uc[c] = fmaf(S[4 * c], kk.x, uc[c]);
-        uc[c] = fmaf(S[4 * c + 1], kk.y, uc[c]);
-        uc[c] = fmaf(S[4 * c + 2], kk.z, uc[c]);
-        uc[c] = fmaf(S[4 * c + 3], kk.w, uc[c]);
-      }
+      const float4 f = (kFull || chunk_col(j, c) < a.dk)
+                           ? *reinterpret_cast<const float4 *>(&ks[t][chunk_col(j, c)])
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      kk[2 * c] = make_float2(f.x, f.y);
+      kk[2 * c + 1] = make_float2(f.z, f.w);
     }
-    float u = row_sum((uc[0] + uc[1]) + (uc[2] + uc[3]));
-    const float e = be * (vs[t][tid / kLanesPerRow] - u);
+    // S' = alpha S ; u = S' k   (two pair accumulators per row)
+    float u[kR];
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 2 * kChunks; m += 2) {
+        S[r][m] = __fmul2_rn(al2, S[r][m]);
+        S[r][m + 1] = __fmul2_rn(al2, S[r][m + 1]);
+        acc0 = __ffma2_rn(S[r][m], kk[m], acc0);
+        acc1 = __ffma2_rn(S[r][m + 1], kk[m + 1], acc1);
+      }
+      u[r] = row_sum((acc0.x + acc0.y) + (acc1.x + acc1.y));
+    }
+    float2 qq[2 * kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const float4 f = (kFull || chunk_col(j, c) < a.dk)
+                           ? *reinterpret_cast<const float4 *>(&qs[t][chunk_col(j, c)])
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      qq[2 * c] = make_float2(f.x, f.y);
+      qq[2 * c + 1] = make_float2(f.z, f.w);
+    }
     // S_t = S' + e k^T ; o = S_t q
-    float oc[kChunks];
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      oc[c] = 0.f;
-      if (kFull || chunk_col(j, c) < a.dk) {
-        const float4 kk = kr[c];
-        const float4 qq = *reinterpret_cast<const float4 *>(&qs[t][chunk_col(j, c)]);
-        S[4 * c] = __fmaf_rn(e, kk.x, S[4 * c]);
-        S[4 * c + 1] = __fmaf_rn(e, kk.y, S[4 * c + 1]);
-        S[4 * c + 2] = __fmaf_rn(e, kk.z, S[4 * c + 2]);
-        S[4 * c + 3] = __fmaf_rn(e, kk.w, S[4 * c + 3]);
-        oc[c] = fmaf(S[4 * c], qq.x, oc[c]);
-        oc[c] = fmaf(S[4 * c + 1], qq.y, oc[c]);
-        oc[c] = fmaf(S[4 * c + 2], qq.z, oc[c]);
-        oc[c] = fmaf(S[4 * c + 3], qq.w, oc[c]);
+    for (int r = 0; r < kR; ++r) {
+      const int rr = rg + kRowsPerCta * r;
+      const float e = be * (vs[t][rr] - u[r]);
+      const float2 e2 = make_float2(e, e);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 2 * kChunks; m += 2) {
+        S[r][m] = __ffma2_rn(e2, kk[m], S[r][m]);
+        S[r][m + 1] = __ffma2_rn(e2, kk[m + 1], S[r][m + 1]);
+        acc0 = __ffma2_rn(S[r][m], qq[m], acc0);
+        acc1 = __ffma2_rn(S[r][m + 1], qq[m + 1], acc1);
       }
-    }
-    const float o = row_sum((oc[0] + oc[1]) + (oc[2] + oc[3]));
-    if (row_ok && j == 0) {
-      *e_out = e;
-      if (o_out) *o_out = o;
+      const float o = row_sum((acc0.x + acc0.y) + (acc1.x + acc1.y));
+      if (j == 0 && r0 + rr < a.dv) {
+        e_out[kRowsPerCta * r] = e;
+        if (o_out) o_out[kRowsPerCta * r] = o;
+      }
     }
     if (blockIdx.x == 0) {
       for (int c = tid; c < a.dk; c += kThreads) k_out[c] = ks[t][c];
@@ -236,13 +257,18 @@ __global__ void __launch_bounds__(kThreads) gdn_capture_kernel(const GdnArgs a) 
     k_out += k_step;
     al_out += a.H;
   }
-  if (a.state_out && row_ok) {
-    float *dst = a.state_out + (((size_t)b * a.H + h) * a.dv + i) * a.dk;
+  if (a.state_out) {
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c)
-      if (chunk_col(j, c) < a.dk)
-        *reinterpret_cast<float4 *>(dst + chunk_col(j, c)) =
-            make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
+    for (int r = 0; r < kR; ++r) {
+      const int i = r0 + rg + kRowsPerCta * r;
+      if (i >= a.dv) continue;
+      float *dst = a.state_out + (((size_t)b * a.H + h) * a.dv + i) * a.dk;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c)
+        if (chunk_col(j, c) < a.dk)
+          *reinterpret_cast<float4 *>(dst + chunk_col(j, c)) =
+              make_float4(S[r][2 * c].x, S[r][2 * c].y, S[r][2 * c + 1].x, S[r][2 * c + 1].y);
+    }
   }
 }
 
@@ -395,15 +421,36 @@ extern "C" sv_status gdn_tape_capture(const float *state0, const float *q, const
   args.H = H;
   args.dk = dk;
   args.dv = dv;
-  dim3 grid((unsigned)((dv + kRowsPerCta - 1) / kRowsPerCta), (unsigned)H, (unsigned)B);
+  // two rows per thread once one row per thread would take more than two
+  // waves of resident CTAs (a small batch keeps the wider grid for latency)
+  const int ctas1 = ((dv + kRowsPerCta - 1) / kRowsPerCta) * H * B;
+  const int R = ctas1 > 2 * 7 * device_sm_count() ? 2 : 1;
+  dim3 grid((unsigned)((dv + kRowsPerCta * R - 1) / (kRowsPerCta * R)), (unsigned)H, (unsigned)B);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   // launched in stream order (starting early measured slower); the kernel
   // triggers its dependents at entry so the following kernel may start early
-  if (cudaLaunchKernelEx(&cfg, dk == kMaxDim ? gdn_capture_kernel<true> : gdn_capture_kernel<false>,
-                         args) != cudaSuccess)
+  // full-width heads at the verify widths M = K + 1 = 3..6 take kernels with
+  // the token count built in
+  void (*kern)(const GdnArgs) = nullptr;
+  if (dk == kMaxDim) {
+    switch (T * 4 + R) {
+      case 3 * 4 + 1: kern = gdn_capture_kernel<true, 1, 3>; break;
+      case 4 * 4 + 1: kern = gdn_capture_kernel<true, 1, 4>; break;
+      case 5 * 4 + 1: kern = gdn_capture_kernel<true, 1, 5>; break;
+      case 6 * 4 + 1: kern = gdn_capture_kernel<true, 1, 6>; break;
+      case 3 * 4 + 2: kern = gdn_capture_kernel<true, 2, 3>; break;
+      case 4 * 4 + 2: kern = gdn_capture_kernel<true, 2, 4>; break;
+      case 5 * 4 + 2: kern = gdn_capture_kernel<true, 2, 5>; break;
+      case 6 * 4 + 2: kern = gdn_capture_kernel<true, 2, 6>; break;
+      default: kern = R == 2 ? gdn_capture_kernel<true, 2, 0> : gdn_capture_kernel<true, 1, 0>;
+    }
+  } else {
+    kern = R == 2 ? gdn_capture_kernel<false, 2, 0> : gdn_capture_kernel<false, 1, 0>;
+  }
+  if (cudaLaunchKernelEx(&cfg, kern, args) != cudaSuccess)
     return fail(SV_ERR_CUDA, "gdn_capture: launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return check_launch("gdn_tape_capture");
 }
