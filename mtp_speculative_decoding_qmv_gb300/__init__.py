@@ -94,6 +94,8 @@ def lib() -> ctypes.CDLL:
         L.qmv_plan_create.restype = I
         L.qmv_plan_run.argtypes = [P, P]
         L.qmv_plan_run.restype = I
+        L.qmv_plan_run_cooperative.argtypes = [P, P]
+        L.qmv_plan_run_cooperative.restype = I
         L.qmv_plan_destroy.argtypes = [P]
         L.qmv_plan_destroy.restype = None
         L.qmv_plan_topk_bytes.argtypes = [I, I]
@@ -366,8 +368,14 @@ class QmvPlan:
         self.problems = list(problems)  # keep the tensors alive
         self.grid = int(lib().qmv_plan_grid(h))
 
-    def run(self) -> None:
-        _check(lib().qmv_plan_run(self._h, _stream(self.device)), "qmv_plan_run")
+    def run(self, cooperative: bool = False) -> None:
+        """One launch on the current stream; ``cooperative`` guarantees that
+        all CTAs are resident together (beside other self-waiting grids)."""
+        if cooperative:
+            _check(lib().qmv_plan_run_cooperative(self._h, _stream(self.device)),
+                   "qmv_plan_run_cooperative")
+        else:
+            _check(lib().qmv_plan_run(self._h, _stream(self.device)), "qmv_plan_run")
 
     def close(self) -> None:
         if getattr(self, "_h", None):

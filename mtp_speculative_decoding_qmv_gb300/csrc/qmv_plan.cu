@@ -903,9 +903,8 @@ extern "C" sv_status qmv_plan_create(const sv_qmv_problem *problems, int n_probl
   return SV_OK;
 }
 
-extern "C" sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream) {
-  clear_error();
-  if (!plan) return fail(SV_ERR_INVALID_ARG, "qmv_plan_run: null plan");
+namespace {
+sv_status plan_launch(const sv_qmv_plan *plan, sv_stream_t stream, bool cooperative) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan->grid);
   cfg.blockDim = dim3(kPlanThreads);
@@ -918,22 +917,42 @@ extern "C" sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream) {
   // counts, split tiles) therefore end; each is bounded all the same.  A
   // cooperative launch would guarantee residency outright but measured ~1.5 us
   // slower per launch.
+  // A cooperative launch guarantees co-residency outright (for callers that
+  // share the device with other grids whose CTAs wait on one another), and
+  // is not combined with the programmatic early start.
   cudaLaunchAttribute attr[1];
   int na = 0;
-  if (pdl_enabled()) {
+  if (cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  } else if (pdl_enabled()) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
+  const char *what = cooperative ? "qmv_plan_run_cooperative" : "qmv_plan_run";
   const cudaError_t e =
       plan->x_dtype == SV_BF16
           ? cudaLaunchKernelEx(&cfg, qmv_plan_kernel<false>, plan->params)
           : cudaLaunchKernelEx(&cfg, qmv_plan_kernel<true>, plan->params);
-  if (e != cudaSuccess)
-    return fail(SV_ERR_CUDA, "qmv_plan_run: launch failed: %s", cudaGetErrorString(e));
-  return check_launch("qmv_plan_run");
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return check_launch(what);
+}
+}  // namespace
+
+extern "C" sv_status qmv_plan_run(const sv_qmv_plan *plan, sv_stream_t stream) {
+  clear_error();
+  if (!plan) return fail(SV_ERR_INVALID_ARG, "qmv_plan_run: null plan");
+  return plan_launch(plan, stream, false);
+}
+
+extern "C" sv_status qmv_plan_run_cooperative(const sv_qmv_plan *plan, sv_stream_t stream) {
+  clear_error();
+  if (!plan) return fail(SV_ERR_INVALID_ARG, "qmv_plan_run_cooperative: null plan");
+  return plan_launch(plan, stream, true);
 }
 
 extern "C" void qmv_plan_destroy(sv_qmv_plan *plan) { delete plan; }

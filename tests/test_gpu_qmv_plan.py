@@ -209,3 +209,40 @@ def test_phase_wait_gives_up_and_reports(sv, oracle):
     plan.run()
     _check(probs, refs)
     sv.device_status()
+
+
+def test_cooperative_run_equals_run(sv, oracle):
+    """qmv_plan_run_cooperative gives the same bits as qmv_plan_run"""
+    specs = [(2048, 1024, None), (1024, 2048, 0), (512, 1024, 1)]
+    plan, probs, refs = _plan_case(sv, oracle, specs, 4, "f32", 21)
+    plan.run()
+    torch.cuda.synchronize()
+    first = [p[4].cpu().numpy().copy() for p in probs]
+    for p in probs:
+        p[4].fill_(float("nan"))
+    plan.run(cooperative=True)
+    torch.cuda.synchronize()
+    for a, p in zip(first, probs):
+        np.testing.assert_array_equal(p[4].cpu().numpy(), a)
+    _check(probs, refs)
+    sv.device_status()
+
+
+def test_two_cooperative_plans_on_two_streams(sv, oracle):
+    """Two multi-phase plans launched cooperatively on two streams at once:
+    the device keeps each plan's CTAs resident together, so neither plan's
+    phase waits run out and both results are right."""
+    specs = [(4096, 2048, None), (2048, 4096, 0), (1024, 2048, 1)]
+    plan_a, probs_a, refs_a = _plan_case(sv, oracle, specs, 4, "f32", 22)
+    plan_b, probs_b, refs_b = _plan_case(sv, oracle, specs, 4, "f32", 23)
+    streams = [torch.cuda.Stream(dev()), torch.cuda.Stream(dev())]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        with torch.cuda.stream(streams[0]):
+            plan_a.run(cooperative=True)
+        with torch.cuda.stream(streams[1]):
+            plan_b.run(cooperative=True)
+    torch.cuda.synchronize()
+    sv.device_status()  # raises if a wait gave up
+    _check(probs_a, refs_a)
+    _check(probs_b, refs_b)
