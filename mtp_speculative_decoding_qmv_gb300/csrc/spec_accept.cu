@@ -10,24 +10,30 @@
 //
 // The distributions are filtered to at most top_k <= 64 tokens, so the only
 // vocabulary-wide work is a top-k per logits row: an HBM-bound read of
-// (2K+1) rows of V fp32 per sequence.  One kernel does everything:
-//  * chunk phase: CTA (chunk, row) reads 16384 logits (coalesced 16-byte
-//    streaming loads), bounds the k-th largest from below by the minimum of
-//    64 (or 32, 16) group maxima, keeps only elements at or above that bound
-//    (typically ~1 % of them) as 64-bit keys (ordered float bits, then lower
-//    token id), and writes the chunk's exact top-k sorted to the workspace;
-//    chunks of finite logits do the maxima and the bound test in float and
-//    build keys only for the kept elements (placed by warp ballots), chunks
-//    holding a NaN or an infinity take the same steps on keys throughout:
-//    with at most 512 candidates each thread ranks its own by counting the
-//    larger keys; otherwise a block radix select finds the k-th key first;
-//  * the last CTA of a sequence to finish (CTA barrier, then one acq_rel
-//    atomic add by thread 0; no spinning) merges the per-chunk lists of each
-//    row (one warp per row,
-//    k-way merge) and runs the acceptance for that sequence in one warp:
-//    softmax over the kept logits, top-p cut on the descending order,
-//    u < p/q test, residual (p - q)+ sampled by inverse CDF in ascending
-//    token-id order, bonus token.
+// (2K+1) rows of V fp32 per sequence, in chunks of 16384 logits.
+//  * chunk selection (chunk_select): the chunk's exact top-k, sorted, as
+//    64-bit keys (ordered float bits, then lower token id) in the workspace.
+//    The k-th largest of 32 (64 when k > 32) group maxima bounds the chunk's
+//    k-th largest from below (k distinct logits reach it); only elements at
+//    or above it are kept (typically a few more than k of the 16384), found
+//    through the threads whose maximum reaches the bound, and placed by
+//    counting larger keys.  Chunks of finite logits work in float and build
+//    keys only for kept elements; chunks holding a NaN or +inf work on keys
+//    throughout; many kept elements go through a radix select.
+//  * finish (finish_sequence), one CTA per sequence: each row's chunk lists
+//    merged into its top-k (a warp per row: the top-k of the lists' first
+//    few entries bounds the rest from below), softmax over the kept logits,
+//    top-p cut on the descending order, and then every position at once (a
+//    warp each): the u < p/q test and the residual (p - q)+ sampled by
+//    inverse CDF in ascending token-id order; the walk to the first
+//    rejection picks the emitted token (the bonus row's sample when all K
+//    are accepted).
+// Launches: 16-byte-aligned logits go through accept_stream_kernel (a
+// persistent CTA per SM, chunks streamed through a ring of bulk copies into
+// shared memory, two groups of 256 threads selecting alternate chunks) and
+// then accept_finish_kernel (a CTA per sequence).  Other logits, and the
+// target lists of a fused LM head, go through spec_accept_kernel, a CTA per
+// (chunk, row) whose last CTA of a sequence runs the finish.
 // Each call clears the workspace's counter words on the stream before the
 // launch, so a workspace needs no preparation and may be reused at any shape.
 //
@@ -42,6 +48,7 @@
 #include <cfloat>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
@@ -54,11 +61,17 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 16384;                  // logits per chunk CTA
 constexpr int kPerThread = kChunk / kThreads;  // 32
 constexpr int kMaxTopK = 64;
-constexpr int kCap = 2048;                     // candidate buffer entries
 constexpr int kMaxChunks = 64;                 // V <= 64 * 16384
 constexpr int kMaxK = 8;
 constexpr int kMaxRows = 2 * kMaxK + 1;
 constexpr int kStageBatch = 8;                 // candidate loads per lane in flight
+constexpr int kFewCandidates = 64;             // packed and ranked by one warp up to here
+constexpr int kMergeBuf = 256;                 // per-warp merge keys (else k-way merge)
+constexpr int kStreamStages = 3;               // chunks in flight per streaming CTA
+constexpr size_t kStreamRingBytes = (size_t)kStreamStages * kChunk * 4;
+constexpr int kAccInWords = 2 * kMaxK + kMaxRows + 1 + 6;  // acceptance inputs, 8-byte multiple
+static_assert(kAccInWords % 2 == 0, "the staging area after the inputs stays 8-aligned");
+static_assert(kPerThread == 32, "a candidate holder's values are one per lane");
 constexpr int kManySequences = 8;              // from here on, three CTAs per SM
 
 typedef unsigned long long u64;
@@ -113,6 +126,12 @@ __host__ inline int lists_chunks(int V, int G) {
 
 // ordered key of a logit: larger float -> larger key; 0 marks an excluded
 // element (-inf mask, NaN, +inf; NaN and +inf also raise `nonfinite`)
+// max(a, b, c), NaN if any operand is NaN
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ uint32_t logit_key(float v, int &nonfinite) {
   uint32_t u = __float_as_uint(v);
   if ((u & 0x7F800000u) == 0x7F800000u) {
@@ -132,36 +151,80 @@ __device__ __forceinline__ u64 composite(uint32_t key, uint32_t idx) {
 __device__ __forceinline__ int composite_id(u64 c) { return (int)(0xFFFFFFFFu - (uint32_t)c); }
 __device__ __forceinline__ float composite_logit(u64 c) { return key_logit((uint32_t)(c >> 32)); }
 
-struct ChunkSmem {
-  u64 buf[kCap];
+// Who selects one chunk: kGT threads (kGW warps) holding kPT logits each.
+template <int kGT_, int kPT_>
+struct SelGeo {
+  static constexpr int kGT = kGT_, kGW = kGT_ / 32, kPT = kPT_;
+  static_assert(kGT_ * kPT_ == kChunk && kPT_ % 32 == 0, "a chunk, whole rows of 32 per thread");
+};
+using CtaGeo = SelGeo<kThreads, kPerThread>;  // a CTA per chunk
+using GroupGeo = SelGeo<256, 64>;               // a group of a streaming CTA
+
+// Shared memory of one chunk's selection.  kCapT: candidate buffer entries,
+// kSeg of them per warp; kRowsT: candidate holders a warp tests at once.
+template <class G, int kCapT, int kRowsT>
+struct ChunkSmemT {
+  static constexpr int kSeg = kCapT / G::kGW;
+  static constexpr int kHolderRows = kRowsT;
+  u64 buf[kCapT];
   u64 top[kMaxTopK];
   unsigned hist[256];
   uint32_t gmax[64];
   float gmaxf[64];
-  uint32_t tau;
+  float scratch[G::kGW][kRowsT][G::kPT];  // candidate holders' values, per warp
+  uint32_t tau;               // the bound, as a key (exotic chunks) or a float
   float tauf;
-  int nc, ntop, done, rem;
+  alignas(16) int wcount[G::kGW];      // candidates each warp found
+  alignas(16) u64 few[kFewCandidates + 2];  // the candidates, packed, when few
+  int ntop, done, rem;
   u64 prefix;
-  int last;
+};
+using ChunkSmem = ChunkSmemT<CtaGeo, 2048, 4>;    // a CTA per chunk
+using StreamSmem = ChunkSmemT<GroupGeo, 512, 4>;  // each group of a streaming CTA
+
+// Barriers over the threads that select one chunk: the whole CTA, or one of
+// the kThreads-thread groups of a CTA (a named barrier).
+struct CtaBarrier {
+  __device__ __forceinline__ void sync() const { __syncthreads(); }
+  __device__ __forceinline__ int sync_or(int p) const { return __syncthreads_or(p); }
+};
+template <int kCount>
+struct GroupBarrier {
+  int id;  // 1 + group: barrier 0 is __syncthreads
+  __device__ __forceinline__ void sync() const {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kCount) : "memory");
+  }
+  __device__ __forceinline__ int sync_or(int p) const {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred q, o;\n\t"
+        "setp.ne.s32 q, %1, 0;\n\t"
+        "bar.red.or.pred o, %2, %3, q;\n\t"
+        "selp.s32 %0, 1, 0, o;\n\t}"
+        : "=r"(r)
+        : "r"(p), "r"(id), "n"(kCount)
+        : "memory");
+    return r;
+  }
 };
 
 // Exact ksel-th largest among the keys each thread enumerates (all distinct,
 // all nonzero): 8-bit radix passes from the top; stops as soon as the whole
 // bin at the boundary belongs to the top set.  Returns the threshold T such
 // that exactly min(ksel, total) keys are >= T.
-template <class Each>
-__device__ u64 block_select_threshold(ChunkSmem &S, int ksel, Each each) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+template <class G, class Smem, class Bar, class Each>
+__device__ u64 block_select_threshold(Smem &S, int ksel, int tid, const Bar &bar, Each each) {
+  const int lane = tid & 31, warp = tid >> 5;
   u64 prefix = 0, mask = 0;
   int rem = ksel;
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
-    for (int i = tid; i < 256; i += kThreads) S.hist[i] = 0;
-    __syncthreads();
+    for (int i = tid; i < 256; i += G::kGT) S.hist[i] = 0;
+    bar.sync();
     each([&](u64 c) {
       if ((c & mask) == prefix) atomicAdd(&S.hist[(c >> shift) & 255u], 1u);
     });
-    __syncthreads();
+    bar.sync();
     if (warp == 0) {
       // lane l owns bins 255-8l ... 248-8l (descending)
       unsigned cnt[8], s = 0;
@@ -203,12 +266,12 @@ __device__ u64 block_select_threshold(ChunkSmem &S, int ksel, Each each) {
         }
       }
     }
-    __syncthreads();
+    bar.sync();
     prefix = S.prefix;
     mask |= (u64)0xFF << shift;
     rem = S.rem;
     const int done = S.done;
-    __syncthreads();
+    bar.sync();
     if (done) break;
   }
   return prefix;
@@ -283,27 +346,33 @@ __device__ float dist_lookup(const RowDist &D, int token) {
 
 // Smallest token id whose running sum of R (ascending id) exceeds u * sum(R);
 // the last token with R > 0 if rounding never crosses; -1 if sum(R) <= 0.
-// ids[h], R[h] as in RowDist, the same 64 ids also in shared memory (row_ids,
-// read by every lane at once); scratch: 64 floats + 64 ints of warp smem.
-__device__ int inverse_cdf_by_id(const int (&ids)[2], const float (&R)[2], float u, float *sR,
-                                 int *sId, const int *row_ids) {
+// ids[h], R[h] as in RowDist: the first n slots hold the row's distinct
+// token ids (also in shared memory, row_ids, read by every lane at once), the
+// others id -1 and no mass; scratch: 64 floats + 64 ints of warp smem.  The
+// slots are placed in ascending id order, the unused ones last.
+__device__ int inverse_cdf_by_id(const int (&ids)[2], const float (&R)[2], int n, float u,
+                                 float *sR, int *sId, const int *row_ids) {
   const int lane = threadIdx.x & 31;
-  // rank of each of the 64 slots by (token id, slot); id -1 (unused) sorts last
-  int rank[2] = {0, 0};
-  u64 mykey[2];
+  // rank of each of the first n slots by token id; the unused ones keep
+  // their places past n
+  int rank[2] = {lane, lane + 32};
+  if (n > 0) {
+    int cnt[2] = {0, 0};
+#pragma unroll 4
+    for (int src = 0; src < n; ++src) {
+      const int other = row_ids[src];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) mykey[h] = ((u64)(uint32_t)ids[h] << 8) | (u64)(lane + 32 * h);
-#pragma unroll 8
-  for (int src = 0; src < 64; ++src) {
-    const int other = row_ids[src];
-    const u64 okey = ((u64)(uint32_t)other << 8) | (u64)src;
+      for (int h = 0; h < 2; ++h) cnt[h] += (other < ids[h]) ? 1 : 0;
+    }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) rank[h] += (okey < mykey[h]) ? 1 : 0;
+    for (int h = 0; h < 2; ++h)
+      if (lane + 32 * h < n) rank[h] = cnt[h];
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    sR[rank[h]] = (ids[h] >= 0) ? R[h] : 0.f;
-    sId[rank[h]] = ids[h];
+    const bool live = lane + 32 * h < n;
+    sR[rank[h]] = live ? R[h] : 0.f;
+    sId[rank[h]] = live ? ids[h] : -1;
   }
   __syncwarp();
   const float r0 = sR[lane], r1 = sR[lane + 32];
@@ -330,22 +399,660 @@ __device__ int inverse_cdf_by_id(const int (&ids)[2], const float (&R)[2], float
   return result;
 }
 
+// Bitonic sort of 64 values held two per lane (element lane in v[0], element
+// lane + 32 in v[1]) into descending order.
+template <class T>
+__device__ __forceinline__ void bitonic64_desc(T (&v)[2], int lane) {
+#pragma unroll
+  for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      T o[2];
+      if (j == 32) {
+        o[0] = v[1];
+        o[1] = v[0];
+      } else {
+        o[0] = __shfl_xor_sync(0xffffffffu, v[0], j);
+        o[1] = __shfl_xor_sync(0xffffffffu, v[1], j);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        // in a block sorted descending (i & k == 0) the lower index of each
+        // pair keeps the larger value
+        const bool keep_max = ((i & j) == 0) == ((i & k) == 0);
+        const T mx = v[h] > o[h] ? v[h] : o[h], mn = v[h] > o[h] ? o[h] : v[h];
+        v[h] = keep_max ? mx : mn;
+      }
+    }
+  }
+}
+
+// The k-th largest (1-based, counted with multiplicity) of the kN (32 or 64)
+// values vals[0, kN) in shared memory (16-byte aligned), by one warp: lane j
+// tests vals[j] (and vals[j + 32]), counting the values above it and at or
+// above it through broadcast reads, and the value v with (# > v) <= k-1 < (#
+// >= v) is the answer.  Every lane returns it.  (The loop is unrolled so
+// that all reads are in flight at once.)
+template <int kN, class T>
+__device__ __forceinline__ T warp_kth_largest(const T *vals, int k) {
+  static_assert(sizeof(T) == 4 && (kN == 32 || kN == 64), "32 or 64 32-bit values");
+  const int lane = threadIdx.x & 31;
+  constexpr int kH = kN / 32;
+  T g[kH];
+  int gt[kH], ge[kH];
+#pragma unroll
+  for (int h = 0; h < kH; ++h) {
+    g[h] = vals[lane + 32 * h];
+    gt[h] = 0;
+    ge[h] = 0;
+  }
+#pragma unroll
+  for (int q = 0; q < kN; q += 4) {
+    const uint4 w = *reinterpret_cast<const uint4 *>(vals + q);
+    const T o[4] = {reinterpret_cast<const T &>(w.x), reinterpret_cast<const T &>(w.y),
+                    reinterpret_cast<const T &>(w.z), reinterpret_cast<const T &>(w.w)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int h = 0; h < kH; ++h) {
+        gt[h] += o[e] > g[h] ? 1 : 0;
+        ge[h] += o[e] >= g[h] ? 1 : 0;
+      }
+  }
+  T r = g[0];
+  bool found = false;
+#pragma unroll
+  for (int h = 0; h < kH; ++h) {
+    const unsigned m = __ballot_sync(0xffffffffu, gt[h] <= k - 1 && k - 1 < ge[h]);
+    const T v = __shfl_sync(0xffffffffu, g[h], m ? __ffs(m) - 1 : 0);
+    if (!found && m) {
+      r = v;
+      found = true;
+    }
+  }
+  return r;
+}
+// Order-preserving map of a float (not NaN) to a 32-bit unsigned.
+__device__ __forceinline__ uint32_t float_order(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The exact top-ksel of one chunk of a logits row, sorted descending, into
+// dst[0, ksel) (empty slots 0), by kThreads threads (thread index tid, all
+// of them behind the barrier bar).  Thread t holds in v[i] the
+// logit of token index_at(t, i) (-inf past V).  A CTA may call it for one
+// chunk after another: every shared word a call writes was last read, in the
+// previous call, before the first barrier of this one.  `extra` (per thread) is OR-ed into the first CTA barrier as bit 1 of its
+// vote, and `after_first` runs in every thread right after that barrier with
+// the vote.  Returns, in every thread, whether the chunk held a NaN or +inf.
+template <class G, class Smem, class Bar, class After>
+__device__ int chunk_select(Smem &S, const float (&v)[G::kPT], const float *row, int V, int base,
+                            bool vec, int ksel, u64 *dst, int tid, const Bar &bar, int extra,
+                            After after_first) {
+  constexpr int kGT = G::kGT, kPT = G::kPT, kQ = kPT / 32;
+  constexpr int kSeg = Smem::kSeg, kHolderRows = Smem::kHolderRows;
+  const int lane = tid & 31, warp = tid >> 5;
+  // token id of value slot i of thread t
+  auto index_at = [&](int t, int i) -> uint32_t {
+    return vec ? (uint32_t)(base + 4 * (t + kGT * (i >> 2)) + (i & 3))
+               : (uint32_t)(base + t + kGT * i);
+  };
+  auto index_of = [&](int i) -> uint32_t { return index_at(tid, i); };
+  // slot lane + 32 q of thread t: base + t * t_mul + slot_off[q]
+  const int t_mul = vec ? 4 : 1;
+  int slot_off[kQ];
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) {
+    const int i = lane + 32 * q;
+    slot_off[q] = vec ? 4 * kGT * (i >> 2) + (i & 3) : kGT * i;
+  }
+  // Chunks holding a NaN or a +inf take the exact key path below; the others
+  // the float path, which keeps the same candidates (the key map is monotone
+  // on finite values, maps -0 and +0 to one key and -inf, a mask, to the
+  // never-kept key 0) and computes keys only for them.  The thread maximum
+  // propagates NaN, so one test finds both.
+  int nonfinite = 0, dummy = 0;
+
+  // ---- lower bound on the ksel-th largest: the ksel-th largest of the group
+  // maxima (ksel distinct logits reach it), 32 groups of threads when
+  // ksel <= 32, else 64, found by warp 0.
+  const int n_groups = ksel <= 32 ? 32 : 64;
+  const int tpg = kGT / n_groups;
+  float tmx = v[0];  // this thread's maximum (NaN if it holds one)
+#pragma unroll
+  for (int i = 1; i + 1 < kPT; i += 2) tmx = max3_nan(tmx, v[i], v[i + 1]);
+  tmx = max3_nan(tmx, v[kPT - 1], v[kPT - 1]);
+  {
+    float fmx = tmx;
+    for (int o = 1; o < tpg; o <<= 1) fmx = fmaxf(fmx, __shfl_xor_sync(0xffffffffu, fmx, o));
+    if ((tid % tpg) == 0) S.gmaxf[tid / tpg] = fmx;
+  }
+  const int vote = bar.sync_or((!(tmx <= FLT_MAX) ? 1 : 0) | (extra ? 2 : 0));
+  after_first(vote);
+  const bool exotic = vote & 1;
+  if (exotic) {  // (rare) key maxima, behind one more barrier
+    uint32_t tmax = 0;
+#pragma unroll
+    for (int i = 0; i < kPT; ++i) tmax = max(tmax, logit_key(v[i], nonfinite));
+    for (int o = 1; o < tpg; o <<= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    if ((tid % tpg) == 0) S.gmax[tid / tpg] = tmax;
+    bar.sync();
+  }
+
+  if (warp == 0) {
+    if (!exotic) {
+      float tauf;
+      const float g0 = S.gmaxf[lane];
+      // groups holding a value above -inf (padding and masks only: -inf)
+      const int nz = __popc(__ballot_sync(0xffffffffu, g0 > -INFINITY)) +
+                     (n_groups > 32 ? __popc(__ballot_sync(0xffffffffu, S.gmaxf[lane + 32] > -INFINITY))
+                                    : 0);
+      if (ksel == 1) {  // the largest: one warp reduction on the ordered bits
+        const uint32_t mo = __reduce_max_sync(0xffffffffu, float_order(g0));
+        tauf = __shfl_sync(0xffffffffu, g0, __ffs(__ballot_sync(0xffffffffu, float_order(g0) == mo)) - 1);
+      } else {
+        tauf = n_groups == 32 ? warp_kth_largest<32>(S.gmaxf, ksel)
+                              : warp_kth_largest<64>(S.gmaxf, ksel);
+      }
+      if (lane == 0) S.tauf = nz >= ksel ? tauf : -FLT_MAX;  // else every finite value
+    } else {
+      const int nz = __popc(__ballot_sync(0xffffffffu, S.gmax[lane] != 0u)) +
+                     (n_groups > 32 ? __popc(__ballot_sync(0xffffffffu, S.gmax[lane + 32] != 0u)) : 0);
+      const uint32_t tau =
+          n_groups == 32 ? warp_kth_largest<32>(S.gmax, ksel) : warp_kth_largest<64>(S.gmax, ksel);
+      if (lane == 0) S.tau = nz >= ksel ? tau : 1u;  // else every key
+    }
+  }
+  bar.sync();
+
+  // ---- keep the candidates at or above the bound ---------------------------
+  // each warp appends its candidates to its own segment of S.buf, without
+  // atomics, and publishes how many it found
+  u64 *seg = S.buf + warp * kSeg;
+  if (!exotic) {
+    const float tauf = S.tauf;
+    // candidates are rare (a few per warp): only threads whose maximum
+    // reaches the bound hold any.  Up to kHolderRows of them at a time put
+    // their values in rows of the warp's scratch, and the warp tests the
+    // rows, lane l taking slots l, l + 32, ...; each kept value takes a place
+    // in the warp's segment with a shared atomic add (a value or two per row:
+    // little contention).
+    if (lane == 0) S.wcount[warp] = 0;
+    __syncwarp();
+    unsigned holders = __ballot_sync(0xffffffffu, tmx >= tauf);
+    while (holders) {
+      const int hrank = __popc(holders & ((1u << lane) - 1u));
+      if (((holders >> lane) & 1u) && hrank < kHolderRows) {
+        float *row_s = S.scratch[warp][hrank];
+#pragma unroll
+        for (int i = 0; i < kPT; i += 4)
+          *reinterpret_cast<float4 *>(row_s + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+      int th[kHolderRows];  // the batch's holders
+#pragma unroll
+      for (int h = 0; h < kHolderRows; ++h) {
+        th[h] = holders ? __ffs(holders) - 1 : -1;
+        holders &= holders - 1u;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < kHolderRows; ++h) {
+        if (th[h] < 0) break;  // (warp-uniform)
+        const int tb = base + (warp * 32 + th[h]) * t_mul;
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          const float x = S.scratch[warp][h][lane + 32 * q];
+          if (x >= tauf) {
+            const int pos = atomicAdd(&S.wcount[warp], 1);
+            if (pos < kSeg) seg[pos] = composite(logit_key(x, dummy), (uint32_t)(tb + slot_off[q]));
+          }
+        }
+      }
+      __syncwarp();  // rows read before the next batch writes
+    }
+  } else {
+    const uint32_t tau = S.tau;
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < kPT; ++i) cnt += logit_key(v[i], dummy) >= tau ? 1 : 0;
+    int incl = cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int pos = incl - cnt;
+#pragma unroll
+    for (int i = 0; i < kPT; ++i) {
+      const uint32_t k = logit_key(v[i], dummy);
+      if (k >= tau) {
+        if (pos < kSeg) seg[pos] = composite(k, index_of(i));
+        ++pos;
+      }
+    }
+    if (lane == 31) S.wcount[warp] = incl;
+  }
+  const int any_nonfinite = bar.sync_or(nonfinite);
+  // every warp: the total, its own offset (candidates of lower warps) and
+  // whether a segment overflowed, by warp reductions over the warp counts
+  const int cl = lane < G::kGW ? S.wcount[lane] : 0;
+  const int nc = (int)__reduce_add_sync(0xffffffffu, (unsigned)cl);
+  const int before = (int)__reduce_add_sync(0xffffffffu, lane < warp ? (unsigned)cl : 0u);
+  const int overflow = (int)__reduce_or_sync(0xffffffffu, cl > kSeg ? 1u : 0u);
+
+  if (nc <= kFewCandidates) {
+    // ---- usual case: the candidates packed in S.few, then warp 0 places
+    // each by counting the larger ones (keys are distinct)
+    const int wc = nc == 0 ? 0 : S.wcount[warp];
+    for (int i = lane; i < wc; i += 32) S.few[before + i] = seg[i];
+    if (tid < 2) S.few[nc + tid] = 0ull;  // pad: read 16 bytes at a time
+    bar.sync();
+    if (warp == 0) {
+      // keys past nc (stale) are masked; the reads are unrolled so that they
+      // are all in flight at once
+      auto place = [&](auto n_max) {
+        constexpr int kMax = decltype(n_max)::value;
+        u64 mine[kMax / 32];
+        int rank[kMax / 32];
+#pragma unroll
+        for (int h = 0; h < kMax / 32; ++h) {
+          mine[h] = lane + 32 * h < nc ? S.few[lane + 32 * h] : 0ull;
+          rank[h] = 0;
+        }
+#pragma unroll
+        for (int j = 0; j < kMax; j += 2) {
+          const ulonglong2 o = *reinterpret_cast<const ulonglong2 *>(&S.few[j]);
+          const u64 ox = j < nc ? o.x : 0ull, oy = j + 1 < nc ? o.y : 0ull;
+#pragma unroll
+          for (int h = 0; h < kMax / 32; ++h) rank[h] += (ox > mine[h] ? 1 : 0) + (oy > mine[h] ? 1 : 0);
+        }
+#pragma unroll
+        for (int h = 0; h < kMax / 32; ++h)
+          if (lane + 32 * h < nc && rank[h] < ksel) dst[rank[h]] = mine[h];
+      };
+      if (nc <= 32) place(std::integral_constant<int, 32>());
+      else place(std::integral_constant<int, kFewCandidates>());
+      for (int i = lane; i < ksel; i += 32)
+        if (i >= nc) dst[i] = 0;  // empty slots
+    }
+    return any_nonfinite;
+  }
+  // ---- exact top-ksel of the chunk -----------------------------------------
+  u64 thr;
+  if (!overflow) {
+    const int wc = S.wcount[warp];
+    thr = block_select_threshold<G>(S, ksel, tid, bar, [&](auto f) {
+      for (int i = lane; i < wc; i += 32) f(seg[i]);
+    });
+    if (tid == 0) S.ntop = 0;
+    bar.sync();
+    for (int i = lane; i < wc; i += 32) {
+      const u64 c = seg[i];
+      if (c >= thr) S.top[atomicAdd(&S.ntop, 1)] = c;
+    }
+  } else {  // many ties / a flat row: select over the whole chunk
+    // (rare) the logits are read again from L2, so that the values need not
+    // stay in registers through the selection
+    auto key_again = [&](int i) -> uint32_t {
+      const int e = (int)index_of(i);
+      return e < V ? logit_key(__ldcg(row + e), dummy) : 0u;
+    };
+    thr = block_select_threshold<G>(S, ksel, tid, bar, [&](auto f) {
+#pragma unroll 4
+      for (int i = 0; i < kPT; ++i) {
+        const uint32_t k = key_again(i);
+        if (k) f(composite(k, index_of(i)));
+      }
+    });
+    if (tid == 0) S.ntop = 0;
+    bar.sync();
+#pragma unroll 4
+    for (int i = 0; i < kPT; ++i) {
+      const uint32_t k = key_again(i);
+      if (k) {
+        const u64 c = composite(k, index_of(i));
+        if (c >= thr) S.top[atomicAdd(&S.ntop, 1)] = c;
+      }
+    }
+  }
+  bar.sync();
+  const int ntop = S.ntop;
+  // sort descending by rank (keys are distinct) and publish
+  u64 mine = 0;
+  int rank = 0;
+  if (tid < ntop) {
+    mine = S.top[tid];
+    for (int j = 0; j < ntop; ++j) rank += S.top[j] > mine ? 1 : 0;
+  }
+  if (tid < ntop) dst[rank] = mine;
+  else if (tid < ksel) dst[tid] = 0;  // empty slots
+  // S.top and S.ntop are read until here: the next call's first use of them
+  // follows its own barriers
+  return any_nonfinite;
+}
+
+// ---- finish: merge each row's chunk lists, then the acceptance -------------
+// Shared-memory layout of the finish (bytes from the start of its region).
+struct FinishLayout {
+  size_t merged, mcount, dist_p, dist_id, dist_n, in, pos, cbuf, stage, total;
+};
+__host__ __device__ inline FinishLayout finish_layout(int rows_per_wave, size_t per_row_bytes) {
+  FinishLayout L;
+  L.merged = 0;                                            // u64 [kMaxRows][kMaxTopK]
+  L.mcount = L.merged + (size_t)kMaxRows * kMaxTopK * 8;   // int [kMaxRows + 1]
+  L.dist_p = L.mcount + (kMaxRows + 1) * 4;                // float [kMaxRows][64]
+  L.dist_id = L.dist_p + (size_t)kMaxRows * 64 * 4;        // int [kMaxRows][64]
+  L.dist_n = L.dist_id + (size_t)kMaxRows * 64 * 4;        // int [kMaxRows + 1]
+  L.in = L.dist_n + (kMaxRows + 1) * 4;                    // int [kAccInWords]
+  L.pos = L.in + kAccInWords * 4;                          // int [3][kMaxK + 1]
+  L.cbuf = (L.pos + 3 * (kMaxK + 1) * 4 + 15) / 16 * 16;   // u64 [rows_per_wave][kMergeBuf]
+  L.stage = L.cbuf + (size_t)rows_per_wave * kMergeBuf * 8;  // u64 [rows_per_wave][C*ksel]
+  const size_t scratch = (size_t)(kMaxK + 1) * 64 * 8;     // per position: 64 floats + 64 ints
+  L.total = L.stage + (rows_per_wave * per_row_bytes > scratch ? rows_per_wave * per_row_bytes
+                                                               : scratch);
+  return L;
+}
+
+// The last steps of sequence b, by one CTA: every row's lists merged into
+// its top-ksel (a warp per row, rows in waves) and, when sampling, its
+// filtered distribution; then every position's test and the token it would
+// emit, in parallel (a warp per position), and the walk to the first
+// rejection.  smem: finish_layout(a.rows_per_wave, C * ksel * 8) bytes.
+__device__ void finish_sequence(const AcceptArgs &a, int b, uint8_t *smem) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = a.K, V = a.V, ksel = a.ksel, C = a.C;
+  const bool greedy = a.temperature == 0.f;
+  const int per_row = C * ksel;
+  const FinishLayout FL = finish_layout(a.rows_per_wave, (size_t)per_row * 8);
+  u64 *merged = reinterpret_cast<u64 *>(smem + FL.merged);
+  int *mcount = reinterpret_cast<int *>(smem + FL.mcount);
+  // each row's filtered distribution, built by the warp that merged it:
+  // entry j at [row][j] (j = lane + 32 h of RowDist), and its support size
+  float *dist_p = reinterpret_cast<float *>(smem + FL.dist_p);
+  int *dist_id = reinterpret_cast<int *>(smem + FL.dist_id);
+  int *dist_n = reinterpret_cast<int *>(smem + FL.dist_n);
+  // the acceptance's inputs: draft tokens [kMaxK], uniforms [kMaxK], row
+  // flags [kMaxRows], the sampling uniform
+  int *in_d = reinterpret_cast<int *>(smem + FL.in);
+  float *in_ua = reinterpret_cast<float *>(in_d + kMaxK);
+  int *in_f = reinterpret_cast<int *>(in_ua + kMaxK);
+  float *in_us = reinterpret_cast<float *>(in_f + kMaxRows);
+  // per position k (K: the bonus row): accepted, the token emitted if the
+  // walk stops there, the flags the walk picks up there
+  int *pos_acc = reinterpret_cast<int *>(smem + FL.pos);
+  int *pos_emit = pos_acc + (kMaxK + 1);
+  int *pos_flags = pos_emit + (kMaxK + 1);
+  u64 *cbuf = reinterpret_cast<u64 *>(smem + FL.cbuf);
+  u64 *stage = reinterpret_cast<u64 *>(smem + FL.stage);
+
+  if (warp == kWarps - 1) {  // loaded while the rows merge (the last warp
+                             // merges a row only when 16 rows do)
+    if (lane < K) {
+      in_d[lane] = a.dt[(size_t)b * K + lane];
+      in_ua[lane] = a.ua[(size_t)b * K + lane];
+    }
+    for (int r = lane; r < a.rows; r += 32) in_f[r] = __ldcg(&a.rowflags[b * a.rows_max + r]);
+    if (lane == 0) in_us[0] = a.us[b];
+  }
+
+  // subset of every list merged first: its first q entries
+  const int q = min(ksel, (3 * ksel + C - 1) / C);
+  const int ns = C * q;  // <= 3 ksel + C - 1 < kMergeBuf
+  const unsigned below = (1u << lane) - 1u;
+  // list and entry of staged key i without an integer division: i < 4096
+  // and ksel <= 64 keep (i + 1/2) / ksel at least 1/128 from an integer,
+  // far beyond the float product's error
+  const float inv_ksel = 1.f / (float)ksel;
+  auto list_of = [&](int i) { return (int)(((float)i + 0.5f) * inv_ksel); };
+  for (int r0 = 0; r0 < a.rows; r0 += a.rows_per_wave) {
+    const int r = r0 + warp;
+    const bool active = warp < a.rows_per_wave && r < a.rows;
+    if (active) {
+      u64 *st = stage + (size_t)warp * per_row;
+      u64 *cb = cbuf + (size_t)warp * kMergeBuf;
+      u64 *mr = merged + r * kMaxTopK;
+      const u64 *src = a.cand + ((size_t)b * a.rows_max + r) * (size_t)C * kMaxTopK;
+      // the row's lists, kStageBatch loads per lane in flight before their
+      // shared-memory stores (a load issued after a store to a possibly
+      // aliasing address would wait for it: one round trip per element);
+      // the first q entries of each list also go to cb, contiguously
+      for (int i0 = 0; i0 < per_row; i0 += 32 * kStageBatch) {
+        u64 v[kStageBatch];
+        int lj[kStageBatch];
+#pragma unroll
+        for (int u = 0; u < kStageBatch; ++u) {
+          const int i = i0 + 32 * u + lane;
+          const int l = list_of(i);
+          lj[u] = l;
+          v[u] = i < per_row ? __ldcg(src + l * kMaxTopK + (i - l * ksel)) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kStageBatch; ++u) {
+          const int i = i0 + 32 * u + lane;
+          if (i < per_row) {
+            st[i] = v[u];
+            const int l = lj[u], j = i - l * ksel;
+            if (j < q) cb[l * q + j] = v[u];
+          }
+        }
+      }
+      if (lane == 0) cb[ns] = 0ull;  // pad: pairs are read 16 bytes at a time
+      __syncwarp();
+      // The subset's ksel-th largest key T bounds the row's from below.  The
+      // subset's keys are ranked by counting larger ones (keys are distinct:
+      // one token, one chunk; empty slots, 0, never count), and the top ksel
+      // of them are the row's when no list has a key >= T past its first q
+      // entries (the usual case: the top ksel rarely take more than q from
+      // one list).
+      u64 T = 0ull;
+      int nnz = 0;  // nonzero keys of the subset
+      for (int e0 = 0; e0 < ns; e0 += 32) {
+        const int e = e0 + lane;
+        const u64 x = e < ns ? cb[e] : 0ull;
+        nnz += __popc(__ballot_sync(0xffffffffu, x != 0ull));
+        if (x != 0ull) {
+          int larger = 0;
+#pragma unroll 4
+          for (int f = 0; f < ns; f += 2) {
+            const ulonglong2 y = *reinterpret_cast<const ulonglong2 *>(cb + f);
+            larger += (y.x > x ? 1 : 0) + (y.y > x ? 1 : 0);
+          }
+          if (larger < ksel) mr[larger] = x;
+          if (larger == ksel - 1) T = x;
+        }
+      }
+      T = warp_max_u64(T);  // one lane holds it; 0 if nnz < ksel
+      // a key >= T (any nonzero key when T = 0) past the first q entries?
+      bool missed = false;
+      if (q < ksel)
+        for (int l = lane; l < C; l += 32) {
+          const u64 x = st[l * ksel + q];
+          missed |= x != 0ull && x >= T;
+        }
+      int j;
+      if (!__any_sync(0xffffffffu, missed)) {
+        j = min(nnz, ksel);
+      } else {
+        // (rare) every key >= T competes, typically a few more than ksel
+        __syncwarp();
+        int nc = 0;
+        for (int i0 = 0; i0 < per_row; i0 += 32) {
+          const int i = i0 + lane;
+          const u64 x = i < per_row ? st[i] : 0ull;
+          const bool keep = x != 0ull && x >= T;
+          const unsigned m = __ballot_sync(0xffffffffu, keep);
+          const int pos = nc + __popc(m & below);
+          if (keep && pos < kMergeBuf - 1) cb[pos] = x;
+          nc += __popc(m);
+        }
+        if (nc < kMergeBuf) {
+          if (lane == 0) cb[nc] = 0ull;
+          __syncwarp();
+          for (int e = lane; e < nc; e += 32) {
+            const u64 x = cb[e];
+            int larger = 0;
+#pragma unroll 4
+            for (int f = 0; f < nc; f += 2) {
+              const ulonglong2 y = *reinterpret_cast<const ulonglong2 *>(cb + f);
+              larger += (y.x > x ? 1 : 0) + (y.y > x ? 1 : 0);
+            }
+            if (larger < ksel) mr[larger] = x;
+          }
+          j = min(nc, ksel);
+        } else {  // (rarer) k-way merge of the lists
+          int h0 = 0, h1 = 0;  // heads of lists lane and lane+32
+          for (j = 0; j < ksel; ++j) {
+            const u64 v0 = (lane < C && h0 < ksel) ? st[lane * ksel + h0] : 0ull;
+            const u64 v1 = (lane + 32 < C && h1 < ksel) ? st[(lane + 32) * ksel + h1] : 0ull;
+            const u64 best = v0 > v1 ? v0 : v1;
+            const u64 g = warp_max_u64(best);
+            if (g == 0ull) break;
+            if (v0 == g) ++h0;
+            else if (v1 == g) ++h1;
+            if (lane == 0) mr[j] = g;
+          }
+        }
+      }
+      if (lane == 0) mcount[r] = j;
+      if (!greedy) {  // the distribution, while the other rows merge
+        __syncwarp();
+        const RowDist D = row_dist(mr, j, a.temperature, a.top_p);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          dist_p[r * 64 + lane + 32 * h] = D.p[h];
+          dist_id[r * 64 + lane + 32 * h] = D.id[h];
+        }
+        if (lane == 0) dist_n[r] = D.n;
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- every position at once: warp k < K tests draft token k and, if it
+  // is rejected, samples the residual (p - q)+ there; warp K the bonus row
+  if (warp <= K) {
+    const int k = warp;
+    int f = in_f[k], acc = 0, emit = -1;
+    if (k == K) {
+      if (greedy) {
+        emit = mcount[K] > 0 ? composite_id(merged[K * kMaxTopK]) : -1;
+      } else {
+        const RowDist P = stored_dist(dist_p, dist_id, dist_n, K);
+        float *sR = reinterpret_cast<float *>(stage) + k * 128;  // 64 floats + 64 ints
+        int *sId = reinterpret_cast<int *>(sR + 64);
+        float R[2] = {P.p[0], P.p[1]};
+        emit = inverse_cdf_by_id(P.id, R, mcount[K], in_us[0], sR, sId, dist_id + K * 64);
+      }
+    } else {
+      const int d = in_d[k];
+      const bool d_ok = d >= 0 && d < V;
+      if (!d_ok) f |= SV_FLAG_DRAFT_OUT_OF_RANGE;
+      if (greedy) {
+        const int am = mcount[k] > 0 ? composite_id(merged[k * kMaxTopK]) : -1;
+        acc = d_ok && am >= 0 && d == am;
+        emit = am;
+      } else {
+        f |= in_f[K + 1 + k];
+        const RowDist P = stored_dist(dist_p, dist_id, dist_n, k);
+        const int qrow = K + 1 + k;
+        const RowDist Q = stored_dist(dist_p, dist_id, dist_n, qrow);
+        if (d_ok) {
+          const float qd = dist_lookup(Q, d);
+          if (qd == 0.f) {
+            f |= SV_FLAG_DRAFT_ZERO_Q;
+          } else {
+            const float pd = dist_lookup(P, d);
+            acc = in_ua[k] < pd / qd;
+          }
+        }
+        if (!acc) {
+          // residual max(0, p - q) over p's support (q's entries read from
+          // the stored distribution, all lanes the same address: broadcast)
+          float R[2] = {P.p[0], P.p[1]};
+          const int nq = Q.n;  // entries past it have no mass
+#pragma unroll 4
+          for (int src = 0; src < nq; ++src) {
+            const int qid = dist_id[qrow * 64 + src];
+            const float qp = dist_p[qrow * 64 + src];
+            if (qid >= 0 && qp > 0.f) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if (P.id[h] == qid) R[h] = P.p[h] - qp;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) R[h] = R[h] > 0.f ? R[h] : 0.f;
+          const float Z = warp_sum(R[0] + R[1]);
+          if (!(Z > 0.f)) {
+            R[0] = P.p[0];
+            R[1] = P.p[1];
+          }
+          float *sR = reinterpret_cast<float *>(stage) + k * 128;
+          int *sId = reinterpret_cast<int *>(sR + 64);
+          emit = inverse_cdf_by_id(P.id, R, mcount[k], in_us[0], sR, sId, dist_id + k * 64);
+        }
+      }
+    }
+    if (lane == 0) {
+      pos_acc[k] = acc;
+      pos_emit[k] = emit;
+      pos_flags[k] = f;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+
+  // ---- the walk: accepted up to the first rejection (or all K, then the
+  // bonus), flags of every position it visits
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < K && pos_acc[lane] == 0);
+  const int stop = rej ? __ffs(rej) - 1 : K;
+  int flags = lane <= stop ? pos_flags[lane] : 0;
+  for (int o = 16; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xffffffffu, flags, o);
+  const int emitted = pos_emit[stop];
+  if (emitted < 0) flags |= SV_FLAG_EMPTY_DIST;
+  int32_t *out = a.out + (size_t)b * (K + 1);
+  if (lane <= K) out[lane] = lane < stop ? in_d[lane] : (lane == stop ? emitted : -1);
+  if (lane == 0) {
+    a.nacc[b] = stop;
+    if (a.flags) a.flags[b] = flags;
+    a.counters[b] = 0;  // ready for the next call
+  }
+  for (int r = lane; r < a.rows_max; r += 32) a.rowflags[b * a.rows_max + r] = 0;
+}
+
+// Sequence and row of a logits chunk; the row's logits.
+__device__ __forceinline__ const float *chunk_row(const AcceptArgs &a, int row_g, int &b,
+                                                  int &rloc) {
+  b = row_g / a.rows;
+  rloc = row_g - b * a.rows;
+  const int K = a.K;
+  return rloc <= K ? a.tl + ((size_t)b * (K + 1) + rloc) * a.V
+                   : a.dl + ((size_t)b * K + (rloc - K - 1)) * a.V;
+}
+__device__ __forceinline__ u64 *chunk_dst(const AcceptArgs &a, int b, int rloc, int cx) {
+  return a.cand + ((size_t)b * a.rows_max + rloc) * (size_t)a.C * kMaxTopK + (size_t)cx * kMaxTopK;
+}
+
 // kCtasPerSm: co-resident CTAs the register budget is cut for.  Three (40
-// registers, a few spilled) hide more load latency when many sequences fill
-// the GPU with chunk CTAs (batch 32: 74.0 -> 66.3 us); two keep the finish
-// path, which one CTA per sequence runs, free of spills (batch 1: 19.5
-// against 20.3 us).
+// registers) hide more load latency when many sequences fill the GPU with
+// chunk CTAs; two keep the finish path, which one CTA per sequence runs,
+// free of spills.
+//
+// One CTA per (chunk, row) of every sequence; the last CTA of a sequence to
+// finish (CTA barrier, then one acq_rel atomic add by thread 0; no spinning)
+// runs the finish.  Serves the rows given as lists of a fused LM head, and
+// logits rows without 16-byte alignment; aligned logits take the streaming
+// pair below.
 template <int kCtasPerSm>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_accept_kernel(const AcceptArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ChunkSmem &S = *reinterpret_cast<ChunkSmem *>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row_g = blockIdx.y;
-  const int b = row_g / a.rows, rloc = row_g % a.rows;
+  int b, rloc;
+  const float *row = chunk_row(a, blockIdx.y, b, rloc);
   const int cx = blockIdx.x;
   const int K = a.K, V = a.V;
-  const float *row = rloc <= K ? a.tl + ((size_t)b * (K + 1) + rloc) * V
-                               : a.dl + ((size_t)b * K + (rloc - K - 1)) * V;
   const int base = cx * kChunk;
   const int ksel = a.ksel;
 
@@ -365,8 +1072,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_accept_kernel(const
     for (int l = tid; l < n; l += kThreads) nf |= __ldcg(tfl + (size_t)(g0 + l) * (K + 1) + rloc) != 0u;
     const int any_nf = __syncthreads_or(nf);
     if (warp == 0) {
-      u64 *dst = a.cand + ((size_t)b * a.rows_max + rloc) * (size_t)a.C * kMaxTopK +
-                 (size_t)cx * kMaxTopK;
+      u64 *dst = chunk_dst(a, b, rloc, cx);
       int h0 = 0, h1 = 0;  // heads of lists lane and lane + 32
       int j = 0;
       for (; j < ksel; ++j) {
@@ -383,383 +1089,223 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_accept_kernel(const
         atomicOr(&a.rowflags[b * a.rows_max + rloc], SV_FLAG_NONFINITE_LOGIT);
     }
   } else {
-  // ---- load the chunk (values past V read as -inf: key 0, never kept) ------
-  float v[kPerThread];
-  float vsum = 0.f;  // finite iff every value of this thread's share is
-  if (a.vec) {
+    // ---- load the chunk (values past V read as -inf: key 0, never kept) ----
+    float v[kPerThread];
+    if (a.vec) {
 #pragma unroll
-    for (int i = 0; i < kPerThread / 4; ++i) {
-      const int e = base + 4 * (tid + kThreads * i);
-      float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      if (e < V) {  // V % 4 == 0 on this path
-        f = __ldcs(reinterpret_cast<const float4 *>(row + e));
-        vsum += (f.x + f.y) + (f.z + f.w);
+      for (int i = 0; i < kPerThread / 4; ++i) {
+        const int e = base + 4 * (tid + kThreads * i);
+        float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (e < V) f = __ldcs(reinterpret_cast<const float4 *>(row + e));  // V % 4 == 0 here
+        v[4 * i + 0] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
       }
-      v[4 * i + 0] = f.x;
-      v[4 * i + 1] = f.y;
-      v[4 * i + 2] = f.z;
-      v[4 * i + 3] = f.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-      const int e = base + tid + kThreads * i;
-      v[i] = -INFINITY;
-      if (e < V) {
-        v[i] = __ldcs(row + e);
-        vsum += v[i];
-      }
-    }
-  }
-  auto index_of = [&](int i) -> uint32_t {
-    return a.vec ? (uint32_t)(base + 4 * (tid + kThreads * (i >> 2)) + (i & 3))
-                 : (uint32_t)(base + tid + kThreads * i);
-  };
-  // Rows whose chunk holds a NaN or an infinity (a -inf mask included) take
-  // the exact key path below; the others the float path, which keeps the same
-  // candidates (the key map is monotone on finite values and maps -0 and +0
-  // to one key) and computes keys only for them.
-  int nonfinite = 0, dummy = 0;
-
-  // ---- lower bound on the ksel-th largest: min over >= ksel group maxima --
-  // (group maxima in float; the same barrier tells whether the chunk is
-  // exotic, and only then are key maxima taken, behind one more barrier)
-  const int n_groups = ksel <= 16 ? 16 : (ksel <= 32 ? 32 : 64);
-  const int tpg = kThreads / n_groups;  // 32, 16 or 8 threads per group
-  {
-    float fmx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) fmx = fmaxf(fmx, v[i]);
-    for (int o = 1; o < tpg; o <<= 1) fmx = fmaxf(fmx, __shfl_xor_sync(0xffffffffu, fmx, o));
-    if ((tid % tpg) == 0) S.gmaxf[tid / tpg] = fmx;
-  }
-  if (tid == 0) S.nc = 0;
-  const int exotic = __syncthreads_or(!(fabsf(vsum) <= FLT_MAX));
-  if (exotic) {
-    uint32_t tmax = 0;
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) tmax = max(tmax, logit_key(v[i], nonfinite));
-    for (int o = 1; o < tpg; o <<= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-    if ((tid % tpg) == 0) S.gmax[tid / tpg] = tmax;
-    __syncthreads();
-  }
-  if (warp == 0) {
-    if (!exotic) {  // a group of padding only has maximum -inf
-      const float g0 = lane < n_groups ? S.gmaxf[lane] : -INFINITY;
-      const float g1 = lane + 32 < n_groups ? S.gmaxf[lane + 32] : -INFINITY;
-      const int nz = __popc(__ballot_sync(0xffffffffu, g0 > -INFINITY)) +
-                     __popc(__ballot_sync(0xffffffffu, g1 > -INFINITY));
-      float mn = INFINITY;
-      if (g0 > -INFINITY) mn = fminf(mn, g0);
-      if (g1 > -INFINITY) mn = fminf(mn, g1);
-      for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      if (lane == 0) S.tauf = nz >= ksel ? mn : -FLT_MAX;  // else every finite value
     } else {
-      const uint32_t g0 = lane < n_groups ? S.gmax[lane] : 0u;
-      const uint32_t g1 = lane + 32 < n_groups ? S.gmax[lane + 32] : 0u;
-      const int nz = __popc(__ballot_sync(0xffffffffu, g0 != 0)) +
-                     __popc(__ballot_sync(0xffffffffu, g1 != 0));
-      uint32_t mn = 0xFFFFFFFFu;
-      if (g0) mn = min(mn, g0);
-      if (g1) mn = min(mn, g1);
-      for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      if (lane == 0) S.tau = nz >= ksel ? mn : 1u;
-    }
-  }
-  __syncthreads();
-
-  // ---- keep the candidates at or above the bound ---------------------------
-  if (!exotic) {
-    // candidates are rare (~1 %): one ballot per value slot, and only a warp
-    // that has some reserves places for them
-    const float tauf = S.tauf;
-    const unsigned below = (1u << lane) - 1u;
 #pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-      const bool keep = v[i] >= tauf;
-      const unsigned m = __ballot_sync(0xffffffffu, keep);
-      if (m) {
-        int wb = 0;
-        if (lane == 0) wb = atomicAdd(&S.nc, __popc(m));
-        wb = __shfl_sync(0xffffffffu, wb, 0);
-        const int pos = wb + __popc(m & below);
-        if (keep && pos < kCap) S.buf[pos] = composite(logit_key(v[i], dummy), index_of(i));
-      }
-    }
-  } else {
-    const uint32_t tau = S.tau;
-    int cnt = 0;
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) cnt += logit_key(v[i], dummy) >= tau ? 1 : 0;
-    int incl = cnt;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    int wbase = 0;
-    if (lane == 31) wbase = atomicAdd(&S.nc, incl);
-    wbase = __shfl_sync(0xffffffffu, wbase, 31);
-    int pos = wbase + incl - cnt;
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-      const uint32_t k = logit_key(v[i], dummy);
-      if (k >= tau) {
-        if (pos < kCap) S.buf[pos] = composite(k, index_of(i));
-        ++pos;
-      }
-    }
-  }
-  const int any_nonfinite = __syncthreads_or(nonfinite);
-  const int nc = S.nc;
-
-  u64 *dst = a.cand + ((size_t)b * a.rows_max + rloc) * (size_t)a.C * kMaxTopK +
-             (size_t)cx * kMaxTopK;
-  if (nc <= kThreads) {
-    // ---- usual case: one candidate per thread; its rank among the (distinct)
-    // candidates is its place in the descending top-ksel list
-    if (tid < nc) {
-      const u64 mine = S.buf[tid];
-      int rank = 0;
-      for (int j = 0; j < nc; ++j) rank += S.buf[j] > mine ? 1 : 0;
-      if (rank < ksel) dst[rank] = mine;
-    }
-    if (tid >= nc && tid < ksel) dst[tid] = 0;  // empty slots
-  } else {
-  // ---- exact top-ksel of the chunk -----------------------------------------
-  u64 thr;
-  if (nc <= kCap) {
-    thr = block_select_threshold(S, ksel, [&](auto f) {
-      for (int i = tid; i < nc; i += kThreads) f(S.buf[i]);
-    });
-    if (tid == 0) S.ntop = 0;
-    __syncthreads();
-    for (int i = tid; i < nc; i += kThreads) {
-      const u64 c = S.buf[i];
-      if (c >= thr) S.top[atomicAdd(&S.ntop, 1)] = c;
-    }
-  } else {  // many ties / a flat row: select over the whole chunk
-    // (rare) the logits are read again from L2, so that the values need not
-    // stay in registers through the selection
-    auto key_again = [&](int i) -> uint32_t {
-      const int e = (int)index_of(i);
-      return e < V ? logit_key(__ldcg(row + e), dummy) : 0u;
-    };
-    thr = block_select_threshold(S, ksel, [&](auto f) {
-#pragma unroll 4
       for (int i = 0; i < kPerThread; ++i) {
-        const uint32_t k = key_again(i);
-        if (k) f(composite(k, index_of(i)));
-      }
-    });
-    if (tid == 0) S.ntop = 0;
-    __syncthreads();
-#pragma unroll 4
-    for (int i = 0; i < kPerThread; ++i) {
-      const uint32_t k = key_again(i);
-      if (k) {
-        const u64 c = composite(k, index_of(i));
-        if (c >= thr) S.top[atomicAdd(&S.ntop, 1)] = c;
+        const int e = base + tid + kThreads * i;
+        v[i] = -INFINITY;
+        if (e < V) v[i] = __ldcs(row + e);
       }
     }
+    const int nf = chunk_select<CtaGeo>(S, v, row, V, base, a.vec != 0, ksel,
+                                        chunk_dst(a, b, rloc, cx), tid, CtaBarrier{}, 0,
+                                        [](int) {});
+    if (tid == 0 && nf) atomicOr(&a.rowflags[b * a.rows_max + rloc], SV_FLAG_NONFINITE_LOGIT);
   }
-  __syncthreads();
-  const int ntop = S.ntop;
-  // sort descending by rank (keys are distinct) and publish
-  u64 mine = 0;
-  int rank = 0;
-  if (tid < ntop) {
-    mine = S.top[tid];
-    for (int j = 0; j < ntop; ++j) rank += S.top[j] > mine ? 1 : 0;
-  }
-  if (tid < ntop) dst[rank] = mine;
-  else if (tid < ksel) dst[tid] = 0;  // empty slots
-  }
-  if (tid == 0 && any_nonfinite) atomicOr(&a.rowflags[b * a.rows_max + rloc], SV_FLAG_NONFINITE_LOGIT);
-  }  // chunk of logits
 
   // ---- the last CTA of this sequence finishes it ---------------------------
   // every thread's candidate stores precede thread 0's release (CTA barrier,
   // then a cumulative acq_rel add); the last CTA acquires the others' lists
   __syncthreads();
+  int last = 0;
   if (tid == 0) {
     int old;
     asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
                  : "=r"(old)
                  : "l"(&a.counters[b])
                  : "memory");
-    S.last = old == a.rows * a.C - 1;
+    last = old == a.rows * a.C - 1;
+  }
+  // the decision travels in the barrier's vote, not in shared memory, which
+  // the finish reuses from here on
+  if (!__syncthreads_or(last)) return;
+  finish_sequence(a, b, smem_raw);
+}
+
+// ---- streaming pair: every chunk of 16-byte-aligned logits rows, then one
+// finish CTA per sequence ------------------------------------------------------
+// A persistent CTA per SM takes chunks c = blockIdx.x + k * gridDim.x,
+// k = 0, 1, ... (sequence-major order), with two groups of kThreads threads
+// that select alternate chunks (k even, k odd), so that one group's
+// barriers and shuffles overlap the other's.  The chunks reach shared memory
+// through a ring of kStreamStages slots: chunk k takes slot k % kStreamStages
+// as one bulk copy of up to 64 KB that completes on the slot's mbarrier.  A
+// group moves a landed chunk to registers, and one of its threads refills the
+// slot with chunk k + kStreamStages right after the group's first barrier of
+// the selection.  Waits are bounded: a wait that runs out marks the device
+// error word, stops the refills, and the CTA runs out its chunks on -inf
+// (garbage lists, flagged) and, before returning, waits (bounded again) for
+// the copies still in flight.
+__device__ unsigned int g_accept_device_error;
+
+constexpr int kStreamGroups = 2;
+struct StreamCtl {
+  uint64_t full[kStreamStages];      // slot mbarriers
+  unsigned issued[kStreamStages];    // copies started per slot
+  unsigned consumed[kStreamStages];  // copies waited for per slot
+  int failed;                        // a wait ran out
+};
+constexpr size_t kStreamSmemBytes =
+    kStreamRingBytes + kStreamGroups * sizeof(StreamSmem) + sizeof(StreamCtl);
+static_assert(kStreamSmemBytes <= 227 * 1024, "the streaming CTA fits one SM's shared memory");
+
+constexpr int kStreamThreads = kStreamGroups * GroupGeo::kGT;
+
+__global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(const AcceptArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  float *ring = reinterpret_cast<float *>(smem_raw);
+  constexpr int kGT = GroupGeo::kGT, kPT = GroupGeo::kPT;
+  const int group = threadIdx.x / kGT, tid = threadIdx.x % kGT, warp = tid >> 5;
+  StreamSmem &S = reinterpret_cast<StreamSmem *>(smem_raw + kStreamRingBytes)[group];
+  StreamCtl &ctl = *reinterpret_cast<StreamCtl *>(smem_raw + kStreamRingBytes +
+                                                  kStreamGroups * sizeof(StreamSmem));
+  const GroupBarrier<kGT> bar{1 + group};
+  const int n_items = a.B * a.rows * a.C;
+  const int V = a.V;
+
+  // (an issuing thread) start the copy of the CTA's k-th chunk into its slot
+  auto issue = [&](int k) {
+    const int item = blockIdx.x + k * gridDim.x;
+    const int s = k % kStreamStages;
+    const int row_g = item / a.C, cx = item - row_g * a.C;
+    int b, rloc;
+    const float *row = chunk_row(a, row_g, b, rloc);
+    const int base = cx * kChunk;
+    const uint32_t bytes = (uint32_t)min(kChunk, V - base) * 4u;  // V % 4 == 0: a 16-multiple
+    ctl.issued[s] += 1;
+    mbar_arrive_expect_tx(&ctl.full[s], bytes);
+    bulk_copy_g2s(ring + (size_t)s * kChunk, row + base, bytes, &ctl.full[s]);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStreamStages; ++s) {
+      mbar_init(&ctl.full[s], 1);
+      ctl.issued[s] = 0;
+      ctl.consumed[s] = 0;
+    }
+    ctl.failed = 0;
+    fence_mbar_init();
+    for (int k = 0; k < kStreamStages; ++k)
+      if (blockIdx.x + k * gridDim.x < n_items) issue(k);
   }
   __syncthreads();
-  if (!S.last) return;
+  pdl_launch_dependents();  // the finish kernel may take SMs as this grid leaves them
 
-  // merge: one warp per row, rows in waves.  The chunk-phase buffers are dead
-  // from here on; this region aliases them.
-  u64 *merged = reinterpret_cast<u64 *>(smem_raw);              // [kMaxRows][kMaxTopK]
-  int *mcount = reinterpret_cast<int *>(merged + kMaxRows * kMaxTopK);
-  // each row's filtered distribution, built by the warp that merged it:
-  // entry j at [row][j] (j = lane + 32 h of RowDist), and its support size
-  float *dist_p = reinterpret_cast<float *>(mcount + kMaxRows + 1);  // [kMaxRows][64]
-  int *dist_id = reinterpret_cast<int *>(dist_p + kMaxRows * 64);    // [kMaxRows][64]
-  int *dist_n = dist_id + kMaxRows * 64;                             // [kMaxRows + 1]
-  u64 *stage = reinterpret_cast<u64 *>(dist_n + kMaxRows + 1);  // [wave][C*ksel] (8-aligned)
-  const int per_row = a.C * ksel;
-  for (int r0 = 0; r0 < a.rows; r0 += a.rows_per_wave) {
-    const int r = r0 + warp;
-    const bool active = warp < a.rows_per_wave && r < a.rows;
-    if (active) {
-      u64 *st = stage + (size_t)warp * per_row;
-      const u64 *src = a.cand + ((size_t)b * a.rows_max + r) * (size_t)a.C * kMaxTopK;
-      // the row's lists, kStageBatch loads per lane in flight before their
-      // shared-memory stores (a load issued after a store to a possibly
-      // aliasing address would wait for it: one round trip per element)
-      for (int i0 = 0; i0 < per_row; i0 += 32 * kStageBatch) {
-        u64 v[kStageBatch];
-#pragma unroll
-        for (int u = 0; u < kStageBatch; ++u) {
-          const int i = i0 + 32 * u + lane;
-          v[u] = i < per_row ? __ldcg(src + (i / ksel) * kMaxTopK + i % ksel) : 0ull;
-        }
-#pragma unroll
-        for (int u = 0; u < kStageBatch; ++u) {
-          const int i = i0 + 32 * u + lane;
-          if (i < per_row) st[i] = v[u];
-        }
-      }
-      __syncwarp();
-      int h0 = 0, h1 = 0;  // heads of lists lane and lane+32
-      int j = 0;
-      for (; j < ksel; ++j) {
-        const u64 v0 = (lane < a.C && h0 < ksel) ? st[lane * ksel + h0] : 0ull;
-        const u64 v1 = (lane + 32 < a.C && h1 < ksel) ? st[(lane + 32) * ksel + h1] : 0ull;
-        const u64 best = v0 > v1 ? v0 : v1;
-        const u64 g = warp_max_u64(best);
-        if (g == 0ull) break;
-        if (v0 == g) ++h0;
-        else if (v1 == g) ++h1;
-        if (lane == 0) merged[r * kMaxTopK + j] = g;
-      }
-      if (lane == 0) mcount[r] = j;
-      if (a.temperature != 0.f) {  // the distribution, while the other rows merge
-        __syncwarp();
-        const RowDist D = row_dist(merged + r * kMaxTopK, j, a.temperature, a.top_p);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          dist_p[r * 64 + lane + 32 * h] = D.p[h];
-          dist_id[r * 64 + lane + 32 * h] = D.id[h];
-        }
-        if (lane == 0) dist_n[r] = D.n;
+  // this group's chunk (sequence b, row rloc, chunk cx), advanced by
+  // kStreamGroups * gridDim.x chunks per step without divisions
+  const int C = a.C, rows = a.rows, K = a.K;
+  const int first = blockIdx.x + group * gridDim.x;
+  const int stride = kStreamGroups * gridDim.x;
+  int cx = first % C, b = (first / C) / rows, rloc = (first / C) % rows;
+  const int dcx = stride % C, drg = stride / C;
+  const int dq0 = drg / rows, dr0 = drg % rows, dq1 = (drg + 1) / rows, dr1 = (drg + 1) % rows;
+  constexpr int kIssuer = 32;  // a thread of the group's warp 1: warp 0 finds the bound meanwhile
+  for (int k = group;; k += kStreamGroups) {
+    const int item = blockIdx.x + k * gridDim.x;
+    if (item >= n_items) break;
+    if (k != group) {
+      cx += dcx;
+      const bool carry = cx >= C;
+      if (carry) cx -= C;
+      b += carry ? dq1 : dq0;
+      rloc += carry ? dr1 : dr0;
+      if (rloc >= rows) {
+        rloc -= rows;
+        ++b;
       }
     }
-    __syncthreads();
+    const int s = k % kStreamStages;
+    const float *row = rloc <= K ? a.tl + ((size_t)b * (K + 1) + rloc) * V
+                                 : a.dl + ((size_t)b * K + (rloc - K - 1)) * V;
+    const int base = cx * kChunk;
+    // warp 0 of the group waits for the slot, and a group barrier passes the
+    // landed bytes on to the rest
+    bool ok = true;
+    if (warp == 0 && !*(volatile int *)&ctl.failed) {
+      ok = mbar_wait(&ctl.full[s], (uint32_t)(k / kStreamStages) & 1u);
+      if (ok && tid == 0) ctl.consumed[s] += 1;
+    }
+    const int timeout = bar.sync_or(!ok);
+    const bool dead = timeout || *(volatile int *)&ctl.failed;
+    float v[kPT];
+    const float *slot = ring + (size_t)s * kChunk;
+    if (!dead && base + kChunk <= V) {  // a whole chunk (all but a row's last)
+#pragma unroll
+      for (int i = 0; i < kPT / 4; ++i) {
+        const float4 f = *reinterpret_cast<const float4 *>(slot + 4 * (tid + kGT * i));
+        v[4 * i + 0] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kPT / 4; ++i) {
+        const int el = 4 * (tid + kGT * i);
+        float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (!dead && base + el < V) f = *reinterpret_cast<const float4 *>(slot + el);
+        v[4 * i + 0] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+      }
+    }
+    const int nf = chunk_select<GroupGeo>(
+        S, v, row, V, base, true, a.ksel, chunk_dst(a, b, rloc, cx), tid, bar, timeout,
+        [&](int vote) {
+          // every thread of the group has read slot s: refill it
+          if (vote & 2) {
+            if (tid == 0) {
+              atomicOr(&g_accept_device_error, 1u);
+              *(volatile int *)&ctl.failed = 1;
+            }
+          } else if (tid == kIssuer && !*(volatile int *)&ctl.failed) {
+            if (blockIdx.x + (k + kStreamStages) * gridDim.x < n_items) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              issue(k + kStreamStages);
+            }
+          }
+        });
+    if (tid == 0 && nf) atomicOr(&a.rowflags[b * a.rows_max + rloc], SV_FLAG_NONFINITE_LOGIT);
   }
-  if (warp != 0) return;
+  // copies still in flight (only after a wait ran out) land before the CTA
+  // gives up its shared memory, or the bounded wait gives up again
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStreamStages; ++s)
+      for (unsigned c = ctl.consumed[s]; c < ctl.issued[s]; ++c)
+        if (!mbar_wait(&ctl.full[s], c & 1u)) break;
+  }
+}
 
-  // ---- acceptance for sequence b (one warp) ---------------------------------
-  float *sR = reinterpret_cast<float *>(stage);  // 64 floats
-  int *sId = reinterpret_cast<int *>(sR + 64);   // 64 ints
-  int flags = 0, nacc = 0;
-  int emitted = -2;  // -2: none yet
-  const bool greedy = a.temperature == 0.f;
-  int32_t *out = a.out + (size_t)b * (K + 1);
-  for (int j = lane; j <= K; j += 32) out[j] = -1;
-  // every position's inputs at once, lane j holding position j (K <= 8):
-  // draft token, uniform, and the flags of rows j (target) and K+1+j (draft);
-  // lane K the bonus row's flags
-  int d_l = 0, f_t = 0, f_d = 0;
-  float ua_l = 0.f;
-  if (lane < K) {
-    d_l = a.dt[(size_t)b * K + lane];
-    ua_l = a.ua[(size_t)b * K + lane];
-    f_t = __ldcg(&a.rowflags[b * a.rows_max + lane]);
-    if (!greedy) f_d = __ldcg(&a.rowflags[b * a.rows_max + K + 1 + lane]);
-  } else if (lane == K) {
-    f_t = __ldcg(&a.rowflags[b * a.rows_max + K]);
-  }
-  const float us_b = a.us[b];
-  __syncwarp();
-  int k = 0;
-  for (; k < K; ++k) {
-    const int d = __shfl_sync(0xffffffffu, d_l, k);
-    const bool d_ok = d >= 0 && d < V;
-    flags |= __shfl_sync(0xffffffffu, f_t, k);
-    if (greedy) {
-      const int am = mcount[k] > 0 ? composite_id(merged[k * kMaxTopK]) : -1;
-      if (!d_ok) flags |= SV_FLAG_DRAFT_OUT_OF_RANGE;
-      if (d_ok && am >= 0 && d == am) {
-        if (lane == 0) out[k] = d;
-        ++nacc;
-        continue;
-      }
-      emitted = am;
-      break;
-    }
-    flags |= __shfl_sync(0xffffffffu, f_d, k);
-    const RowDist P = stored_dist(dist_p, dist_id, dist_n, k);
-    const int qrow = K + 1 + k;
-    const RowDist Q = stored_dist(dist_p, dist_id, dist_n, qrow);
-    bool accept = false;
-    if (!d_ok) {
-      flags |= SV_FLAG_DRAFT_OUT_OF_RANGE;
-    } else {
-      const float qd = dist_lookup(Q, d);
-      if (qd == 0.f) {
-        flags |= SV_FLAG_DRAFT_ZERO_Q;
-      } else {
-        const float pd = dist_lookup(P, d);
-        accept = __shfl_sync(0xffffffffu, ua_l, k) < pd / qd;
-      }
-    }
-    if (accept) {
-      if (lane == 0) out[k] = d;
-      ++nacc;
-      continue;
-    }
-    // residual max(0, p - q) over p's support (q's entries read from the
-    // stored distribution, all lanes the same address: broadcast)
-    float R[2] = {P.p[0], P.p[1]};
-#pragma unroll 8
-    for (int src = 0; src < 64; ++src) {
-      const int qid = dist_id[qrow * 64 + src];
-      const float qp = dist_p[qrow * 64 + src];
-      if (qid >= 0 && qp > 0.f) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (P.id[h] == qid) R[h] = P.p[h] - qp;
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) R[h] = R[h] > 0.f ? R[h] : 0.f;
-    const float Z = warp_sum(R[0] + R[1]);
-    if (!(Z > 0.f)) {
-      R[0] = P.p[0];
-      R[1] = P.p[1];
-    }
-    emitted = inverse_cdf_by_id(P.id, R, us_b, sR, sId, dist_id + k * 64);
-    break;
-  }
-  if (emitted == -2) {  // all K accepted: bonus from position K+1
-    flags |= __shfl_sync(0xffffffffu, f_t, K);
-    if (greedy) {
-      emitted = mcount[K] > 0 ? composite_id(merged[K * kMaxTopK]) : -1;
-    } else {
-      const RowDist P = stored_dist(dist_p, dist_id, dist_n, K);
-      float R[2] = {P.p[0], P.p[1]};
-      emitted = inverse_cdf_by_id(P.id, R, us_b, sR, sId, dist_id + K * 64);
-    }
-  }
-  if (emitted < 0) flags |= SV_FLAG_EMPTY_DIST;
-  if (lane == 0) {
-    out[nacc] = emitted;
-    a.nacc[b] = nacc;
-    if (a.flags) a.flags[b] = flags;
-    a.counters[b] = 0;  // ready for the next call
-  }
-  for (int r = lane; r < a.rows_max; r += 32) a.rowflags[b * a.rows_max + r] = 0;
+// One CTA per sequence, after the stream kernel.
+__global__ void __launch_bounds__(kThreads, 1) accept_finish_kernel(const AcceptArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_wait();  // the lists and row flags are the stream kernel's output
+  finish_sequence(a, blockIdx.x, smem_raw);
 }
 
 }  // namespace
 
-unsigned take_device_error_accept() { return 0u; }  // no bounded waits in this unit
+unsigned take_device_error_accept() {
+  unsigned v = 0, zero = 0;
+  cudaMemcpyFromSymbol(&v, g_accept_device_error, sizeof v);
+  cudaMemcpyToSymbol(g_accept_device_error, &zero, sizeof zero);
+  return v;
+}
 
 }  // namespace sv
 
@@ -818,7 +1364,8 @@ sv_status accept_impl(const float *target_logits, const u64 *target_lists, int G
       return fail(SV_ERR_INVALID_ARG, "spec_accept_lists: target_lists must be 16-byte aligned");
   }
   const int C = target_lists ? lists_chunks(V, G) : (V + kChunk - 1) / kChunk;
-  static_assert(kListsPerChunk * kMaxTopK <= kCap, "a chunk's lists fit the candidate buffer");
+  static_assert(kListsPerChunk * kMaxTopK <= ChunkSmem::kSeg * CtaGeo::kGW,
+                "a chunk's lists fit the candidate buffer");
   const WsLayout W = ws_layout_c(B, K, (size_t)C);
   if (workspace_bytes < W.total)
     return fail(SV_ERR_INVALID_ARG, "spec_accept: workspace of %zu bytes, need %zu",
@@ -877,16 +1424,21 @@ sv_status accept_impl(const float *target_logits, const u64 *target_lists, int G
   const size_t per_row = (size_t)args.C * args.ksel * 8;
   args.rows_per_wave = (int)std::max<size_t>(
       1, std::min<size_t>({(size_t)args.rows, (size_t)kWarps, (size_t)(48 * 1024) / per_row}));
-  const size_t final_bytes = (size_t)kMaxRows * kMaxTopK * 8 + (kMaxRows + 1) * 4 +
-                             (size_t)kMaxRows * 64 * 8 + (kMaxRows + 1) * 4 +
-                             std::max<size_t>((size_t)args.rows_per_wave * per_row, 64 * 8);
+  const size_t final_bytes = finish_layout(args.rows_per_wave, per_row).total;
   const size_t smem = std::max(sizeof(ChunkSmem), final_bytes);
+  const size_t stream_smem = kStreamSmemBytes;
   static PerDeviceOnce attrs_once;
-  const cudaError_t ce = attrs_once.run([] {
+  const cudaError_t ce = attrs_once.run([stream_smem] {
     cudaError_t e = cudaFuncSetAttribute(spec_accept_kernel<2>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(spec_accept_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               160 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(accept_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)stream_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(accept_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                160 * 1024);
     return e;
   });
@@ -898,11 +1450,35 @@ sv_status accept_impl(const float *target_logits, const u64 *target_lists, int G
   if (cudaMemsetAsync(workspace, 0, W.cand, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return fail(SV_ERR_CUDA, "spec_accept: clearing the workspace counters failed: %s",
                 cudaGetErrorString(cudaGetLastError()));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!target_lists && args.vec) {
+    // aligned logits: the streaming kernel (a CTA per SM), then a finish CTA
+    // per sequence
+    const long long items = (long long)B * args.rows * args.C;
+    const int grid = (int)std::min<long long>(items, device_sm_count());
+    accept_stream_kernel<<<grid, kStreamThreads, stream_smem, st>>>(args);
+    const sv_status ls = check_launch("spec_accept (chunks)");
+    if (ls != SV_OK) return ls;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = final_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, accept_finish_kernel, args) != cudaSuccess)
+      return fail(SV_ERR_CUDA, "spec_accept (finish): launch failed: %s",
+                  cudaGetErrorString(cudaGetLastError()));
+    return check_launch("spec_accept (finish)");
+  }
   dim3 grid((unsigned)args.C, (unsigned)(B * args.rows));
   if (B >= kManySequences)
-    spec_accept_kernel<3><<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+    spec_accept_kernel<3><<<grid, kThreads, smem, st>>>(args);
   else
-    spec_accept_kernel<2><<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(args);
+    spec_accept_kernel<2><<<grid, kThreads, smem, st>>>(args);
   return check_launch("spec_accept");
 }
 
