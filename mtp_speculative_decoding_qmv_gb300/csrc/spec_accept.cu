@@ -847,19 +847,38 @@ __device__ void finish_sequence(const AcceptArgs &a, int b, uint8_t *smem) {
       // one list).
       u64 T = 0ull;
       int nnz = 0;  // nonzero keys of the subset
-      for (int e0 = 0; e0 < ns; e0 += 32) {
-        const int e = e0 + lane;
-        const u64 x = e < ns ? cb[e] : 0ull;
-        nnz += __popc(__ballot_sync(0xffffffffu, x != 0ull));
-        if (x != 0ull) {
-          int larger = 0;
-#pragma unroll 4
+      {
+        // every lane's keys of the subset (e = lane + 32 h, h < kH) compared
+        // in one pass over it, eight pairs in flight at a time
+        auto rank_subset = [&](auto kh_c) {
+          constexpr int kH = decltype(kh_c)::value;
+          u64 xs[kH];
+          int larger[kH];
+#pragma unroll
+          for (int h = 0; h < kH; ++h) {
+            const int e = lane + 32 * h;
+            xs[h] = e < ns ? cb[e] : 0ull;
+            larger[h] = 0;
+            nnz += __popc(__ballot_sync(0xffffffffu, xs[h] != 0ull));
+          }
+#pragma unroll 8
           for (int f = 0; f < ns; f += 2) {
             const ulonglong2 y = *reinterpret_cast<const ulonglong2 *>(cb + f);
-            larger += (y.x > x ? 1 : 0) + (y.y > x ? 1 : 0);
+#pragma unroll
+            for (int h = 0; h < kH; ++h) larger[h] += (y.x > xs[h] ? 1 : 0) + (y.y > xs[h] ? 1 : 0);
           }
-          if (larger < ksel) mr[larger] = x;
-          if (larger == ksel - 1) T = x;
+#pragma unroll
+          for (int h = 0; h < kH; ++h) {
+            if (xs[h] != 0ull && larger[h] < ksel) mr[larger[h]] = xs[h];
+            if (xs[h] != 0ull && larger[h] == ksel - 1) T = xs[h];
+          }
+        };
+        switch ((ns + 31) / 32) {  // ns < kMergeBuf = 256
+          case 1: rank_subset(std::integral_constant<int, 1>()); break;
+          case 2: rank_subset(std::integral_constant<int, 2>()); break;
+          case 3: rank_subset(std::integral_constant<int, 3>()); break;
+          case 4: rank_subset(std::integral_constant<int, 4>()); break;
+          default: rank_subset(std::integral_constant<int, kMergeBuf / 32>()); break;
         }
       }
       T = warp_max_u64(T);  // one lane holds it; 0 if nnz < ksel
@@ -1007,8 +1026,7 @@ __device__ void finish_sequence(const AcceptArgs &a, int b, uint8_t *smem) {
   // bonus), flags of every position it visits
   const unsigned rej = __ballot_sync(0xffffffffu, lane < K && pos_acc[lane] == 0);
   const int stop = rej ? __ffs(rej) - 1 : K;
-  int flags = lane <= stop ? pos_flags[lane] : 0;
-  for (int o = 16; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xffffffffu, flags, o);
+  int flags = (int)__reduce_or_sync(0xffffffffu, lane <= stop ? (unsigned)pos_flags[lane] : 0u);
   const int emitted = pos_emit[stop];
   if (emitted < 0) flags |= SV_FLAG_EMPTY_DIST;
   int32_t *out = a.out + (size_t)b * (K + 1);
