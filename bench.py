@@ -69,9 +69,9 @@ def measured_peaks():
 
 # DRAM bytes (read + written) per algorithmic byte of one qmv_plan launch,
 # from the ncu capture of the 4-layer weight-stream plan (bench.py --workload
-# stream --layers 4): 1.2921 GB of traffic for 1.2830 GB of algorithmic bytes.
+# stream --layers 4): 1.2924 GB of traffic for 1.2830 GB of algorithmic bytes.
 # Re-take it whenever the plan kernel changes.
-PLAN_TRAFFIC_RATIO = 1.292094 / 1.283004
+PLAN_TRAFFIC_RATIO = 1.292445 / 1.283004
 E_DRAWS = 16  # seeded draft/uniform draws the end-to-end steps rotate through
 
 
@@ -236,7 +236,9 @@ class Cycle:
             self._make_plans()
         self.qmv_launches = (len(self.plans) + (layers if layout == "plans" else 0)
                              if self.plans else len(self.qmv_calls))
-        self.launches_per_step = self.qmv_launches + layers + 2
+        # + the GatedDeltaNet captures, the replay, and spec_accept: a chunk
+        # kernel and a finish kernel on the logits, one kernel on fused lists
+        self.launches_per_step = self.qmv_launches + layers + 1 + (1 if self.fused_head else 2)
 
     def _make_plans(self):
         """Per layer: one plan for q, k, v and one for gate, up (projections
