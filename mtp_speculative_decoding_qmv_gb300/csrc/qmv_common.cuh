@@ -17,8 +17,10 @@
 //    streamed byte, about half the integer instructions.
 // Each consumer warp reduces one 64-group of a stage for 16-row MMA tiles:
 // the widened weights are A of mma.m16n8k16, the (<= 8) activation rows B;
-// per group D = -128 sum(x) + sum (128 + q) x (the offset is the first MMA's
-// accumulator) and acc += s * D + b * sum(x), sum(x) from an all-ones MMA.
+// per group D = sum (128 + q) x, and acc += s * D + (b - 128 s) * sum(x)
+// for packed stages; byte-expanded stages start D from -128 sum(x) (the
+// first MMA's accumulator input) and take acc += s * D + b * sum(x).
+// sum(x) comes from an all-ones MMA.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -173,74 +175,36 @@ __device__ __forceinline__ void b_fragments(const XRaw<kXF32> &r, uint32_t (&hi)
 }
 
 // One 64-group of one stage for the four 16-row tiles of a CTA:
-//   D = -128 sum(x) + sum_k (128 + q) x   (the offset enters as the first
-//                                          MMA's accumulator)
-//   acc[rt] += s * D + b * sum(x)
+//   acc[rt] += s * D + (b - 128 s) * sum(x)
 // `wbase` is the lane's ldmatrix address in the stage for tile 0; the
 // lane's scale of row g8 of tile rt is at sb + rt * sb_rt, of row g8+8 at
 // + sb_r8, and the biases at + sb_b.
-// The activation side of one 64-group: B fragments and the sum of x
-// (columns 2t, 2t+1; all-ones A operand).  Independent of the weights, so it
-// can be formed ahead of the stage it belongs to.
-template <bool kXF32>
-struct XFrag {
-  uint32_t hi[8], lo[8];
-  float xs0, xs1;
-};
-template <bool kXF32>
-__device__ __forceinline__ void prepare_x(XFrag<kXF32> &f, const XRaw<kXF32> &raw) {
-  b_fragments<kXF32>(raw, f.hi, f.lo);
-  float xs[4];
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks) {
-    if (ks == 0)
-      mma_bf16_zero(xs, kBf16One2, kBf16One2, kBf16One2, kBf16One2, f.hi[0], f.hi[1]);
-    else
-      mma_bf16_m16n8k16(xs, kBf16One2, kBf16One2, kBf16One2, kBf16One2, f.hi[2 * ks],
-                        f.hi[2 * ks + 1]);
-    if constexpr (kXF32)
-      mma_bf16_m16n8k16(xs, kBf16One2, kBf16One2, kBf16One2, kBf16One2, f.lo[2 * ks],
-                        f.lo[2 * ks + 1]);
-  }
-  f.xs0 = xs[0];
-  f.xs1 = xs[1];
-}
-
-template <bool kXF32>
-__device__ __forceinline__ void group_math_xf(float (&acc)[kTiles][4], uint32_t wbase,
-                                              const XFrag<kXF32> &xf, uint32_t sb, uint32_t sb_rt,
-                                              uint32_t sb_r8, uint32_t sb_b);
-
 template <bool kXF32>
 __device__ __forceinline__ void group_math(float (&acc)[kTiles][4], uint32_t wbase,
                                            const XRaw<kXF32> &xcur, uint32_t sb, uint32_t sb_rt,
                                            uint32_t sb_r8, uint32_t sb_b) {
-  XFrag<kXF32> xf;
-  prepare_x<kXF32>(xf, xcur);
-  group_math_xf<kXF32>(acc, wbase, xf, sb, sb_rt, sb_r8, sb_b);
-}
-
-// group_math with the activation side formed beforehand (prepare_x).
-template <bool kXF32>
-__device__ __forceinline__ void group_math_xf(float (&acc)[kTiles][4], uint32_t wbase,
-                                              const XFrag<kXF32> &xf, uint32_t sb, uint32_t sb_rt,
-                                              uint32_t sb_r8, uint32_t sb_b) {
-  const uint32_t(&hi)[8] = xf.hi;
-  const uint32_t(&lo)[8] = xf.lo;
-  const float xs[2] = {xf.xs0, xf.xs1};
+  uint32_t hi[8], lo[8];
+  b_fragments<kXF32>(xcur, hi, lo);
   // words t, 4+t of the group for rows g8 and g8+8 of each MMA tile
   uint32_t w[kTiles][4];
 #pragma unroll
   for (int rt = 0; rt < kTiles; ++rt) ldmatrix_x4(w[rt], wbase + rt * 16 * 128);
-  const float c0 = -128.f * xs[0], c1 = -128.f * xs[1];
   // four k16 steps; the tiles' accumulation chains are interleaved so that no
   // MMA waits on the one just issued
+  float xs[4];  // sum of x over the group, columns 2t, 2t+1
   float d[kTiles][4];
 #pragma unroll
   for (int ks = 0; ks < 4; ++ks) {
     const int wi = (ks >> 1) * 2;  // word t (ks 0,1) or 4+t (ks 2,3)
     const int sh = (ks & 1) * 8;   // nibbles j, j+4 for j = 0,1 or 2,3
     const uint32_t b0 = hi[2 * ks], b1 = hi[2 * ks + 1];
+    if (ks == 0)
+      mma_bf16_zero(xs, kBf16One2, kBf16One2, kBf16One2, kBf16One2, b0, b1);
+    else
+      mma_bf16_m16n8k16(xs, kBf16One2, kBf16One2, kBf16One2, kBf16One2, b0, b1);
+    if constexpr (kXF32)
+      mma_bf16_m16n8k16(xs, kBf16One2, kBf16One2, kBf16One2, kBf16One2, lo[2 * ks],
+                        lo[2 * ks + 1]);
 #pragma unroll
     for (int rt = 0; rt < kTiles; ++rt) {
       const uint32_t wr = w[rt][wi] >> sh, wr8 = w[rt][wi + 1] >> sh;
@@ -249,7 +213,7 @@ __device__ __forceinline__ void group_math_xf(float (&acc)[kTiles][4], uint32_t 
       const uint32_t p1 = and_or(wr >> 4, kNibbleMask, kBf16Base);
       const uint32_t p1r8 = and_or(wr8 >> 4, kNibbleMask, kBf16Base);
       if (ks == 0)
-        mma_bf16_c(d[rt], p0, p0r8, p1, p1r8, b0, b1, c0, c1);
+        mma_bf16_zero(d[rt], p0, p0r8, p1, p1r8, b0, b1);
       else
         mma_bf16_m16n8k16(d[rt], p0, p0r8, p1, p1r8, b0, b1);
       if constexpr (kXF32)
@@ -261,12 +225,12 @@ __device__ __forceinline__ void group_math_xf(float (&acc)[kTiles][4], uint32_t 
     const uint32_t p = sb + rt * sb_rt;
     const float s0 = bf16_bits_to_float(lds_u16(p));
     const float s1 = bf16_bits_to_float(lds_u16(p + sb_r8));
-    const float b0 = bf16_bits_to_float(lds_u16(p + sb_b));
-    const float b1 = bf16_bits_to_float(lds_u16(p + sb_b + sb_r8));
-    acc[rt][0] = fmaf(s0, d[rt][0], fmaf(b0, xs[0], acc[rt][0]));
-    acc[rt][1] = fmaf(s0, d[rt][1], fmaf(b0, xs[1], acc[rt][1]));
-    acc[rt][2] = fmaf(s1, d[rt][2], fmaf(b1, xs[0], acc[rt][2]));
-    acc[rt][3] = fmaf(s1, d[rt][3], fmaf(b1, xs[1], acc[rt][3]));
+    const float c0 = fmaf(-128.f, s0, bf16_bits_to_float(lds_u16(p + sb_b)));
+    const float c1 = fmaf(-128.f, s1, bf16_bits_to_float(lds_u16(p + sb_b + sb_r8)));
+    acc[rt][0] = fmaf(s0, d[rt][0], fmaf(c0, xs[0], acc[rt][0]));
+    acc[rt][1] = fmaf(s0, d[rt][1], fmaf(c0, xs[1], acc[rt][1]));
+    acc[rt][2] = fmaf(s1, d[rt][2], fmaf(c1, xs[0], acc[rt][2]));
+    acc[rt][3] = fmaf(s1, d[rt][3], fmaf(c1, xs[1], acc[rt][3]));
   }
 }
 
@@ -284,12 +248,16 @@ __device__ __forceinline__ void group_math_x2(float (&acc)[2][kTiles][4], uint32
 #pragma unroll
   for (int rt = 0; rt < kTiles; ++rt) ldmatrix_x4(w[rt], wbase + rt * 16 * 128);
   float xs[2][4];  // sum of x over the group per n-tile, columns 2t, 2t+1
+  float d[2][kTiles][4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  for (int ks = 0; ks < 4; ++ks) {
+    const int wi = (ks >> 1) * 2;
+    const int sh = (ks & 1) * 8;
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
+    for (int nt = 0; nt < 2; ++nt) {
       if (ks == 0)
-        mma_bf16_zero(xs[nt], kBf16One2, kBf16One2, kBf16One2, kBf16One2, hi[nt][0], hi[nt][1]);
+        mma_bf16_zero(xs[nt], kBf16One2, kBf16One2, kBf16One2, kBf16One2, hi[nt][2 * ks],
+                      hi[nt][2 * ks + 1]);
       else
         mma_bf16_m16n8k16(xs[nt], kBf16One2, kBf16One2, kBf16One2, kBf16One2, hi[nt][2 * ks],
                           hi[nt][2 * ks + 1]);
@@ -297,12 +265,6 @@ __device__ __forceinline__ void group_math_x2(float (&acc)[2][kTiles][4], uint32
         mma_bf16_m16n8k16(xs[nt], kBf16One2, kBf16One2, kBf16One2, kBf16One2, lo[nt][2 * ks],
                           lo[nt][2 * ks + 1]);
     }
-  }
-  float d[2][kTiles][4];
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks) {
-    const int wi = (ks >> 1) * 2;
-    const int sh = (ks & 1) * 8;
 #pragma unroll
     for (int rt = 0; rt < kTiles; ++rt) {
       const uint32_t wr = w[rt][wi] >> sh, wr8 = w[rt][wi + 1] >> sh;
@@ -313,8 +275,7 @@ __device__ __forceinline__ void group_math_x2(float (&acc)[2][kTiles][4], uint32
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         if (ks == 0)
-          mma_bf16_c(d[nt][rt], p0, p0r8, p1, p1r8, hi[nt][0], hi[nt][1], -128.f * xs[nt][0],
-                     -128.f * xs[nt][1]);
+          mma_bf16_zero(d[nt][rt], p0, p0r8, p1, p1r8, hi[nt][2 * ks], hi[nt][2 * ks + 1]);
         else
           mma_bf16_m16n8k16(d[nt][rt], p0, p0r8, p1, p1r8, hi[nt][2 * ks], hi[nt][2 * ks + 1]);
         if constexpr (kXF32)
@@ -327,14 +288,14 @@ __device__ __forceinline__ void group_math_x2(float (&acc)[2][kTiles][4], uint32
     const uint32_t p = sb + rt * sb_rt;
     const float s0 = bf16_bits_to_float(lds_u16(p));
     const float s1 = bf16_bits_to_float(lds_u16(p + sb_r8));
-    const float b0 = bf16_bits_to_float(lds_u16(p + sb_b));
-    const float b1 = bf16_bits_to_float(lds_u16(p + sb_b + sb_r8));
+    const float c0 = fmaf(-128.f, s0, bf16_bits_to_float(lds_u16(p + sb_b)));
+    const float c1 = fmaf(-128.f, s1, bf16_bits_to_float(lds_u16(p + sb_b + sb_r8)));
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      acc[nt][rt][0] = fmaf(s0, d[nt][rt][0], fmaf(b0, xs[nt][0], acc[nt][rt][0]));
-      acc[nt][rt][1] = fmaf(s0, d[nt][rt][1], fmaf(b0, xs[nt][1], acc[nt][rt][1]));
-      acc[nt][rt][2] = fmaf(s1, d[nt][rt][2], fmaf(b1, xs[nt][0], acc[nt][rt][2]));
-      acc[nt][rt][3] = fmaf(s1, d[nt][rt][3], fmaf(b1, xs[nt][1], acc[nt][rt][3]));
+      acc[nt][rt][0] = fmaf(s0, d[nt][rt][0], fmaf(c0, xs[nt][0], acc[nt][rt][0]));
+      acc[nt][rt][1] = fmaf(s0, d[nt][rt][1], fmaf(c0, xs[nt][1], acc[nt][rt][1]));
+      acc[nt][rt][2] = fmaf(s1, d[nt][rt][2], fmaf(c1, xs[nt][0], acc[nt][rt][2]));
+      acc[nt][rt][3] = fmaf(s1, d[nt][rt][3], fmaf(c1, xs[nt][1], acc[nt][rt][3]));
     }
   }
 }

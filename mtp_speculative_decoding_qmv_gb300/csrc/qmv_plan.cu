@@ -27,9 +27,8 @@
 //  * consumers read a phase's activations only after the device-wide count
 //    of finished tiles says every tile of the earlier phases has been
 //    written (one acquire load by one thread, bounded wait);
-//  * a tile whose stages fall in several CTAs' runs: every run stores its
-//    partial and counts it, and the run that counts last sums the partials
-//    in run order -- deterministic, and nobody waits on another CTA;
+//  * a tile whose stages fall in several CTAs' runs is reduced by the last of
+//    them to finish, summing the partials in run order -- deterministic;
 //  * counters are left at zero by the last CTA / last arriver, so the plan
 //    is ready for the next launch.
 // The per-group math (nibble widening, bf16 MMA, scale/bias epilogue) is the
@@ -275,7 +274,7 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init_u32(full0 + 8u * i, 1);
-      mbar_init_u32(empty0 + 8u * i, kConsumerWarps * 32);  // every consumer lane
+      mbar_init_u32(empty0 + 8u * i, kConsumerWarps);
     }
     mbar_init_u32(red_full, kConsumerWarps * 32);
     mbar_init_u32(red_empty, 32);
@@ -372,52 +371,46 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
         ++nseg;
         const PlanProblem &q = P.problems[s.p];
         const int N = q.N, n0 = s.tile * kRows;
-        // A split tile: every run stores its partial and counts it; the run
-        // that counts last sums all the partials in run order (the order,
-        // not who sums, fixes the result) and finishes the tile.  Nobody
-        // waits for another CTA.
+        // A split tile is summed by its first run (split 0): that CTA's run
+        // ends with the tile, so it reaches it last and the later runs,
+        // which start their CTAs' ranges with it, have usually published
+        // their partials already.  They store and count without waiting.
         bool write = true;
+        float4 *slots = nullptr;
         if (s.n_splits > 1) {
-          const float4 *slots = reinterpret_cast<const float4 *>(P.partials) +
-                                (size_t)s.tile_in_phase * max_splits * (kPartial / 4);
-          float4 *mine = reinterpret_cast<float4 *>(P.partials) +
-                         ((size_t)s.tile_in_phase * max_splits + s.split) * (kPartial / 4);
+          slots = reinterpret_cast<float4 *>(P.partials) +
+                  (size_t)s.tile_in_phase * max_splits * (kPartial / 4);
           int *count = &P.tile_count[s.tile_in_phase];
+          if (s.split > 0) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) __stcg(&mine[(lane + 32 * (i >> 1)) * 2 + (i & 1)], v[i]);
-          __syncwarp();
-          int last = 0;
-          // acq_rel: publishes this run's partial, and the last arriver sees
-          // every other run's
-          if (lane == 0) last = atom_add_acq_rel(count, 1) == s.n_splits - 1;
-          last = __shfl_sync(0xffffffffu, last, 0);
-          __syncwarp();  // the other lanes read after lane 0's acquire
-          if (!last) {
+            for (int i = 0; i < 4; ++i)
+              __stcg(&slots[(size_t)s.split * (kPartial / 4) + (lane + 32 * (i >> 1)) * 2 + (i & 1)],
+                     v[i]);
+            __syncwarp();
+            if (lane == 0) red_add_release(count, 1);  // publishes this run's partial
             write = false;
           } else {
-            const float4 own[4] = {v[0], v[1], v[2], v[3]};
+            if (lane == 0 && !wait_count(count, s.n_splits - 1))
+              atomicOr(&g_plan_device_error, 32u);
+            __syncwarp();  // the other lanes read after lane 0's acquire
+            // own partial first, then the later runs in run order
 #pragma unroll 1
-            for (int r = 0; r < s.n_splits; r += 2) {
+            for (int r = 1; r < s.n_splits; r += 2) {
               float4 a[4], b[4];
               const bool two = r + 1 < s.n_splits;
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const size_t o = (size_t)(lane + 32 * (i >> 1)) * 2 + (i & 1);
-                a[i] = r == s.split ? own[i] : __ldcg(&slots[(size_t)r * (kPartial / 4) + o]);
-                b[i] = !two ? make_float4(0.f, 0.f, 0.f, 0.f)
-                            : (r + 1 == s.split ? own[i]
-                                                : __ldcg(&slots[(size_t)(r + 1) * (kPartial / 4) + o]));
+                a[i] = __ldcg(&slots[(size_t)r * (kPartial / 4) + o]);
+                b[i] = two ? __ldcg(&slots[(size_t)(r + 1) * (kPartial / 4) + o])
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
               }
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                if (r == 0) {
-                  v[i] = a[i];
-                } else {
-                  v[i].x += a[i].x;
-                  v[i].y += a[i].y;
-                  v[i].z += a[i].z;
-                  v[i].w += a[i].w;
-                }
+                v[i].x += a[i].x;
+                v[i].y += a[i].y;
+                v[i].z += a[i].z;
+                v[i].w += a[i].w;
                 if (two) {
                   v[i].x += b[i].x;
                   v[i].y += b[i].y;
@@ -426,7 +419,6 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
                 }
               }
             }
-            if (lane == 0) *count = 0;  // every run has counted: ready for the next launch
           }
         }
         if (write) {
@@ -453,7 +445,10 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
             }
           }
           __syncwarp();
-          if (lane == 0 && signal) red_add_release(P.done_tiles, 1);
+          if (lane == 0) {
+            if (slots) P.tile_count[s.tile_in_phase] = 0;  // ready for the next launch
+            if (signal) red_add_release(P.done_tiles, 1);
+          }
         }
       }
     }
@@ -484,10 +479,8 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     const int i_end = runs.n;
     int i = 0;
     int cur_phase = -1;
-    // the activation side of the next stage to process (B fragments and
-    // sum of x), formed at the end of the stage before it
-    bool have_x = false;
-    XFrag<kXF32> xf;
+    bool have_x = false;  // xnext holds the first stage of segment i
+    XRaw<kXF32> xnext;
     PlanSeg s;
     if (i < i_end) s = runs[0];
     while (i < i_end) {
@@ -503,37 +496,35 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
         have_x = false;
       }
       const void *xrow = static_cast<const uint8_t *>(s.x) + (size_t)xm * s.K * xbytes;
-      if (!have_x) prepare_x<kXF32>(xf, load_x_l2<kXF32>(xrow, s.c0 * kConsumerWarps + gl, t));
+      if (!have_x) xnext = load_x_l2<kXF32>(xrow, s.c0 * kConsumerWarps + gl, t);
       // the next run, for the activation prefetch (same phase only)
       const bool have2 = i + 1 < i_end;
       PlanSeg s2 = s;
       if (have2) s2 = runs[i + 1];
       const bool same = have2 && s2.phase == s.phase;
-      const void *xrow2 = static_cast<const uint8_t *>(s2.x) + (size_t)xm * s2.K * xbytes;
       int g = s.c0 * kConsumerWarps + gl;
       for (int c = s.c0; c < s.c1; ++c, g += kConsumerWarps) {
-        // the next stage's activations fly during this stage's work
-        const bool more = c + 1 < s.c1;
-        const bool next = more || same;
-        XRaw<kXF32> xraw;
-        if (next)
-          xraw = load_x_l2<kXF32>(more ? xrow : xrow2,
-                                  more ? g + kConsumerWarps : s2.c0 * kConsumerWarps + gl, t);
+        const XRaw<kXF32> xcur = xnext;
+        if (c + 1 < s.c1)
+          xnext = load_x_l2<kXF32>(xrow, g + kConsumerWarps, t);
+        else if (same)
+          xnext = load_x_l2<kXF32>(static_cast<const uint8_t *>(s2.x) + (size_t)xm * s2.K * xbytes,
+                                   s2.c0 * kConsumerWarps + gl, t);
         if (ok && !warp_wait_stage(full0 + 8u * st, ph)) {
           ok = false;
           if (lane == 0) atomicOr(&g_plan_device_error, 2u);
         }
         if (ok) {
           const uint32_t stage = base + st * kStageBytesStream;
-          group_math_xf<kXF32>(acc, stage + ldm_off, xf, stage + sb_off, 16 * 16, 8 * 16,
-                               kRows * 16);
+          group_math<kXF32>(acc, stage + ldm_off, xcur, stage + sb_off, 16 * 16, 8 * 16,
+                            kRows * 16);
         }
-        mbar_arrive_u32(empty0 + 8u * st);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_u32(empty0 + 8u * st);
         if (++st == stages) {
           st = 0;
           ph ^= 1;
         }
-        if (next) prepare_x<kXF32>(xf, xraw);
       }
       // hand the run's sums to the epilogue warp: red[warp][row][col]
       if (nseg > 0 && !__all_sync(0xffffffffu, mbar_wait_u32(red_empty, (nseg - 1) & 1)) &&
