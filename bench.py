@@ -71,7 +71,7 @@ def measured_peaks():
 # from the ncu capture of the 4-layer weight-stream plan (bench.py --workload
 # stream --layers 4): 1.2924 GB of traffic for 1.2830 GB of algorithmic bytes.
 # Re-take it whenever the plan kernel changes.
-PLAN_TRAFFIC_RATIO = 1.292445 / 1.283004
+PLAN_TRAFFIC_RATIO = 1.292397 / 1.283004
 E_DRAWS = 16  # seeded draft/uniform draws the end-to-end steps rotate through
 
 
