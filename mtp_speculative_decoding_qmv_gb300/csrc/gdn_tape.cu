@@ -102,10 +102,12 @@ __device__ __forceinline__ float row_sum(float v) {
 // code (the decay a round-to-nearest multiply, the rank-1 term one fused
 // multiply-add), so replay still reproduces the capture bit for bit.
 // kT > 0: the token count is known at compile time (the token loop unrolls).
-// Two rows per thread (large batches) are held to 80 registers, six CTAs
-// per SM: 16 sequences x 48 heads take 3.4 waves of CTAs instead of 4.04.
+// Register budgets: two rows per thread (large batches) at 80 registers, six
+// CTAs per SM (16 sequences x 48 heads take 3.4 waves of CTAs instead of
+// 4.04); one row at 64, eight CTAs per SM (the verify cycle's batch 1: 0.5 %
+// more cycles/s than at 72).
 template <bool kFull, int kR, int kT>
-__global__ void __launch_bounds__(kThreads, kR == 2 ? 6 : 1) gdn_capture_kernel(const GdnArgs a) {
+__global__ void __launch_bounds__(kThreads, kR == 2 ? 6 : 8) gdn_capture_kernel(const GdnArgs a) {
   constexpr int kRows = kRowsPerCta * kR;
   const int T = kT > 0 ? kT : a.T;
   static_assert(kMaxT * (kRows / 4) <= kThreads, "one float4 of values per thread");
