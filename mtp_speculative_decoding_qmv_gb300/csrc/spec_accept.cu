@@ -171,7 +171,9 @@ struct ChunkSmemT {
   unsigned hist[256];
   uint32_t gmax[64];
   float gmaxf[64];
-  float scratch[G::kGW][kRowsT][G::kPT];  // candidate holders' values, per warp
+  // candidate holders' values, per warp; rows padded by 16 bytes so that the
+  // holders' simultaneous 16-byte stores fall in different banks
+  float scratch[G::kGW][kRowsT][G::kPT + 4];
   uint32_t tau;               // the bound, as a key (exotic chunks) or a float
   float tauf;
   alignas(16) int wcount[G::kGW];      // candidates each warp found
