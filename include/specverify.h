@@ -329,7 +329,9 @@ sv_status qmv_wide(const uint32_t *w_packed, const uint16_t *scales, const uint1
  * distribution with no finite logit is empty and emits -1.
  * Requires B >= 0 (0: no-op), B*(2K+1) <= 65535, 1 <= K <= 8,
  * 1 <= V <= 1048576, all pointers 4-byte aligned (16-byte aligned logits with
- * V % 4 == 0 use 16-byte loads); temperature finite and >= 0; if
+ * V % 4 == 0 are streamed through shared memory by bulk copies, and the
+ * call is then two kernel launches on `stream`: the chunk selection and a
+ * finish per sequence); temperature finite and >= 0; if
  * temperature > 0 then 1 <= top_k <= 64 and 0 < top_p <= 1.  No output may
  * overlap an input or another output.
  * workspace: device memory of spec_accept_workspace_bytes(B, K, V) bytes,
@@ -384,7 +386,7 @@ sv_status spec_accept_lists(const uint64_t *target_lists, int G, const float *dr
  * (cudaFree synchronises the device).
  * Arguments, outputs, flags and results are those of spec_accept without the
  * workspace pair; like every spec_accept call it clears the counter words
- * it needs on `stream` before the kernel, whatever shape the previous call
+ * it needs on `stream` before its kernels, whatever shape the previous call
  * on the scratch had.
  * Errors: SV_ERR_UNSUPPORTED when spec_accept_workspace_bytes(B, K, V)
  * exceeds the scratch size (nothing is launched; use spec_accept with a
