@@ -1157,10 +1157,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_accept_kernel(const
 
 // ---- streaming pair: every chunk of 16-byte-aligned logits rows, then one
 // finish CTA per sequence ------------------------------------------------------
-// A persistent CTA per SM takes chunks c = blockIdx.x + k * gridDim.x,
-// k = 0, 1, ... (sequence-major order), with two groups of kThreads threads
-// that select alternate chunks (k even, k odd), so that one group's
-// barriers and shuffles overlap the other's.  The chunks reach shared memory
+// A persistent CTA per SM runs two groups of kGT threads that select
+// alternate chunks of the CTA's sequence (k even, k odd), so that one group's
+// barriers and shuffles overlap the other's.  The work order lists every
+// row's whole chunks first (sequence-major) and the rows' shorter last chunks
+// after them; the 2G group slots (G = gridDim.x, slot p = CTA + G * group)
+// take it in rounds of 2G positions, slot p taking position p of even rounds
+// and 2G - 1 - p of odd ones, so that the slots that take a position more
+// take the shorter chunks.  A slot's positions grow from round to round, and
+// chunk k + kStreamStages of a CTA lies rounds after chunk k.  The chunks reach shared memory
 // through a ring of kStreamStages slots: chunk k takes slot k % kStreamStages
 // as one bulk copy of up to 64 KB that completes on the slot's mbarrier.  A
 // group moves a landed chunk to registers, and one of its threads refills the
@@ -1174,6 +1179,7 @@ __device__ unsigned int g_accept_device_error;
 constexpr int kStreamGroups = 2;
 struct StreamCtl {
   uint64_t full[kStreamStages];      // slot mbarriers
+  int4 item[kStreamStages];          // the slot's chunk: position, b, rloc, cx
   unsigned issued[kStreamStages];    // copies started per slot
   unsigned consumed[kStreamStages];  // copies waited for per slot
   int failed;                        // a wait ran out
@@ -1193,21 +1199,44 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(const 
   StreamCtl &ctl = *reinterpret_cast<StreamCtl *>(smem_raw + kStreamRingBytes +
                                                   kStreamGroups * sizeof(StreamSmem));
   const GroupBarrier<kGT> bar{1 + group};
-  const int n_items = a.B * a.rows * a.C;
-  const int V = a.V;
+  const int C = a.C, V = a.V, K = a.K;
+  const int n_items = a.B * a.rows * C;
+  const int n_full = a.B * a.rows * (C - 1);  // whole chunks (all of them when V % kChunk == 0)
+  const int G = gridDim.x;
+
+  // position of the CTA's k-th chunk in the work order
+  auto position = [&](int k) {
+    const int i = k >> 1, p = blockIdx.x + G * (k & 1);
+    return 2 * G * i + ((i & 1) ? 2 * G - 1 - p : p);
+  };
+  // the chunk at a position: sequence, row, chunk of the row
+  auto decode = [&](int pos) {
+    int row_g, cx;
+    if (pos < n_full) {
+      row_g = pos / (C - 1);
+      cx = pos - row_g * (C - 1);
+    } else {
+      row_g = pos - n_full;
+      cx = C - 1;
+    }
+    const int b = row_g / a.rows;
+    return make_int4(pos, b, row_g - b * a.rows, cx);
+  };
+  auto row_of = [&](int b, int rloc) {
+    return rloc <= K ? a.tl + ((size_t)b * (K + 1) + rloc) * V
+                     : a.dl + ((size_t)b * K + (rloc - K - 1)) * V;
+  };
 
   // (an issuing thread) start the copy of the CTA's k-th chunk into its slot
   auto issue = [&](int k) {
-    const int item = blockIdx.x + k * gridDim.x;
     const int s = k % kStreamStages;
-    const int row_g = item / a.C, cx = item - row_g * a.C;
-    int b, rloc;
-    const float *row = chunk_row(a, row_g, b, rloc);
-    const int base = cx * kChunk;
+    const int4 it = decode(position(k));
+    const int base = it.w * kChunk;
     const uint32_t bytes = (uint32_t)min(kChunk, V - base) * 4u;  // V % 4 == 0: a 16-multiple
+    ctl.item[s] = it;
     ctl.issued[s] += 1;
     mbar_arrive_expect_tx(&ctl.full[s], bytes);
-    bulk_copy_g2s(ring + (size_t)s * kChunk, row + base, bytes, &ctl.full[s]);
+    bulk_copy_g2s(ring + (size_t)s * kChunk, row_of(it.y, it.z) + base, bytes, &ctl.full[s]);
   };
 
   if (threadIdx.x == 0) {
@@ -1219,40 +1248,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(const 
     ctl.failed = 0;
     fence_mbar_init();
     for (int k = 0; k < kStreamStages; ++k)
-      if (blockIdx.x + k * gridDim.x < n_items) issue(k);
+      if (position(k) < n_items) issue(k);
   }
   __syncthreads();
   pdl_launch_dependents();  // the finish kernel may take SMs as this grid leaves them
 
-  // this group's chunk (sequence b, row rloc, chunk cx), advanced by
-  // kStreamGroups * gridDim.x chunks per step without divisions
-  const int C = a.C, rows = a.rows, K = a.K;
-  const int first = blockIdx.x + group * gridDim.x;
-  const int stride = kStreamGroups * gridDim.x;
-  int cx = first % C, b = (first / C) / rows, rloc = (first / C) % rows;
-  const int dcx = stride % C, drg = stride / C;
-  const int dq0 = drg / rows, dr0 = drg % rows, dq1 = (drg + 1) / rows, dr1 = (drg + 1) % rows;
   constexpr int kIssuer = 32;  // a thread of the group's warp 1: warp 0 finds the bound meanwhile
   for (int k = group;; k += kStreamGroups) {
-    const int item = blockIdx.x + k * gridDim.x;
-    if (item >= n_items) break;
-    if (k != group) {
-      cx += dcx;
-      const bool carry = cx >= C;
-      if (carry) cx -= C;
-      b += carry ? dq1 : dq0;
-      rloc += carry ? dr1 : dr0;
-      if (rloc >= rows) {
-        rloc -= rows;
-        ++b;
-      }
-    }
+    if (position(k) >= n_items) break;  // (the group's positions only grow)
     const int s = k % kStreamStages;
-    const float *row = rloc <= K ? a.tl + ((size_t)b * (K + 1) + rloc) * V
-                                 : a.dl + ((size_t)b * K + (rloc - K - 1)) * V;
-    const int base = cx * kChunk;
     // warp 0 of the group waits for the slot, and a group barrier passes the
-    // landed bytes on to the rest
+    // landed bytes (and the slot's chunk) on to the rest
     bool ok = true;
     if (warp == 0 && !*(volatile int *)&ctl.failed) {
       ok = mbar_wait(&ctl.full[s], (uint32_t)(k / kStreamStages) & 1u);
@@ -1260,6 +1266,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(const 
     }
     const int timeout = bar.sync_or(!ok);
     const bool dead = timeout || *(volatile int *)&ctl.failed;
+    // after a wait ran out the slot's record may never have been written:
+    // the chunk is decoded again (its lists are written, flagged garbage)
+    const int4 it = dead ? decode(position(k)) : ctl.item[s];
+    const int b = it.y, rloc = it.z, cx = it.w;
+    const float *row = row_of(b, rloc);
+    const int base = cx * kChunk;
     float v[kPT];
     const float *slot = ring + (size_t)s * kChunk;
     if (!dead && base + kChunk <= V) {  // a whole chunk (all but a row's last)
@@ -1293,7 +1305,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(const 
               *(volatile int *)&ctl.failed = 1;
             }
           } else if (tid == kIssuer && !*(volatile int *)&ctl.failed) {
-            if (blockIdx.x + (k + kStreamStages) * gridDim.x < n_items) {
+            if (position(k + kStreamStages) < n_items) {
               asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
               issue(k + kStreamStages);
             }
