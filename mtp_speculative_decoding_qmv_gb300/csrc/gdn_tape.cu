@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, kR == 2 ? 6 : 8) gdn_capture_kernel(
         acc0 = __ffma2_rn(S[r][m], kk[m], acc0);
         acc1 = __ffma2_rn(S[r][m + 1], kk[m + 1], acc1);
       }
-      u[r] = row_sum((acc0.x + acc0.y) + (acc1.x + acc1.y));
+      const float2 a2 = __fadd2_rn(acc0, acc1);
+      u[r] = row_sum(a2.x + a2.y);
     }
     // S_t = S' + e k^T (the keys' last use, so the queries take their
     // registers), then o = S_t q
@@ -243,20 +244,37 @@ __global__ void __launch_bounds__(kThreads, kR == 2 ? 6 : 8) gdn_capture_kernel(
       qq[2 * c] = make_float2(f.x, f.y);
       qq[2 * c + 1] = make_float2(f.z, f.w);
     }
+    float op[kR];  // the lane's partial of each row's output
 #pragma unroll
     for (int r = 0; r < kR; ++r) {
-      const int rr = rg + kRowsPerCta * r;
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < 2 * kChunks; m += 2) {
         acc0 = __ffma2_rn(S[r][m], qq[m], acc0);
         acc1 = __ffma2_rn(S[r][m + 1], qq[m + 1], acc1);
       }
-      const float o = row_sum((acc0.x + acc0.y) + (acc1.x + acc1.y));
-      if (j == 0 && r0 + rr < a.dv) {
-        e_out[kRowsPerCta * r] = ev[r];
-        if (o_out) o_out[kRowsPerCta * r] = o;
-      }
+      const float2 a2 = __fadd2_rn(acc0, acc1);
+      op[r] = a2.x + a2.y;
+    }
+    // The outputs leave the critical chain, so two rows share one butterfly:
+    // the row group's lanes first swap halves (even lanes keep row 0, odd
+    // lanes row 1), then every step adds the same row's partials -- the same
+    // additions in the same order as one row at a time.  Then one store per
+    // lane: the outputs from lanes 0 (row 0) and 1 (row 1), the records e
+    // from lanes 2 and 3 (one row: lane 0 the record, lane 1 the output).
+    if constexpr (kR == 2) {
+      const int rsel = j & 1;
+      float o = rsel ? op[1] : op[0];
+      o += __shfl_xor_sync(0xffffffffu, rsel ? op[0] : op[1], 1);
+      o += __shfl_xor_sync(0xffffffffu, o, 2);
+      o += __shfl_xor_sync(0xffffffffu, o, 4);
+      float *dst = j < 2 ? o_out : e_out;
+      const float val = j < 2 ? o : (rsel ? ev[1] : ev[0]);
+      if (j < 4 && dst && r0 + rg + kRowsPerCta * rsel < a.dv) dst[kRowsPerCta * rsel] = val;
+    } else {
+      const float o = row_sum(op[0]);
+      float *dst = j == 0 ? e_out : o_out;
+      if (j < 2 && dst && r0 + rg < a.dv) dst[0] = j == 0 ? ev[0] : o;
     }
     if (blockIdx.x == 0) {
       for (int c = tid; c < a.dk; c += kThreads) k_out[c] = ks[t][c];
