@@ -1236,7 +1236,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(const 
     ctl.item[s] = it;
     ctl.issued[s] += 1;
     mbar_arrive_expect_tx(&ctl.full[s], bytes);
-    bulk_copy_g2s(ring + (size_t)s * kChunk, row_of(it.y, it.z) + base, bytes, &ctl.full[s]);
+    // the logits are read once: evict-first in L2, so that the chunk lists
+    // written meanwhile stay there for the finish
+    bulk_copy_g2s_hint(ring + (size_t)s * kChunk, row_of(it.y, it.z) + base, bytes, &ctl.full[s],
+                       l2_policy_evict_first());
   };
 
   if (threadIdx.x == 0) {
