@@ -146,14 +146,29 @@ __global__ void __launch_bounds__(kThreads, kR == 2 ? 6 : 8) gdn_capture_kernel(
   {
     const int dk4 = a.dk / 4, nk4 = T * dk4;
     float4 kr[kStage4], qr[kStage4];
+    // float4 e = tid + u kThreads of the staged tokens is (t, c4) = (e / dk4,
+    // e % dk4); at full width (dk4 = 32, kThreads = 128) that is
+    // (tid / 32 + 4 u, tid % 32), one fixed stride per u
+    static_assert(kThreads == 4 * 32, "full-width staging: four tokens per pass");
+    const size_t tok_stride = (size_t)a.H * a.dk;  // floats from token t to t + 1
+    const size_t off0 = ((size_t)b * T * a.H + h) * a.dk;
 #pragma unroll
     for (int u = 0; u < kStage4; ++u) {
-      const int e = tid + u * kThreads;
-      if (e < nk4) {
-        const int t = e / dk4, c4 = e - t * dk4;
-        const size_t off = (((size_t)b * T + t) * a.H + h) * a.dk + 4 * c4;
-        kr[u] = __ldcg(reinterpret_cast<const float4 *>(a.k + off));
-        qr[u] = __ldcg(reinterpret_cast<const float4 *>(a.q + off));
+      if constexpr (kFull) {
+        const int t = (tid >> 5) + 4 * u;
+        if (t < T) {
+          const size_t off = off0 + t * tok_stride + 4 * (tid & 31);
+          kr[u] = __ldcg(reinterpret_cast<const float4 *>(a.k + off));
+          qr[u] = __ldcg(reinterpret_cast<const float4 *>(a.q + off));
+        }
+      } else {
+        const int e = tid + u * kThreads;
+        if (e < nk4) {
+          const int t = e / dk4, c4 = e - t * dk4;
+          const size_t off = off0 + t * tok_stride + 4 * c4;
+          kr[u] = __ldcg(reinterpret_cast<const float4 *>(a.k + off));
+          qr[u] = __ldcg(reinterpret_cast<const float4 *>(a.q + off));
+        }
       }
     }
     // this CTA's value rows per token as float4 (dv % 4 == 0, so a float4 is
@@ -172,11 +187,19 @@ __global__ void __launch_bounds__(kThreads, kR == 2 ? 6 : 8) gdn_capture_kernel(
     }
 #pragma unroll
     for (int u = 0; u < kStage4; ++u) {
-      const int e = tid + u * kThreads;
-      if (e < nk4) {
-        const int t = e / dk4, c4 = e - t * dk4;
-        *reinterpret_cast<float4 *>(&ks[t][4 * c4]) = kr[u];
-        *reinterpret_cast<float4 *>(&qs[t][4 * c4]) = qr[u];
+      if constexpr (kFull) {
+        const int t = (tid >> 5) + 4 * u;
+        if (t < T) {
+          *reinterpret_cast<float4 *>(&ks[t][4 * (tid & 31)]) = kr[u];
+          *reinterpret_cast<float4 *>(&qs[t][4 * (tid & 31)]) = qr[u];
+        }
+      } else {
+        const int e = tid + u * kThreads;
+        if (e < nk4) {
+          const int t = e / dk4, c4 = e - t * dk4;
+          *reinterpret_cast<float4 *>(&ks[t][4 * c4]) = kr[u];
+          *reinterpret_cast<float4 *>(&qs[t][4 * c4]) = qr[u];
+        }
       }
     }
     if (has_v) *reinterpret_cast<float4 *>(&vs[t_v][r_v]) = vr;
