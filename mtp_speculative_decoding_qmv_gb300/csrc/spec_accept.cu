@@ -1233,6 +1233,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(const 
     const int4 it = decode(position(k));
     const int base = it.w * kChunk;
     const uint32_t bytes = (uint32_t)min(kChunk, V - base) * 4u;  // V % 4 == 0: a 16-multiple
+    __threadfence_block();  // the slot's previous phase, seen complete, before the record
     ctl.item[s] = it;
     ctl.issued[s] += 1;
     mbar_arrive_expect_tx(&ctl.full[s], bytes);
@@ -1261,10 +1262,27 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(const 
     if (position(k) >= n_items) break;  // (the group's positions only grow)
     const int s = k % kStreamStages;
     // warp 0 of the group waits for the slot, and a group barrier passes the
-    // landed bytes (and the slot's chunk) on to the rest
+    // landed bytes (and the slot's chunk) on to the rest.  The slot's
+    // previous chunk belongs to the other group and its copy may still be
+    // landing (copies complete in any order); a parity wait for this chunk's
+    // phase would then match the phase before it.  So the wait starts once
+    // the slot's record names this chunk (the issuer writes it before
+    // starting the copy, after the previous chunk was read): the slot is
+    // then in this chunk's phase.
     bool ok = true;
     if (warp == 0 && !*(volatile int *)&ctl.failed) {
-      ok = mbar_wait(&ctl.full[s], (uint32_t)(k / kStreamStages) & 1u);
+      const int want = position(k);
+      const volatile int *rec = &ctl.item[s].x;
+      if (*rec != want) {
+        const unsigned long long t0 = global_timer_ns();
+        while (*rec != want)
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            ok = false;
+            break;
+          }
+      }
+      __threadfence_block();  // the record before the slot's barrier state
+      if (ok) ok = mbar_wait(&ctl.full[s], (uint32_t)(k / kStreamStages) & 1u);
       if (ok && tid == 0) ctl.consumed[s] += 1;
     }
     const int timeout = bar.sync_or(!ok);
