@@ -101,10 +101,13 @@ def test_shapes_and_settings(sv, oracle, K, T, top_k, top_p, V):
     assert near <= 3
 
 
-@pytest.mark.parametrize("T,top_k,top_p", [(0.6, 20, 0.95), (0.0, 0, 1.0)])
+@pytest.mark.parametrize("T,top_k,top_p", [(0.6, 20, 0.95), (0.0, 0, 1.0), (1.0, 64, 1.0)])
 def test_lm_head_config(sv, oracle, T, top_k, top_p):
     """vocab 151936, K=3, batch 32; draft = target + N(0, 0.5); logit scale
-    3.0 puts the per-position acceptance near 70 %."""
+    3.0 puts the per-position acceptance near 70 %.  top_k 64 at T 1 keeps
+    the widest filtered support: each chunk's bound comes from 64 thread
+    groups and many threads hold candidates, over the streaming kernel's
+    full ring of chunks."""
     r, gpu, near = _case(sv, oracle, 32, 3, 151936, T, top_k, top_p, 20, sigma=3.0, noise=0.5)
     assert near <= 2
     print(f"mean accepted {r['n_accepted'].mean():.2f} of 3, near ties {near}")
