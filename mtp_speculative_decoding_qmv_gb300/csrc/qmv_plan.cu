@@ -113,7 +113,9 @@ struct PlanParams {
 
 constexpr int kTopK = 64;        // keys kept per CTA and output row by the epilogue
 constexpr int kTopKRows = 8;     // M <= 8
-constexpr uint32_t kTopKBytes = kTopKRows * kTopK * 8 + kTopKRows * 4;
+// the lists, their flags, and one tile's keys for the merge
+constexpr uint32_t kTopKBytes = kTopKRows * kTopK * 8 + kTopKRows * 4 + 64 * 8;
+static_assert((kTopKRows * kTopK * 8 + kTopKRows * 4) % 16 == 0, "the tile keys, 16-byte aligned");
 
 struct PlanLayout {
   uint32_t ring, red, topk, bar, total;
@@ -144,11 +146,15 @@ __device__ __forceinline__ uint32_t topk_logit_key(float v, int &nonfinite) {
 }
 
 // One warp merges a tile's values of output row m (lane: rows n0 + lane and
-// n0 + lane + 32) into the descending list `list` [kTopK] (shared memory):
-// the values above the list's last key are inserted largest first, each by
-// counting the larger entries and shifting the rest down one place.
-__device__ void topk_merge_tile(unsigned long long *list, unsigned int *flag, float c0, float c1,
-                                int n0, int N) {
+// n0 + lane + 32) into the descending list `list` [kTopK] (shared memory).
+// Only values above the list's last key can enter.  Several of them are
+// placed at once: every key's place in the merged list is the number of
+// larger keys in the list and among the tile's values (keys are distinct:
+// one row each), counted against both in shared memory (`tile`, 64 keys),
+// and the keys whose place is below kTopK are written there.  A single one
+// is inserted by counting the larger entries and shifting the rest down.
+__device__ void topk_merge_tile(unsigned long long *list, unsigned long long *tile,
+                                unsigned int *flag, float c0, float c1, int n0, int N) {
   const int lane = threadIdx.x & 31;
   int nf = 0;
   const int r0 = n0 + lane, r1 = n0 + lane + 32;
@@ -161,6 +167,30 @@ __device__ void topk_merge_tile(unsigned long long *list, unsigned int *flag, fl
   unsigned long long thr = __shfl_sync(0xffffffffu, l1, 31);
   if (e0 <= thr) e0 = 0ull;
   if (e1 <= thr) e1 = 0ull;
+  const int entering = __popc(__ballot_sync(0xffffffffu, e0 != 0ull)) +
+                       __popc(__ballot_sync(0xffffffffu, e1 != 0ull));
+  if (entering > 1) {
+    tile[lane] = e0;
+    tile[lane + 32] = e1;
+    __syncwarp();
+    int p_e0 = 0, p_e1 = 0, p_l0 = lane, p_l1 = lane + 32;  // places in the merged list
+#pragma unroll 4
+    for (int j = 0; j < kTopK; j += 2) {
+      const ulonglong2 t = *reinterpret_cast<const ulonglong2 *>(tile + j);
+      const ulonglong2 l = *reinterpret_cast<const ulonglong2 *>(list + j);
+      p_e0 += (t.x > e0) + (t.y > e0) + (l.x > e0) + (l.y > e0);
+      p_e1 += (t.x > e1) + (t.y > e1) + (l.x > e1) + (l.y > e1);
+      p_l0 += (t.x > l0) + (t.y > l0);
+      p_l1 += (t.x > l1) + (t.y > l1);
+    }
+    __syncwarp();  // every read of the list before the first write
+    if (l0 != 0ull && p_l0 < kTopK) list[p_l0] = l0;
+    if (l1 != 0ull && p_l1 < kTopK) list[p_l1] = l1;
+    if (e0 != 0ull && p_e0 < kTopK) list[p_e0] = e0;
+    if (e1 != 0ull && p_e1 < kTopK) list[p_e1] = e1;
+    __syncwarp();
+    return;
+  }
   while (__any_sync(0xffffffffu, (e0 | e1) != 0ull)) {
     const unsigned long long g = warp_max_u64(e0 > e1 ? e0 : e1);
     const int pos = __popc(__ballot_sync(0xffffffffu, l0 > g)) +
@@ -335,6 +365,8 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
     // the top-64 lists of this CTA (empty = key 0) and their non-finite flags
     unsigned long long *tk_list = reinterpret_cast<unsigned long long *>(smem + L.topk);
     unsigned int *tk_flag = reinterpret_cast<unsigned int *>(tk_list + kTopKRows * kTopK);
+    unsigned long long *tk_tile =
+        reinterpret_cast<unsigned long long *>(tk_flag + kTopKRows);  // 16-byte aligned
     if (P.topk) {
       for (int i = lane; i < kTopKRows * kTopK; i += 32) tk_list[i] = 0ull;
       if (lane < kTopKRows) tk_flag[lane] = 0u;
@@ -429,7 +461,8 @@ __global__ void __launch_bounds__(kPlanThreads, kPlanCtasPerSm)
 #pragma unroll
             for (int col = 0; col < 8; ++col)
               if (col < P.M)
-                topk_merge_tile(tk_list + col * kTopK, tk_flag + col, c0[col], c1[col], n0, N);
+                topk_merge_tile(tk_list + col * kTopK, tk_tile, tk_flag + col, c0[col], c1[col],
+                                n0, N);
           } else {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
