@@ -69,9 +69,9 @@ def measured_peaks():
 
 # DRAM bytes (read + written) per algorithmic byte of one qmv_plan launch,
 # from the ncu capture of the 4-layer weight-stream plan (bench.py --workload
-# stream --layers 4): 1.2924 GB of traffic for 1.2830 GB of algorithmic bytes.
+# stream --layers 4): 1.2925 GB of traffic for 1.2830 GB of algorithmic bytes.
 # Re-take it whenever the plan kernel changes.
-PLAN_TRAFFIC_RATIO = 1.292397 / 1.283004
+PLAN_TRAFFIC_RATIO = 1.292530 / 1.283004
 E_DRAWS = 16  # seeded draft/uniform draws the end-to-end steps rotate through
 
 
