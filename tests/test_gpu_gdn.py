@@ -46,7 +46,8 @@ def _capture(sv, x, T=None, state_out=True):
 
 
 @pytest.mark.parametrize("B,T,H,dk,dv", [(16, 5, 48, 128, 128), (2, 3, 3, 64, 64),
-                                         (3, 7, 2, 32, 96), (1, 1, 1, 128, 4), (2, 16, 1, 8, 128)])
+                                         (3, 7, 2, 32, 96), (1, 1, 1, 128, 4), (2, 16, 1, 8, 128),
+                                         (2, 12, 3, 128, 128), (1, 16, 2, 128, 64)])
 def test_capture_and_replay_match_the_oracle(sv, oracle, B, T, H, dk, dv):
     x = wl.gdn_inputs(B * 100 + T, B, T, H, dk, dv)
     out_ref, tape_ref = oracle.gdn_capture(x["state0"], x["q"], x["k"], x["v"], x["alpha"],
